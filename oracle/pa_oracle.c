@@ -1,0 +1,353 @@
+/*
+ * pa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * The plain, slow, fp64 CPU oracle for paged-attention decode.  Only the
+ * tests, the smoke check and the CPU-baseline leg of the benchmark load it;
+ * the product library never does, and the two share no code, header, table
+ * or helper.  Every loop below is the textbook definition written out, with
+ * no blocking, fusion or reordering beyond what the definition states.
+ *
+ * Passages followed (project_6, commit cd0d9e1 "qwen3_6_scripts"):
+ *   [gather]   "_forward_prefix_pytorch: Pre-gather ALL context K/V":
+ *              key_cache[blk_ids] -- a sequence's logical block j lives in
+ *              the physical block block_tables[s][j] of the cache.
+ *   [v1/v2]    "forward_decode: V2 enabled via original heuristic": V1 runs
+ *              the whole KV range in one pass, V2 splits it; both compute the
+ *              same attention output for the one decode query.
+ *   [phase 1]  "V2: splits into PARTITION_SIZE=512 chunks ... Phase 1:
+ *              Per-partition attention -- for each (seq, head, partition):
+ *              QK^T, softmax, weighted V sum; store tmp_output, exp_sums,
+ *              max_logits".
+ *   [phase 2]  "Phase 2: Cross-partition reduction (log-sum-exp)": the global
+ *              max over partitions, a per-partition rescale of
+ *              exp(partition max - global max) times the partition exp-sum,
+ *              and the output as the rescale-weighted sum of the partition
+ *              outputs divided by the total.
+ *
+ * Readings where the pages are silent (each one is listed in the design
+ * notes): query head h reads KV head h / (Hq/Hkv); max_logits are maxima of
+ * the *scaled* logits scale*q.k; exp_sums are taken relative to the
+ * partition's own max; tmp_output is normalised by its own exp_sum (this is
+ * what makes the phase-2 rescale by the exp_sum correct); the partition
+ * count is ceil(L/P); a sequence with L = 0 produces a zero output.
+ *
+ * Layouts (all row-major, element offsets):
+ *   query        [S][Hq][d]                 16-bit float bit patterns
+ *   key/value    [num_blocks][bs][Hkv][d]   16-bit float bit patterns
+ *   block_tables [S][max_blocks]            int32
+ *   seq_lens     [S]                        int32
+ *   out          [S][Hq][d]                 double
+ *   tmp_out      [S][Hq][NP][d]             double
+ *   exp_sums, max_logits [S][Hq][NP]        double
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F16 0
+#define ORACLE_BF16 1
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARGS (-1)
+#define ORACLE_BAD_TABLE (-2)
+#define ORACLE_NO_MEMORY (-3)
+
+/* Exact widening of one IEEE binary16 or bfloat16 bit pattern to double. */
+double oracle_half_bits_to_f64(uint16_t h, int dtype)
+{
+    if (dtype == ORACLE_BF16) {
+        /* bfloat16 is the top half of an IEEE binary32 word. */
+        uint32_t w = ((uint32_t)h) << 16;
+        float f;
+        memcpy(&f, &w, sizeof f);
+        return (double)f;
+    }
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);              /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x400), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+void oracle_bits_to_f64(const uint16_t *in, double *out, int64_t n, int dtype)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_half_bits_to_f64(in[i], dtype);
+}
+
+/* Offset of element (block, row, kv head, dim) in a cache. */
+static int64_t cache_off(int64_t b, int o, int kvh, int i, int bs, int Hkv, int d)
+{
+    return ((b * bs + o) * (int64_t)Hkv + kvh) * d + i;
+}
+
+/* Physical block holding token t of sequence s, or -1 if the table entry is
+ * outside the cache. [gather] */
+static int64_t phys_block(const int32_t *bt, int s, int t, int bs, int max_blocks,
+                          int num_blocks)
+{
+    int64_t b = bt[(int64_t)s * max_blocks + t / bs];
+    if (b < 0 || b >= num_blocks)
+        return -1;
+    return b;
+}
+
+static int check_lengths(const int32_t *seq_lens, int S, int bs, int max_blocks)
+{
+    for (int s = 0; s < S; ++s)
+        if (seq_lens[s] < 0 || (int64_t)seq_lens[s] > (int64_t)max_blocks * bs)
+            return ORACLE_BAD_ARGS;
+    return ORACLE_OK;
+}
+
+static int check_dims(int S, int Hq, int Hkv, int d, int bs, int num_blocks,
+                      int max_blocks)
+{
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || bs <= 0 || num_blocks < 0 ||
+        max_blocks < 0 || Hq % Hkv != 0)
+        return ORACLE_BAD_ARGS;
+    return ORACLE_OK;
+}
+
+/* x[t - t0] = scale * sum_i q[s][h][i] * k_t[i] for t in [t0, t1), and the
+ * query row widened once into qd[d]. */
+static int scaled_logits(double *x, double *qd, const uint16_t *q, const uint16_t *kc,
+                         const int32_t *bt, int s, int h, int kvh, int t0, int t1,
+                         int Hq, int Hkv, int d, int bs, int num_blocks, int max_blocks,
+                         double scale, int dtype)
+{
+    for (int i = 0; i < d; ++i)
+        qd[i] = oracle_half_bits_to_f64(q[((int64_t)s * Hq + h) * d + i], dtype);
+    for (int t = t0; t < t1; ++t) {
+        int64_t b = phys_block(bt, s, t, bs, max_blocks, num_blocks);
+        if (b < 0)
+            return ORACLE_BAD_TABLE;
+        int64_t base = cache_off(b, t % bs, kvh, 0, bs, Hkv, d);
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i)
+            acc += qd[i] * oracle_half_bits_to_f64(kc[base + i], dtype);
+        x[t - t0] = scale * acc;
+    }
+    return ORACLE_OK;
+}
+
+/* Softmax-weighted V sum over tokens [t0, t1) given their logits x:
+ *   m = max x,  l = sum exp(x - m),  o = sum exp(x - m) v_t / l.          */
+static void softmax_v(double *o, double *m_out, double *l_out, const double *x,
+                      const uint16_t *vc, const int32_t *bt, int s, int kvh, int t0,
+                      int t1, int Hkv, int d, int bs, int num_blocks, int max_blocks,
+                      int dtype)
+{
+    double m = -INFINITY;
+    for (int t = t0; t < t1; ++t)
+        if (x[t - t0] > m)
+            m = x[t - t0];
+    double l = 0.0;
+    for (int i = 0; i < d; ++i)
+        o[i] = 0.0;
+    for (int t = t0; t < t1; ++t) {
+        double p = exp(x[t - t0] - m);
+        l += p;
+        int64_t b = phys_block(bt, s, t, bs, max_blocks, num_blocks);
+        int64_t base = cache_off(b, t % bs, kvh, 0, bs, Hkv, d);
+        for (int i = 0; i < d; ++i)
+            o[i] += p * oracle_half_bits_to_f64(vc[base + i], dtype);
+    }
+    for (int i = 0; i < d; ++i)
+        o[i] /= l;
+    *m_out = m;
+    *l_out = l;
+}
+
+/*
+ * Single-pass decode [v1/v2]: for every sequence s and query head h,
+ *   out[s][h] = softmax_t(scale * q[s][h] . k_t) weighted sum of v_t,
+ * t over the sequence's L = seq_lens[s] tokens, K/V read through the table.
+ */
+int oracle_attention(double *out, const uint16_t *q, const uint16_t *kc,
+                     const uint16_t *vc, const int32_t *bt, const int32_t *seq_lens,
+                     int S, int Hq, int Hkv, int d, int bs, int num_blocks,
+                     int max_blocks, float scale, int dtype)
+{
+    int rc = check_dims(S, Hq, Hkv, d, bs, num_blocks, max_blocks);
+    if (rc == ORACLE_OK)
+        rc = check_lengths(seq_lens, S, bs, max_blocks);
+    if (rc != ORACLE_OK)
+        return rc;
+    int g = Hq / Hkv;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < (int64_t)S * Hq; ++u) {
+        int s = (int)(u / Hq), h = (int)(u % Hq);
+        int L = seq_lens[s];
+        double *o = out + u * d;
+        if (L == 0) {
+            for (int i = 0; i < d; ++i)
+                o[i] = 0.0;
+            continue;
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)L);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!x || !qd) {
+            free(x);
+            free(qd);
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+            continue;
+        }
+        int kvh = h / g;
+        int r = scaled_logits(x, qd, q, kc, bt, s, h, kvh, 0, L, Hq, Hkv, d, bs,
+                              num_blocks, max_blocks, (double)scale, dtype);
+        if (r == ORACLE_OK) {
+            double m, l;
+            softmax_v(o, &m, &l, x, vc, bt, s, kvh, 0, L, Hkv, d, bs, num_blocks,
+                      max_blocks, dtype);
+        } else {
+#pragma omp atomic write
+            status = r;
+        }
+        free(x);
+        free(qd);
+    }
+    return status;
+}
+
+/*
+ * Phase 1 [phase 1]: for each partition p < ceil(L/P) of tokens
+ * [p*P, min((p+1)*P, L)):
+ *   max_logits[s][h][p] = m_p = max of the scaled logits,
+ *   exp_sums[s][h][p]   = l_p = sum exp(x_t - m_p),
+ *   tmp_out[s][h][p]    = sum exp(x_t - m_p) v_t / l_p.
+ * Slots p >= ceil(L/P) are left as the caller filled them.
+ */
+int oracle_partials(double *tmp_out, double *exp_sums, double *max_logits,
+                    const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
+                    const int32_t *bt, const int32_t *seq_lens, int S, int Hq, int Hkv,
+                    int d, int bs, int num_blocks, int max_blocks, float scale,
+                    int P, int NP, int dtype)
+{
+    int rc = check_dims(S, Hq, Hkv, d, bs, num_blocks, max_blocks);
+    if (rc == ORACLE_OK)
+        rc = check_lengths(seq_lens, S, bs, max_blocks);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (P <= 0 || NP < 0)
+        return ORACLE_BAD_ARGS;
+    for (int s = 0; s < S; ++s)
+        if ((seq_lens[s] + (int64_t)P - 1) / P > NP)
+            return ORACLE_BAD_ARGS;
+    int g = Hq / Hkv;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < (int64_t)S * Hq; ++u) {
+        int s = (int)(u / Hq), h = (int)(u % Hq);
+        int L = seq_lens[s];
+        int n = (int)((L + (int64_t)P - 1) / P);
+        int kvh = h / g;
+        double *x = (double *)malloc(sizeof(double) * (size_t)P);
+        double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!x || !qd) {
+            free(x);
+            free(qd);
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+            continue;
+        }
+        for (int p = 0; p < n; ++p) {
+            int t0 = p * P;
+            int t1 = (t0 + P < L) ? t0 + P : L;
+            int r = scaled_logits(x, qd, q, kc, bt, s, h, kvh, t0, t1, Hq, Hkv, d, bs,
+                                  num_blocks, max_blocks, (double)scale, dtype);
+            if (r != ORACLE_OK) {
+#pragma omp atomic write
+                status = r;
+                break;
+            }
+            int64_t slot = u * NP + p;
+            softmax_v(tmp_out + slot * d, &max_logits[slot], &exp_sums[slot], x, vc,
+                      bt, s, kvh, t0, t1, Hkv, d, bs, num_blocks, max_blocks, dtype);
+        }
+        free(x);
+        free(qd);
+    }
+    return status;
+}
+
+/*
+ * Phase 2 [phase 2]: with n = ceil(L/P) partitions,
+ *   M = max_p m_p,  w_p = exp(m_p - M) * l_p,
+ *   out = sum_p (w_p / sum_q w_q) * tmp_out_p.
+ * A sequence with no partition (L = 0) gets a zero output.
+ */
+int oracle_lse_merge(double *out, const double *tmp_out, const double *exp_sums,
+                     const double *max_logits, const int32_t *seq_lens, int S, int Hq,
+                     int d, int P, int NP)
+{
+    if (S < 0 || Hq <= 0 || d <= 0 || P <= 0 || NP < 0)
+        return ORACLE_BAD_ARGS;
+    for (int s = 0; s < S; ++s)
+        if (seq_lens[s] < 0 || (seq_lens[s] + (int64_t)P - 1) / P > NP)
+            return ORACLE_BAD_ARGS;
+    for (int64_t u = 0; u < (int64_t)S * Hq; ++u) {
+        int s = (int)(u / Hq);
+        int n = (int)((seq_lens[s] + (int64_t)P - 1) / P);
+        double *o = out + u * d;
+        for (int i = 0; i < d; ++i)
+            o[i] = 0.0;
+        if (n == 0)
+            continue;
+        double M = -INFINITY;
+        for (int p = 0; p < n; ++p)
+            if (max_logits[u * NP + p] > M)
+                M = max_logits[u * NP + p];
+        double total = 0.0;
+        for (int p = 0; p < n; ++p) {
+            double w = exp(max_logits[u * NP + p] - M) * exp_sums[u * NP + p];
+            total += w;
+            for (int i = 0; i < d; ++i)
+                o[i] += w * tmp_out[(u * NP + p) * d + i];
+        }
+        for (int i = 0; i < d; ++i)
+            o[i] /= total;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * [gather]: dense copies k_dense[s][t][kvh][:] = key_cache[b][t % bs][kvh][:]
+ * with b = block_tables[s][t / bs], for t < L; rows t >= L are untouched.
+ * Bit patterns are copied unchanged.
+ */
+int oracle_gather(uint16_t *k_dense, uint16_t *v_dense, const uint16_t *kc,
+                  const uint16_t *vc, const int32_t *bt, const int32_t *seq_lens, int S,
+                  int Hkv, int d, int bs, int num_blocks, int max_blocks, int max_len)
+{
+    int rc = check_dims(S, Hkv, Hkv, d, bs, num_blocks, max_blocks);
+    if (rc == ORACLE_OK)
+        rc = check_lengths(seq_lens, S, bs, max_blocks);
+    if (rc != ORACLE_OK)
+        return rc;
+    for (int s = 0; s < S; ++s) {
+        if (seq_lens[s] > max_len)
+            return ORACLE_BAD_ARGS;
+        for (int t = 0; t < seq_lens[s]; ++t) {
+            int64_t b = phys_block(bt, s, t, bs, max_blocks, num_blocks);
+            if (b < 0)
+                return ORACLE_BAD_TABLE;
+            for (int kvh = 0; kvh < Hkv; ++kvh) {
+                int64_t src = cache_off(b, t % bs, kvh, 0, bs, Hkv, d);
+                int64_t dst = (((int64_t)s * max_len + t) * Hkv + kvh) * d;
+                memcpy(k_dense + dst, kc + src, sizeof(uint16_t) * (size_t)d);
+                memcpy(v_dense + dst, vc + src, sizeof(uint16_t) * (size_t)d);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
