@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention decode step on GB300; prints one JSON line.
+
+A step is one pass of the whole decode path over one batch: the work list /
+V1-V2 choice, the paged K/V walk, QK^T, online softmax, PV, the partition
+epilogue and the log-sum-exp reduce.  The default workload is the mixed
+serving batch (256 sequences, lengths log-uniform in [128, 65536], 24 query /
+4 KV heads, head_dim 128, block 16, bf16; sequences <= 8192 tokens single
+pass, longer ones split into 512-token partitions), the one workload whose
+step runs every stage of the path.  ``--workload N`` selects another.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise; every step is timed with CUDA events on the stream
+the kernels are launched on, with a 2x-L2 buffer write between steps (the
+KV inputs are also far larger than L2).  The attention kernel alone is timed
+the same way (events between its launch and its neighbours') for the
+roofline.  ``e2e`` repeats the step through ``pa_decode_auto`` (the one call a
+user makes) with the per-step inputs copied from pinned host memory and the
+output read back, inside the timed region.  ``cpu_baseline`` times the fp64
+oracle on a bounded sample of the same workload on the host cores.
+
+``--impl reference`` times the oracle alone (the reference arm) on the same
+workload, metric and unit.  Multi-GPU (torchrun): every rank runs its own
+replica of the workload (no collective on the data path); time is the max
+over ranks and the value is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-read GB/s and % of GB300 HBM peak; decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--partition-size", type=int, default=None,
+                    help="override the workload's (first) partition size")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target oracle CPU time of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--check", action="store_true",
+                    help="also compare sampled sequences of the output with the oracle")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def kv_bytes(case) -> int:
+    w = case.workload
+    return case.total_tokens * 2 * w.num_kv_heads * w.head_dim * 2
+
+
+def qo_bytes(case) -> int:
+    w = case.workload
+    return 2 * case.num_seqs * w.num_q_heads * w.head_dim * 2
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_decode_partitioned_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "pa_decode.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def committed_traffic(wid: int, partition_size: int):
+    """DRAM bytes per attention-kernel launch from the committed ncu summary, or None
+    if the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(f"workload{wid}_P{partition_size}")
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.gpu = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[1].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + parts[1].split(".")[1]) if "." in parts[1] else 0.0
+                    rows.append({"t": ts + frac, "sm": float(parts[2]), "max": float(parts[3]),
+                                 "reasons": {"hw_slowdown": parts[6], "hw_thermal_slowdown":
+                                             parts[7], "sw_thermal_slowdown": parts[8],
+                                             "sw_power_cap": parts[9]}})
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summary(rows, t0, t1):
+        inside = [r for r in rows if t0 <= r["t"] <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [r for r in rows if r["t"] <= t1]
+            window = "warm-up + timed region (timed region shorter than 3 samples)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no samples (nvidia-smi unavailable)"}
+        reasons = sorted({k for r in inside for k, v in r["reasons"].items() if v == "Active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["max"] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def host_subcase(case, seq_ids):
+    """Host copies (query, caches, tables, lengths) of some sequences of a case.
+
+    The blocks those sequences reference are copied into a compact host pool
+    and their table rows relabelled to it; the result of the attention does
+    not depend on which physical block holds a page."""
+    import torch
+    ids = torch.as_tensor(seq_ids, dtype=torch.long)
+    bs = case.key_cache.shape[1]
+    lens = [case.seq_lens_list[i] for i in seq_ids]
+    bt = case.block_tables.cpu()[ids]
+    need = [-(-L // bs) for L in lens]
+    used = torch.cat([bt[j, :n] for j, n in enumerate(need)] + [torch.zeros(0, dtype=torch.int32)])
+    uniq, inv = torch.unique(used.long(), return_inverse=True)
+    idx = uniq.to(case.key_cache.device)
+    kc = case.key_cache.index_select(0, idx).cpu()
+    vc = case.value_cache.index_select(0, idx).cpu()
+    nbt = torch.full((len(seq_ids), max(need + [1])), -1, dtype=torch.int32)
+    off = 0
+    for j, n in enumerate(need):
+        nbt[j, :n] = inv[off:off + n].to(torch.int32)
+        off += n
+    q = case.query.index_select(0, ids.to(case.query.device)).cpu()
+    return q, kc, vc, nbt, torch.tensor(lens, dtype=torch.int32)
+
+
+def oracle_sample_plan(case, target_seconds: float, seed: int = 0):
+    """Pick a sample of sequences whose oracle time is about target_seconds.
+
+    A calibration run on a few short sequences gives the oracle's rate in
+    (token x query head) per second on this host."""
+    import numpy as np
+    import oracle
+    w = case.workload
+    order = list(np.random.default_rng(seed).permutation(case.num_seqs))
+    calib, tok = [], 0
+    for i in sorted(order, key=lambda i: case.seq_lens_list[i]):
+        calib.append(int(i))
+        tok += case.seq_lens_list[i]
+        if tok >= 4096:
+            break
+    q, kc, vc, bt, sl = host_subcase(case, calib)
+    t = time.perf_counter()
+    oracle.attention(q, kc, vc, bt, sl, w.scale)
+    rate = max(1.0, tok * w.num_q_heads / max(time.perf_counter() - t, 1e-6))
+    budget = target_seconds * rate / w.num_q_heads   # tokens
+    sample, tok = [], 0
+    for i in order:
+        L = case.seq_lens_list[i]
+        if sample and tok + L > budget:
+            continue
+        sample.append(int(i))
+        tok += L
+        if tok >= budget:
+            break
+    return sorted(sample), tok
+
+
+def time_oracle(case, sample):
+    import oracle
+    w = case.workload
+    q, kc, vc, bt, sl = host_subcase(case, sample)
+    t = time.perf_counter()
+    oracle.attention(q, kc, vc, bt, sl, w.scale)
+    return time.perf_counter() - t
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def make_inputs(wid, device):
+    from workloads import WORKLOADS, make_case
+    return make_case(WORKLOADS[wid], device=device)
+
+
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores (the reference arm)."""
+    import torch
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = make_inputs(args.workload, dev)
+    w = case.workload
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    sample, tok = oracle_sample_plan(case, per_step)
+    kvb = tok * 2 * w.num_kv_heads * w.head_dim * 2
+    for _ in range(args.warmup):
+        time_oracle(case, sample)
+    times = [time_oracle(case, sample) for _ in range(args.steps)]
+    mean = sum(times) / len(times)
+    value = kvb / mean / 1e9
+    threads = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": case.num_seqs,
+                   "seq_len": case.max_seq_len, "parallelism": "host threads (OpenMP)"},
+        "decode_tokens_per_s": round(len(sample) / mean, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{len(sample)} of {case.num_seqs} sequences, {tok} tokens "
+                                   f"per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.steps < 1 or args.warmup < 3:
+        raise SystemExit("need --steps >= 1 and --warmup >= 3")
+
+    import torch
+    import torch.distributed as dist
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    from paged_kv_decode_partitioned_gb300 import build as pa_build
+    if rank == 0:
+        pa_build.build()
+    barrier()
+    pa_build.build()
+    import paged_kv_decode_partitioned_gb300 as pa
+    from paged_kv_decode_partitioned_gb300.step import DecodeStep
+
+    case = make_inputs(args.workload, "cuda")
+    w = case.workload
+    P = args.partition_size or w.partition_sizes[0]
+    step = DecodeStep(w.mode, case.query, case.key_cache, case.value_cache, case.block_tables,
+                      case.seq_lens, w.scale, max_seq_len=case.max_seq_len, partition_size=P,
+                      single_pass_max_len=w.single_pass_max_len)
+    launches = step.launches()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device="cuda")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if pa.device_status() != 0:
+        raise SystemExit("device status flags raised during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+          for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        for j, (_, fn) in enumerate(launches):
+            fn()
+            ev[k][j + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    rows = sampler.stop()
+
+    attn_idx = [name for name, _ in launches].index("attention")
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
+    attn_ms = [ev[k][attn_idx].elapsed_time(ev[k][attn_idx + 1]) for k in range(K)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    kvb = kv_bytes(case)
+    value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    tok_s = world * case.num_seqs / (ms_per_step * 1e-3)
+    peak, peak_src = measured_peaks()
+    alg = kvb + qo_bytes(case)
+    attn_mean_ms = sum(attn_ms) / K
+    achieved = alg / (attn_mean_ms * 1e-3) / 1e9
+
+    # end to end through pa_decode_auto / the public calls with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = case.query.cpu().pin_memory()
+        hbt = case.block_tables.cpu().pin_memory()
+        hsl = case.seq_lens.cpu().pin_memory()
+        hout = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+        h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hsl.numel() * 4
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            case.query.copy_(hq, non_blocking=True)
+            case.block_tables.copy_(hbt, non_blocking=True)
+            case.seq_lens.copy_(hsl, non_blocking=True)
+            step()
+            hout.copy_(step.out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        barrier()
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            e0[k].record(stream)
+            e2e_step()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(e0[k].elapsed_time(e1[k]) for k in range(K))
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(world * kvb / (e2e_ms / K * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "kv_cache": "resident in HBM (decode state); per-step inputs copied"}
+
+    check = None
+    if args.check and rank == 0:
+        import numpy as np
+        import oracle
+        torch.cuda.synchronize()
+        ids = sorted({int(np.argmax(case.seq_lens_list)), int(np.argmin(case.seq_lens_list)), 0})
+        q, kc, vc, bt, sl = host_subcase(case, ids)
+        ref = oracle.attention(q, kc, vc, bt, sl, w.scale)
+        got = step.out.index_select(0, torch.as_tensor(ids, device="cuda")).float().cpu().double()
+        err = (got.numpy() - ref)
+        ok = bool((abs(err) <= 1e-2 + 1e-2 * abs(ref)).all())
+        check = {"seqs": ids, "max_abs_err": float(abs(err).max()), "pass": ok}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sample, tok = oracle_sample_plan(case, args.cpu_seconds)
+        secs = time_oracle(case, sample)
+        skv = tok * 2 * w.num_kv_heads * w.head_dim * 2
+        cpu = {"value": round(skv / secs / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(),
+               "kind": "oracle",
+               "sample": f"{len(sample)} of {case.num_seqs} sequences ({tok} tokens) of the "
+                         f"same workload, {secs:.1f} s"}
+
+    if rank != 0:
+        return
+    clocks = ClockSampler.summary(rows, t_wall0, t_wall1)
+    traffic = committed_traffic(args.workload, P)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if w.dtype.__repr__().endswith("bfloat16") else "f16", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": world * case.num_seqs,
+                   "seq_len": case.max_seq_len, "total_tokens": case.total_tokens,
+                   "mode": w.mode, "partition_size": P,
+                   "single_pass_max_len": w.single_pass_max_len,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{flush.numel() >> 20} MiB buffer written between steps; "
+                         f"K/V inputs {kvb / 2**30:.2f} GiB > L2"},
+        "decode_tokens_per_s": round(tok_s, 1),
+        "hbm_frac_kv": round(value / world / peak, 4),
+        "hbm_frac_kvqo": round((alg / (ms_per_step * 1e-3) / 1e9) / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": step.attention_kernel,
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg,
+                     "attention_ms_per_launch": round(attn_mean_ms, 4),
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * len(launches),
+        "clocks": clocks,
+    }
+    if check is not None:
+        line["check"] = check
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-attention decode library
+ * (libpadecode.so).
+ *
+ * The operation (project_6, commit cd0d9e1 "qwen3_6_scripts"):
+ *   One query token per sequence attends over that sequence's keys and
+ *   values, which live in a block-paged cache: logical block j of sequence s
+ *   is the physical block block_tables[s][j] ("_forward_prefix_pytorch:
+ *   Pre-gather ALL context K/V": key_cache[blk_ids]).  The result is
+ *       out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) * v_t,
+ *   t over the sequence's seq_lens[s] tokens.  "forward_decode: V2 enabled via
+ *   original heuristic" runs short sequences in one pass (V1) and long ones
+ *   split into PARTITION_SIZE-token partitions (V2): "Phase 1: Per-partition
+ *   attention" stores a partial output, max logit and exp-sum per partition,
+ *   and "Phase 2: Cross-partition reduction (log-sum-exp)" merges them.
+ *
+ * Conventions shared by every entry point:
+ *   - All array pointers are DEVICE pointers, owned by the caller, dense and
+ *     row-major in the layouts given below.  The library allocates no device
+ *     memory and keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and run on the current CUDA device.  Every argument is
+ *     checked on the host before anything is launched; a call that returns an
+ *     error has launched nothing (except PA_ERR_CUDA, which reports a failed
+ *     launch).
+ *   - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - dtype selects IEEE binary16 (PA_F16) or bfloat16 (PA_BF16) for query,
+ *     caches and out.  Accumulation is fp32.  Partials are fp32.
+ *   - Supported shapes: head_dim in {64, 128, 256}; block_size a multiple of
+ *     16; num_q_heads / num_kv_heads between 1 and 8.  Other shapes return
+ *     PA_ERR_UNSUPPORTED.
+ *   - Alignment: caches, query, out and partial buffers 16-byte aligned
+ *     (PA_ERR_MISALIGNED otherwise).
+ *   - block_tables contents and seq_lens values are read on the device only.
+ *     A table entry outside [0, num_blocks) reads zeros (never memory outside
+ *     the cache) and a length above max_blocks_per_seq * block_size is
+ *     clamped; both raise a flag that pa_device_status() reports.
+ *
+ * Layouts:
+ *   query        [num_seqs][num_q_heads][head_dim]
+ *   key_cache    [num_blocks][block_size][num_kv_heads][head_dim]
+ *   value_cache  [num_blocks][block_size][num_kv_heads][head_dim]
+ *   block_tables int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens     int32 [num_seqs]
+ *   out          [num_seqs][num_q_heads][head_dim]
+ *   tmp_out      fp32 [num_seqs][num_q_heads][max_num_partitions][head_dim]
+ *   exp_sums, max_logits  fp32 [num_seqs][num_q_heads][max_num_partitions]
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype_t;
+
+/* Status codes returned by every int-valued entry point. */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARGUMENT = -1,   /* null pointer, negative or inconsistent size */
+    PA_ERR_UNSUPPORTED = -2,        /* head_dim / block_size / GQA group not supported */
+    PA_ERR_MISALIGNED = -3,         /* a pointer is not 16-byte aligned */
+    PA_ERR_WORKSPACE_TOO_SMALL = -4,/* workspace_bytes below what the call needs */
+    PA_ERR_CUDA = -5,               /* a CUDA runtime / driver call or launch failed */
+    PA_ERR_DEVICE = -6,             /* pa_device_status: the device raised a flag */
+    PA_ERR_NO_DEVICE = -7           /* no usable CUDA device / TMA entry point */
+};
+
+/* Flags that kernels raise in the device status word (pa_device_status). */
+enum {
+    PA_DEV_BAD_BLOCK = 1,           /* a block-table entry outside [0, num_blocks) */
+    PA_DEV_LEN_CLAMPED = 2,         /* seq_len > max_blocks_per_seq*block_size or < 0 */
+    PA_DEV_WAIT_TIMEOUT = 4,        /* a pipeline wait gave up; that output is not written */
+    PA_DEV_TOO_MANY_PARTITIONS = 8  /* ceil(seq_len/partition_size) > max_num_partitions */
+};
+
+/*
+ * pa_decode -- single-pass decode (V1: the whole KV range of a sequence in
+ * one launch, no partial results in global memory).
+ *   out[s][h][:] = softmax(scale * q[s][h] . k_t) weighted sum of v_t over
+ *   t < seq_lens[s]; a sequence with seq_len 0 gets zeros.
+ * scale: the logit scale (usually 1/sqrt(head_dim)).
+ */
+PA_API int pa_decode(void *out, const void *query, const void *key_cache,
+              const void *value_cache, const int32_t *block_tables,
+              const int32_t *seq_lens, int num_seqs, int num_q_heads,
+              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+              int max_blocks_per_seq, float scale, pa_dtype_t dtype, void *stream);
+
+/*
+ * pa_decode_partitioned -- phase 1 of the split-KV decode ("Phase 1:
+ * Per-partition attention"; "V2: splits into PARTITION_SIZE=512 chunks").
+ * For partition p < ceil(seq_lens[s] / partition_size) covering tokens
+ * [p*P, min((p+1)*P, L)) and every query head h:
+ *   max_logits[s][h][p] = m_p = max_t scale * q.k_t
+ *   exp_sums[s][h][p]   = l_p = sum_t exp(scale * q.k_t - m_p)
+ *   tmp_out[s][h][p][:] = sum_t exp(scale * q.k_t - m_p) v_t / l_p
+ * Slots p >= ceil(L/P) are not written.  partition_size must be a positive
+ * multiple of block_size; max_num_partitions >= ceil(max seq_len / P) (a
+ * sequence with more partitions raises PA_DEV_TOO_MANY_PARTITIONS and has
+ * only its first max_num_partitions written).
+ */
+PA_API int pa_decode_partitioned(float *tmp_out, float *exp_sums, float *max_logits,
+                          const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, int max_blocks_per_seq, float scale,
+                          int partition_size, int max_num_partitions,
+                          pa_dtype_t dtype, void *stream);
+
+/*
+ * pa_partition_reduce -- phase 2 ("Phase 2: Cross-partition reduction
+ * (log-sum-exp)").  With n = ceil(seq_lens[s] / partition_size):
+ *   M = max_p m_p,  w_p = exp(m_p - M) * l_p,
+ *   out[s][h][:] = sum_{p<n} w_p * tmp_out[s][h][p][:] / sum_{p<n} w_p
+ * rounded to dtype; n = 0 gives zeros.  Reads only slots p < n.
+ */
+PA_API int pa_partition_reduce(void *out, const float *tmp_out, const float *exp_sums,
+                        const float *max_logits, const int32_t *seq_lens,
+                        int num_seqs, int num_q_heads, int head_dim,
+                        int partition_size, int max_num_partitions,
+                        pa_dtype_t dtype, void *stream);
+
+/*
+ * pa_default_single_pass_max_len -- the launch heuristic's threshold.
+ * Sequences longer than the returned length are partitioned by
+ * pa_decode_auto.  It is the pages' 8192 ("seq_len > 8192 -> V2 (partitioned,
+ * better parallelism); seq_len <= 8192 -> V1") when num_seqs * num_kv_heads
+ * single-pass units fill every SM of the device at least twice, and
+ * partition_size otherwise (too few units: split everything longer than one
+ * partition so the SMs have work).  num_sms <= 0 queries the current device.
+ */
+PA_API int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int partition_size,
+                                   int num_sms);
+
+/*
+ * pa_auto_workspace_bytes -- device workspace pa_decode_auto needs (bytes),
+ * for at most `max_seq_len` tokens per sequence.  Returns 0 on bad
+ * arguments.  single_pass_max_len < 0 selects the heuristic above.
+ */
+PA_API size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                               int head_dim, int max_seq_len, int single_pass_max_len,
+                               int partition_size);
+
+/*
+ * pa_decode_auto -- the whole decode step with a per-sequence choice of path
+ * ("forward_decode: V2 enabled via original heuristic").  A sequence with
+ * seq_len <= single_pass_max_len is computed in one pass and written to out
+ * directly; a longer one is split into ceil(L/partition_size) partitions whose
+ * partials (kept in `workspace`) are merged by the log-sum-exp reduce.  The
+ * device builds the work list from seq_lens, so the host needs only the upper
+ * bound `max_seq_len` (every seq_len must be <= it; a longer one raises
+ * PA_DEV_TOO_MANY_PARTITIONS).  single_pass_max_len < 0 selects
+ * pa_default_single_pass_max_len.  workspace: device memory of at least
+ * pa_auto_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller;
+ * its contents need no initialisation and are scratch after the call.
+ * Launches three kernels (plan, attention, reduce) on `stream`.
+ */
+PA_API int pa_decode_auto(void *out, const void *query, const void *key_cache,
+                   const void *value_cache, const int32_t *block_tables,
+                   const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   int max_blocks_per_seq, float scale, int max_seq_len,
+                   int single_pass_max_len, int partition_size, void *workspace,
+                   size_t workspace_bytes, pa_dtype_t dtype, void *stream);
+
+/* Phases of pa_decode_auto_phases (bit mask). */
+enum { PA_PHASE_PLAN = 1, PA_PHASE_ATTEND = 2, PA_PHASE_REDUCE = 4 };
+
+/*
+ * pa_decode_auto_phases -- pa_decode_auto split into its three launches so
+ * a caller can order other stream work (events, copies) between them:
+ * PA_PHASE_PLAN builds the work list in `workspace` from seq_lens;
+ * PA_PHASE_ATTEND runs the attention kernel over it (single-pass sequences
+ * write `out`, partitioned ones write their partials to `workspace`);
+ * PA_PHASE_REDUCE merges the partials into `out`.  All arguments must be the
+ * same for the phases of one step and the phases must run in this order on
+ * one stream.  phases = PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE is
+ * exactly pa_decode_auto.  Other masks return PA_ERR_INVALID_ARGUMENT.
+ */
+PA_API int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
+                                 const void *value_cache, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, int max_blocks_per_seq, float scale,
+                                 int max_seq_len, int single_pass_max_len,
+                                 int partition_size, void *workspace, size_t workspace_bytes,
+                                 pa_dtype_t dtype, void *stream, int phases);
+
+/*
+ * pa_gather_kv -- test entry: copies each sequence's K and V rows, fetched
+ * through the block table with the same tile loader the attention kernels
+ * use, into dense arrays k_dense/v_dense [num_seqs][max_len][num_kv_heads]
+ * [head_dim] (rows t < seq_lens[s]; rows t >= seq_len are not written).  Bit
+ * patterns are copied unchanged, so the result can be compared bit for bit.
+ */
+PA_API int pa_gather_kv(void *k_dense, void *v_dense, const void *key_cache,
+                 const void *value_cache, const int32_t *block_tables,
+                 const int32_t *seq_lens, int num_seqs, int num_kv_heads,
+                 int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                 int max_len, pa_dtype_t dtype, void *stream);
+
+/*
+ * pa_device_status -- synchronises `stream`, returns in *flags the PA_DEV_*
+ * flags raised by kernels on the current device since the last call, and
+ * clears them.  Returns PA_OK, or PA_ERR_CUDA if synchronisation failed.
+ */
+PA_API int pa_device_status(void *stream, int *flags);
+
+/* Human-readable name of a status code (static string). */
+PA_API const char *pa_status_string(int status);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

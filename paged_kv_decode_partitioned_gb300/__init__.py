@@ -1,0 +1,278 @@
+"""Paged-attention decode for GB300 (sm_103a): the Python binding of libpadecode.so.
+
+Every function here only marshals arguments (torch tensors -> device pointers,
+the current CUDA stream) and calls the C ABI declared in ``include/pa_decode.h``;
+all of the computation runs in the library's CUDA kernels.  There is no other
+code path: if the compiled library is missing, importing a function raises.
+
+The operation (project_6, commit cd0d9e1 "qwen3_6_scripts"): one decode query
+per sequence attends over a block-paged KV cache through a per-sequence block
+table; long sequences are split into partitions whose partial results are
+merged with a log-sum-exp rescale (the "V2" path of the forward_decode
+heuristic, "Phase 1" / "Phase 2").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "PaError", "load_library", "library_path", "decode", "decode_partitioned",
+    "partition_reduce", "decode_auto", "auto_workspace_bytes", "default_single_pass_max_len",
+    "gather_kv", "device_status", "num_partitions", "version",
+    "DEV_BAD_BLOCK", "DEV_LEN_CLAMPED", "DEV_WAIT_TIMEOUT", "DEV_TOO_MANY_PARTITIONS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libpadecode.so")
+
+PA_F16, PA_BF16 = 0, 1
+PHASE_PLAN, PHASE_ATTEND, PHASE_REDUCE = 1, 2, 4
+DEV_BAD_BLOCK, DEV_LEN_CLAMPED, DEV_WAIT_TIMEOUT, DEV_TOO_MANY_PARTITIONS = 1, 2, 4, 8
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+
+# (name, restype, argtypes) of every entry point in include/pa_decode.h
+SIGNATURES = [
+    ("pa_decode", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _vp]),
+    ("pa_decode_partitioned", _i, [_vp] * 8 + [_i] * 7 + [_f, _i, _i, _i, _vp]),
+    ("pa_partition_reduce", _i, [_vp] * 5 + [_i] * 6 + [_vp]),
+    ("pa_default_single_pass_max_len", _i, [_i] * 4),
+    ("pa_auto_workspace_bytes", ctypes.c_size_t, [_i] * 7),
+    ("pa_decode_auto", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t, _i,
+                                                    _vp]),
+    ("pa_decode_auto_phases", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t,
+                                                           _i, _vp, _i]),
+    ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
+    ("pa_device_status", _i, [_vp, ctypes.POINTER(_i)]),
+    ("pa_status_string", ctypes.c_char_p, [_i]),
+    ("pa_version", _i, []),
+]
+
+
+class PaError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = _load().pa_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what} failed: {name} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    f"libpadecode.so is not built ({_LIB_PATH}); run "
+                    "`python -m paged_kv_decode_partitioned_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, res, args in SIGNATURES:
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def load_library():
+    """Load (and return) the ctypes handle of libpadecode.so."""
+    return _load()
+
+
+def version() -> int:
+    return _load().pa_version()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"query/cache dtype must be float16 or bfloat16, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor, name: str) -> int:
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return _dev(t, name)
+
+
+def _f32(t: torch.Tensor, name: str) -> int:
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return _dev(t, name)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise PaError(status, what)
+
+
+def num_partitions(seq_len: int, partition_size: int) -> int:
+    """ceil(seq_len / partition_size)."""
+    return -(-int(seq_len) // int(partition_size))
+
+
+def _shape(query, key_cache, block_tables):
+    S, Hq, D = query.shape
+    nb, bs, Hkv, D2 = key_cache.shape
+    if D2 != D:
+        raise ValueError("query and cache head_dim differ")
+    return S, Hq, Hkv, D, bs, nb, block_tables.shape[1]
+
+
+def decode(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-pass decode (``pa_decode``); returns ``out`` [S, Hq, D]."""
+    S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
+    if out is None:
+        out = torch.empty_like(query)
+    with torch.cuda.device(query.device):
+        st = _load().pa_decode(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
+            _i32(seq_lens, "seq_lens"), S, Hq, Hkv, D, bs, nb, mb, float(scale),
+            _dtype_code(query), _stream(query))
+    _check(st, "pa_decode")
+    return out
+
+
+def decode_partitioned(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                       partition_size: int, max_num_partitions: int,
+                       tmp_out=None, exp_sums=None, max_logits=None
+                       ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Phase 1 (``pa_decode_partitioned``); returns (tmp_out, exp_sums, max_logits)."""
+    S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
+    NP = int(max_num_partitions)
+    dev = query.device
+    if tmp_out is None:
+        tmp_out = torch.empty((S, Hq, NP, D), dtype=torch.float32, device=dev)
+    if exp_sums is None:
+        exp_sums = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+    if max_logits is None:
+        max_logits = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().pa_decode_partitioned(
+            _f32(tmp_out, "tmp_out"), _f32(exp_sums, "exp_sums"), _f32(max_logits, "max_logits"),
+            _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+            _i32(block_tables, "block_tables"), _i32(seq_lens, "seq_lens"),
+            S, Hq, Hkv, D, bs, nb, mb, float(scale), int(partition_size), NP,
+            _dtype_code(query), _stream(query))
+    _check(st, "pa_decode_partitioned")
+    return tmp_out, exp_sums, max_logits
+
+
+def partition_reduce(tmp_out, exp_sums, max_logits, seq_lens, partition_size: int,
+                     out: Optional[torch.Tensor] = None, dtype=torch.bfloat16) -> torch.Tensor:
+    """Phase 2 (``pa_partition_reduce``); returns ``out`` [S, Hq, D] of ``dtype``."""
+    S, Hq, NP, D = tmp_out.shape
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=dtype, device=tmp_out.device)
+    with torch.cuda.device(tmp_out.device):
+        st = _load().pa_partition_reduce(
+            _dev(out, "out"), _f32(tmp_out, "tmp_out"), _f32(exp_sums, "exp_sums"),
+            _f32(max_logits, "max_logits"), _i32(seq_lens, "seq_lens"), S, Hq, D,
+            int(partition_size), NP, _dtype_code(out), _stream(tmp_out))
+    _check(st, "pa_partition_reduce")
+    return out
+
+
+def default_single_pass_max_len(num_seqs: int, num_kv_heads: int, partition_size: int = 512,
+                                num_sms: int = 0) -> int:
+    return _load().pa_default_single_pass_max_len(num_seqs, num_kv_heads, partition_size,
+                                                  num_sms)
+
+
+def auto_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                         max_seq_len: int, single_pass_max_len: int = 8192,
+                         partition_size: int = 512) -> int:
+    return int(_load().pa_auto_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_seq_len, single_pass_max_len,
+                                               partition_size))
+
+
+def decode_auto(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                max_seq_len: int, single_pass_max_len: int = 8192, partition_size: int = 512,
+                workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, phases: Optional[int] = None) -> torch.Tensor:
+    """Whole decode step with the per-sequence V1/V2 choice (``pa_decode_auto``).
+
+    ``phases`` (a PHASE_* mask) calls ``pa_decode_auto_phases`` instead, to
+    run only some of the step's launches; every phase needs the same arguments.
+    """
+    S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
+    need = auto_workspace_bytes(S, Hq, Hkv, D, max_seq_len, single_pass_max_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if out is None:
+        out = torch.empty_like(query)
+    args = (_dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
+            _i32(seq_lens, "seq_lens"), S, Hq, Hkv, D, bs, nb, mb, float(scale),
+            int(max_seq_len), int(single_pass_max_len), int(partition_size),
+            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _dtype_code(query), _stream(query))
+    with torch.cuda.device(query.device):
+        if phases is None:
+            st = _load().pa_decode_auto(*args)
+        else:
+            st = _load().pa_decode_auto_phases(*args, int(phases))
+    _check(st, "pa_decode_auto")
+    return out
+
+
+def gather_kv(key_cache, value_cache, block_tables, seq_lens, max_len: int):
+    """Test entry ``pa_gather_kv``: dense K/V [S, max_len, Hkv, D] (rows >= L are 0)."""
+    nb, bs, Hkv, D = key_cache.shape
+    S, mb = block_tables.shape
+    kd = torch.zeros((S, max_len, Hkv, D), dtype=key_cache.dtype, device=key_cache.device)
+    vd = torch.zeros_like(kd)
+    with torch.cuda.device(key_cache.device):
+        st = _load().pa_gather_kv(
+            _dev(kd, "k_dense"), _dev(vd, "v_dense"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
+            _i32(seq_lens, "seq_lens"), S, Hkv, D, bs, nb, mb, int(max_len),
+            _dtype_code(key_cache), _stream(key_cache))
+    _check(st, "pa_gather_kv")
+    return kd, vd
+
+
+def device_status(device=None) -> int:
+    """Read and clear the PA_DEV_* flags raised on ``device`` (synchronises its stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    flags = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        st = _load().pa_device_status(torch.cuda.current_stream(dev).cuda_stream,
+                                      ctypes.byref(flags))
+    _check(st, "pa_device_status")
+    return flags.value

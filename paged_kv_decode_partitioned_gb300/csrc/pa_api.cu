@@ -1,0 +1,521 @@
+// pa_api.cu -- the C ABI of libpadecode.so (declared in include/pa_decode.h):
+// argument checks, TMA tensor maps over the caches, work decomposition and
+// kernel launches.  Every check happens here, before anything is launched.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_decode.h"
+#include "pa_launch.h"
+
+namespace {
+
+using namespace pa;
+
+// Device status word (PA_DEV_* flags), one per device that loads the library.
+__device__ int g_pa_status_word;
+
+constexpr int kMaxDev = 64;
+constexpr int kVersion = 10000;   // 1.0.0
+
+struct DevInfo {
+    int *status = nullptr;
+    int num_sms = 0;
+    bool ready = false;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[kMaxDev];
+
+int device_info(DevInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return PA_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_status_word) != cudaSuccess) return PA_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        d.status = static_cast<int *>(p);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    *out = &d;
+    return PA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 5-D view of a cache [num_blocks][bs][Hkv][D] for TMA: (64-element piece,
+// piece index, KV head, row in block, block); one box = 16 rows of one KV
+// head, 128-byte swizzled.  Out-of-range boxes read zeros.
+int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv, int bs,
+                   int num_blocks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PA_ERR_NO_DEVICE;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(Hkv),
+                          static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(num_blocks)};
+    cuuint64_t strides[4] = {64 * e, D * e, static_cast<cuuint64_t>(Hkv) * D * e,
+                             static_cast<cuuint64_t>(bs) * Hkv * D * e};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(D / 64), 1, static_cast<cuuint32_t>(kTile), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    5, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Shape {
+    int S, Hq, Hkv, D, bs, num_blocks, max_blocks;
+};
+
+// Checks shared by the attention entry points.  Returns PA_OK, or 1 when
+// there is nothing to do (num_seqs == 0), or a negative status.
+int check_attention(const Shape &s, pa_dtype_t dtype, const void *query, const void *kc,
+                    const void *vc, const int32_t *bt, const int32_t *sl) {
+    if (s.S < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.D <= 0 || s.bs <= 0 || s.num_blocks < 0 ||
+        s.max_blocks < 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
+    if (s.Hq % s.Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
+    if (s.D != 64 && s.D != 128 && s.D != 256) return PA_ERR_UNSUPPORTED;
+    if (s.bs % kTile != 0) return PA_ERR_UNSUPPORTED;
+    if (s.Hq / s.Hkv > kHeadsPad) return PA_ERR_UNSUPPORTED;
+    if (s.S > 65535 || s.Hkv > 65535 || s.Hq > 65535) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(s.max_blocks) * s.bs > INT_MAX) return PA_ERR_UNSUPPORTED;
+    if (s.S == 0) return 1;
+    if (!query || !kc || !vc || !bt || !sl) return PA_ERR_INVALID_ARGUMENT;
+    if (s.num_blocks == 0 || s.max_blocks == 0) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(query, 16) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(bt, 4) ||
+        !aligned(sl, 4))
+        return PA_ERR_MISALIGNED;
+    return PA_OK;
+}
+
+Params base_params(const Shape &s, const void *query, const int32_t *bt, const int32_t *sl,
+                   float scale, int *status) {
+    Params p{};
+    p.q = query;
+    p.block_tables = bt;
+    p.seq_lens = sl;
+    p.status = status;
+    p.num_seqs = s.S;
+    p.num_q_heads = s.Hq;
+    p.num_kv_heads = s.Hkv;
+    p.group = s.Hq / s.Hkv;
+    p.block_size = s.bs;
+    p.max_blocks = s.max_blocks;
+    p.num_blocks = s.num_blocks;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    return p;
+}
+
+cudaError_t attn(pa_dtype_t dt, int D, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
+                 const Params &p, dim3 grid, cudaStream_t st) {
+    return dt == PA_BF16 ? launch_attn<__nv_bfloat16>(D, mode, tk, tv, p, grid, st)
+                         : launch_attn<__half>(D, mode, tk, tv, p, grid, st);
+}
+
+cudaError_t reduce(pa_dtype_t dt, int D, bool compact, const ReduceParams &r, dim3 grid,
+                   cudaStream_t st) {
+    return dt == PA_BF16 ? launch_reduce<__nv_bfloat16>(D, compact, r, grid, st)
+                         : launch_reduce<__half>(D, compact, r, grid, st);
+}
+
+// Workspace layout of pa_decode_auto.
+struct AutoLayout {
+    size_t counter, units, part_base, exp_sums, max_logits, tmp_out, total;
+    int max_parts, max_slots, max_units;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P, AutoLayout *L) {
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seq_len < 0 || P <= 0) return false;
+    const int64_t parts = max_seq_len > thr ? (static_cast<int64_t>(max_seq_len) + P - 1) / P : 0;
+    const int64_t slots = static_cast<int64_t>(S) * parts;
+    const int64_t units = static_cast<int64_t>(S) * Hkv * (parts > 1 ? parts : 1);
+    if (slots * Hq > INT_MAX || units > INT_MAX) return false;
+    L->max_parts = static_cast<int>(parts);
+    L->max_slots = static_cast<int>(slots);
+    L->max_units = static_cast<int>(units);
+    size_t off = 0;
+    L->counter = off;
+    off = align256(off + 2 * sizeof(int));
+    L->units = off;
+    off = align256(off + static_cast<size_t>(units) * sizeof(int4));
+    L->part_base = off;
+    off = align256(off + static_cast<size_t>(S) * sizeof(int32_t));
+    L->exp_sums = off;
+    off = align256(off + static_cast<size_t>(slots) * Hq * sizeof(float));
+    L->max_logits = off;
+    off = align256(off + static_cast<size_t>(slots) * Hq * sizeof(float));
+    L->tmp_out = off;
+    off = align256(off + static_cast<size_t>(slots) * Hq * D * sizeof(float));
+    L->total = off;
+    return true;
+}
+
+int default_thr(int S, int Hkv, int P, int num_sms) {
+    const int64_t units = static_cast<int64_t>(S) * Hkv;
+    return units >= 2 * static_cast<int64_t>(num_sms) ? 8192 : P;
+}
+
+int num_sms_now() {
+    DevInfo *d = nullptr;
+    if (device_info(&d) != PA_OK) return 0;
+    return d->num_sms;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return kVersion; }
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARGUMENT: return "PA_ERR_INVALID_ARGUMENT";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_MISALIGNED: return "PA_ERR_MISALIGNED";
+        case PA_ERR_WORKSPACE_TOO_SMALL: return "PA_ERR_WORKSPACE_TOO_SMALL";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+        case PA_ERR_NO_DEVICE: return "PA_ERR_NO_DEVICE";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_decode(void *out, const void *query, const void *key_cache, const void *value_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+              int max_blocks_per_seq, float scale, pa_dtype_t dtype, void *stream) {
+    const Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks_per_seq};
+    int rc = check_attention(s, dtype, query, key_cache, value_cache, block_tables, seq_lens);
+    if (rc != PA_OK) return rc > 0 ? PA_OK : rc;
+    if (!out) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(out, 16)) return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    if ((rc = device_info(&di)) != PA_OK) return rc;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
+    p.out = out;
+    const dim3 grid(num_kv_heads, num_seqs);
+    return attn(dtype, head_dim, kModeSingle, tk, tv, p, grid, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_decode_partitioned(float *tmp_out, float *exp_sums, float *max_logits, const void *query,
+                          const void *key_cache, const void *value_cache,
+                          const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, int max_blocks_per_seq, float scale,
+                          int partition_size, int max_num_partitions, pa_dtype_t dtype,
+                          void *stream) {
+    const Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks_per_seq};
+    int rc = check_attention(s, dtype, query, key_cache, value_cache, block_tables, seq_lens);
+    if (rc < 0) return rc;
+    if (partition_size <= 0 || max_num_partitions <= 0) return PA_ERR_INVALID_ARGUMENT;
+    if (partition_size % block_size != 0) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_seqs) * num_q_heads * max_num_partitions * head_dim >
+        (static_cast<int64_t>(1) << 40))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (rc > 0) return PA_OK;
+    if (!tmp_out || !exp_sums || !max_logits) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(tmp_out, 16) || !aligned(exp_sums, 4) || !aligned(max_logits, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    if ((rc = device_info(&di)) != PA_OK) return rc;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
+    p.tmp_out = tmp_out;
+    p.exp_sums = exp_sums;
+    p.max_logits = max_logits;
+    p.partition_size = partition_size;
+    p.max_parts = max_num_partitions;
+    const dim3 grid(max_num_partitions, num_kv_heads, num_seqs);
+    return attn(dtype, head_dim, kModePartitioned, tk, tv, p, grid,
+                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_partition_reduce(void *out, const float *tmp_out, const float *exp_sums,
+                        const float *max_logits, const int32_t *seq_lens, int num_seqs,
+                        int num_q_heads, int head_dim, int partition_size,
+                        int max_num_partitions, pa_dtype_t dtype, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || partition_size <= 0 || max_num_partitions <= 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !tmp_out || !exp_sums || !max_logits || !seq_lens) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(out, 16) || !aligned(tmp_out, 16) || !aligned(exp_sums, 4) ||
+        !aligned(max_logits, 4) || !aligned(seq_lens, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    ReduceParams r{};
+    r.out = out;
+    r.tmp_out = tmp_out;
+    r.exp_sums = exp_sums;
+    r.max_logits = max_logits;
+    r.seq_lens = seq_lens;
+    r.status = di->status;
+    r.num_q_heads = num_q_heads;
+    r.partition_size = partition_size;
+    r.max_parts = max_num_partitions;
+    r.single_pass_max_len = -1;
+    r.len_cap = INT_MAX;
+    return reduce(dtype, head_dim, false, r, dim3(num_q_heads, num_seqs),
+                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int partition_size,
+                                   int num_sms) {
+    if (num_sms <= 0) num_sms = num_sms_now();
+    if (num_sms <= 0) num_sms = 1;
+    return default_thr(num_seqs, num_kv_heads, partition_size, num_sms);
+}
+
+size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_seq_len, int single_pass_max_len, int partition_size) {
+    if (partition_size <= 0 || num_kv_heads <= 0) return 0;
+    const int thr = single_pass_max_len >= 0
+                        ? single_pass_max_len
+                        : pa_default_single_pass_max_len(num_seqs, num_kv_heads, partition_size, 0);
+    AutoLayout L;
+    if (!auto_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, thr,
+                     partition_size, &L))
+        return 0;
+    return L.total;
+}
+
+int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, float scale, int max_seq_len,
+                          int single_pass_max_len, int partition_size, void *workspace,
+                          size_t workspace_bytes, pa_dtype_t dtype, void *stream, int phases) {
+    const Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks_per_seq};
+    int rc = check_attention(s, dtype, query, key_cache, value_cache, block_tables, seq_lens);
+    if (rc < 0) return rc;
+    if (partition_size <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (phases <= 0 || (phases & ~(PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE)) != 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (partition_size % block_size != 0) return PA_ERR_UNSUPPORTED;
+    if (rc > 0) return PA_OK;
+    if (!out) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(out, 16)) return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    int thr = single_pass_max_len;
+    if (thr < 0) {   // the heuristic needs the device's SM count
+        if ((rc = device_info(&di)) != PA_OK) return rc;
+        thr = default_thr(num_seqs, num_kv_heads, partition_size, di->num_sms);
+    }
+    AutoLayout L;
+    if (!auto_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, thr,
+                     partition_size, &L))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (!workspace) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256)) return PA_ERR_MISALIGNED;
+    if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (!di && (rc = device_info(&di)) != PA_OK) return rc;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *counter = reinterpret_cast<int *>(ws + L.counter);
+    int4 *units = reinterpret_cast<int4 *>(ws + L.units);
+    int32_t *part_base = reinterpret_cast<int32_t *>(ws + L.part_base);
+    float *es = reinterpret_cast<float *>(ws + L.exp_sums);
+    float *ml = reinterpret_cast<float *>(ws + L.max_logits);
+    float *tmp = reinterpret_cast<float *>(ws + L.tmp_out);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int len_cap = max_blocks_per_seq * block_size;
+
+    PlanParams pp{};
+    pp.seq_lens = seq_lens;
+    pp.units = units;
+    pp.unit_counter = counter;
+    pp.unit_count = counter + 1;
+    pp.part_base = part_base;
+    pp.status = di->status;
+    pp.num_seqs = num_seqs;
+    pp.num_kv_heads = num_kv_heads;
+    pp.partition_size = partition_size;
+    pp.single_pass_max_len = thr;
+    pp.len_cap = len_cap;
+    pp.max_parts = L.max_parts;
+    if ((phases & PA_PHASE_PLAN) && launch_plan(pp, st) != cudaSuccess) return PA_ERR_CUDA;
+
+    Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
+    p.out = out;
+    p.tmp_out = tmp;
+    p.exp_sums = es;
+    p.max_logits = ml;
+    p.units = units;
+    p.unit_counter = counter;
+    p.unit_count = counter + 1;
+    p.part_base = part_base;
+    p.partition_size = partition_size;
+    p.max_parts = L.max_parts;
+    p.single_pass_max_len = thr;
+    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim)
+                                        : attn_ctas_per_sm<__half>(head_dim);
+    if (per_sm <= 0) return PA_ERR_CUDA;
+    int64_t ctas = static_cast<int64_t>(per_sm) * di->num_sms;
+    if (ctas > L.max_units) ctas = L.max_units;
+    if (ctas < 1) ctas = 1;
+    if ((phases & PA_PHASE_ATTEND) &&
+        attn(dtype, head_dim, kModeWorklist, tk, tv, p, dim3(static_cast<unsigned>(ctas)), st) !=
+            cudaSuccess)
+        return PA_ERR_CUDA;
+
+    if ((phases & PA_PHASE_REDUCE) && L.max_parts > 0) {
+        ReduceParams r{};
+        r.out = out;
+        r.tmp_out = tmp;
+        r.exp_sums = es;
+        r.max_logits = ml;
+        r.seq_lens = seq_lens;
+        r.part_base = part_base;
+        r.status = di->status;
+        r.num_q_heads = num_q_heads;
+        r.partition_size = partition_size;
+        r.max_parts = L.max_parts;
+        r.single_pass_max_len = thr;
+        r.len_cap = len_cap;
+        if (reduce(dtype, head_dim, true, r, dim3(num_q_heads, num_seqs), st) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_decode_auto(void *out, const void *query, const void *key_cache, const void *value_cache,
+                   const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, int max_blocks_per_seq, float scale, int max_seq_len,
+                   int single_pass_max_len, int partition_size, void *workspace,
+                   size_t workspace_bytes, pa_dtype_t dtype, void *stream) {
+    return pa_decode_auto_phases(out, query, key_cache, value_cache, block_tables, seq_lens,
+                                 num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 num_blocks, max_blocks_per_seq, scale, max_seq_len,
+                                 single_pass_max_len, partition_size, workspace, workspace_bytes,
+                                 dtype, stream,
+                                 PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE);
+}
+
+int pa_gather_kv(void *k_dense, void *v_dense, const void *key_cache, const void *value_cache,
+                 const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                 int max_blocks_per_seq, int max_len, pa_dtype_t dtype, void *stream) {
+    const Shape s{num_seqs, num_kv_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks_per_seq};
+    int rc = check_attention(s, dtype, key_cache, key_cache, value_cache, block_tables, seq_lens);
+    if (rc < 0) return rc;
+    if (max_len < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (rc > 0 || max_len == 0) return PA_OK;
+    if (!k_dense || !v_dense) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_dense, 16) || !aligned(v_dense, 16)) return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    if ((rc = device_info(&di)) != PA_OK) return rc;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    GatherParams gp{};
+    gp.k_dense = k_dense;
+    gp.v_dense = v_dense;
+    gp.block_tables = block_tables;
+    gp.seq_lens = seq_lens;
+    gp.status = di->status;
+    gp.num_kv_heads = num_kv_heads;
+    gp.block_size = block_size;
+    gp.max_blocks = max_blocks_per_seq;
+    gp.num_blocks = num_blocks;
+    gp.max_len = max_len;
+    const dim3 grid((max_len + kTile - 1) / kTile, num_kv_heads, num_seqs);
+    return launch_gather(head_dim, tk, tv, gp, grid, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_device_status(void *stream, int *flags) {
+    if (!flags) return PA_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_pa_status_word, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                  st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_pa_status_word, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    *flags = v;
+    return PA_OK;
+}
+
+}  // extern "C"

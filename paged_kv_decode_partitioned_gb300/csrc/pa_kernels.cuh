@@ -1,0 +1,610 @@
+// pa_kernels.cuh -- device code of the paged-attention decode library for
+// GB300 (sm_103a).
+//
+// The method (project_6, commit cd0d9e1 "qwen3_6_scripts"):
+//   * "forward_decode: V2 enabled via original heuristic" -- a decode query
+//     attends over its sequence's whole KV range in one pass (V1), or
+//   * "V2: splits into PARTITION_SIZE=512 chunks, runs them in parallel, then
+//     reduces with log-sum-exp": "Phase 1: Per-partition attention" stores a
+//     normalised partial output, its max logit and its exp-sum, and "Phase 2:
+//     Cross-partition reduction (log-sum-exp)" merges them with the rescale
+//     exp(partition_max - global_max) * partition_exp_sum;
+//   * "The online softmax tiling is the same as Flash Attention's
+//     partitioning" and "The reduction pattern is identical to CCCL's
+//     block_reduce_warp_reductions (combine partial statistics from
+//     independent segments)": inside a partition, each warp keeps a running
+//     (max, exp-sum, output) over its tiles, and the warps' states are merged
+//     with the same rescale as phase 2.
+//
+// GB300 design (how, not what):
+//   * One work unit = (sequence, KV head, token range).  All query heads that
+//     share the KV head (the GQA group, <= 8) are handled by the unit, so each
+//     K/V byte is read from HBM once.
+//   * Each warp of a CTA owns a ring of NS shared-memory stages and streams
+//     16-token tiles of its share of the unit through them with TMA
+//     (cp.async.bulk.tensor, 5-D tensor map over the cache, 128-byte swizzle)
+//     completing on an mbarrier.  Block-table entries are prefetched 32 tiles
+//     ahead into a lane-distributed register window.  A table entry outside
+//     the cache becomes an out-of-bounds TMA coordinate, which reads zeros.
+//   * The per-tile contraction is tiny (16 tokens x <=8 heads x head_dim), so
+//     it runs on warp-level tensor-core MMAs (m16n8k16, fp32 accumulate) in a
+//     transposed form: S^T = K Q^T (M = tokens, N = heads) and
+//     O^T += V^T P^T (M = head_dim, N = heads).  The softmax probabilities go
+//     from the S^T accumulator to the P^T operand with one movmatrix
+//     transpose per 8x8 block, never touching shared memory.
+//   * Softmax runs in the log2 domain (logit * scale * log2 e) with ex2.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_types.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 5-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T> struct Mma;
+
+template <> struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    static __device__ __forceinline__ __nv_bfloat16 cvt(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <> struct Mma<__half> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    static __device__ __forceinline__ __half cvt(float x) { return __float2half_rn(x); }
+};
+
+// Byte offset of element (row, col) of one 16-row tile as TMA lays it out:
+// rows of D elements split into 64-element (128-byte) pieces, row-major over
+// (row, piece), with the 128-byte swizzle (16-byte chunk index XOR the
+// 128-byte row index mod 8).  Tiles start on 1024-byte boundaries.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    const int r128 = row * (D / 64) + (col >> 6);
+    const int chunk = (col & 63) >> 3;
+    return static_cast<uint32_t>(r128 * 128 + ((chunk ^ (r128 & 7)) << 4) + ((col & 7) << 1));
+}
+
+__device__ __forceinline__ int clamp_len(const int32_t *seq_lens, int s, int cap, int *status) {
+    int L = __ldg(seq_lens + s);
+    if (L < 0 || L > cap) {
+        atomicOr(status, kLenClamped);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory plan of the attention kernel
+// ---------------------------------------------------------------------------
+template <int D, int NW, int NS>
+struct Smem {
+    static constexpr int kTileBytes = kTile * D * 2;            // one K or V tile
+    static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
+    static constexpr int kStagesBytes = NW * NS * kStageBytes;
+    static constexpr int kMergeBytes = NW * kHeadsPad * (D + 2) * 4;
+    static constexpr int kBarOffset =
+        ((kStagesBytes > kMergeBytes ? kStagesBytes : kMergeBytes) + 15) / 16 * 16;
+    static constexpr int kBytes = kBarOffset + NW * NS * 8 + 16;
+    static constexpr int kLaunchBytes = kBytes + 1024;          // slack for 1024-byte alignment
+};
+
+// ---------------------------------------------------------------------------
+// One work unit: tokens [t0, t1) of (seq, kvh), all heads of the GQA group.
+// Returns false if a pipeline wait gave up (the CTA must stop).
+// ---------------------------------------------------------------------------
+template <typename T, int D, int NW, int NS>
+__device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *tmK,
+                                            const CUtensorMap *tmV, uint8_t *smem, uint32_t bar0,
+                                            uint32_t &uses, int seq, int kvh, int t0, int t1,
+                                            int out_kind, int part, int slot, int *s_abort) {
+    using SM = Smem<D, NW, NS>;
+    constexpr int KT = D / 16;   // k-steps of S^T, m-tiles of O^T
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = p.group;
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+    const int32_t *bt_row = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
+
+    // Block-table window: lane l holds the physical block of local tile base+l.
+    auto fetch = [&](int i) -> int {
+        if (i >= my_tiles) return 0;
+        const int tok = t0 + (warp + i * NW) * kTile;
+        const int b = __ldg(bt_row + tok / p.block_size);
+        if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
+            atomicOr(p.status, kBadBlock);
+        return b;
+    };
+    int win_cur = fetch(lane);
+    int win_next = fetch(32 + lane);
+    int win_base = 0;
+    auto phys_of = [&](int i) -> int {   // warp-uniform, called with i = 0, 1, 2, ...
+        if (i - win_base >= 32) {
+            win_cur = win_next;
+            win_base += 32;
+            win_next = fetch(win_base + 32 + lane);
+        }
+        return __shfl_sync(0xffffffffu, win_cur, i - win_base);
+    };
+
+    const uint32_t stage0 = smem_u32(smem) + warp * NS * SM::kStageBytes;
+    auto issue = [&](int i) {
+        const int b = phys_of(i);
+        if (lane == 0) {
+            const uint32_t st = (uses + i) % NS;
+            const uint32_t bar = bar0 + (warp * NS + st) * 8;
+            const uint32_t dk = stage0 + st * SM::kStageBytes;
+            const int row = (t0 + (warp + i * NW) * kTile) % p.block_size;
+            mbar_expect_tx(bar, SM::kStageBytes);
+            tma_load_5d(dk, tmK, bar, 0, 0, kvh, row, b);
+            tma_load_5d(dk + SM::kTileBytes, tmV, bar, 0, 0, kvh, row, b);
+        }
+    };
+
+    // Query fragments (the B operand of S^T = K Q^T): lane holds head lane/4,
+    // dims 2*(lane%4)+{0,1} and +8 of every 16-dim step; padded heads are 0.
+    uint32_t qf[KT][2];
+    {
+        const int h = lane >> 2;
+        const T *qrow = static_cast<const T *>(p.q) +
+                        (static_cast<size_t>(seq) * p.num_q_heads + kvh * g + (h < g ? h : 0)) * D;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            qf[kk][0] = h < g ? __ldg(q32 + (kk * 16 + 2 * (lane & 3)) / 2) : 0u;
+            qf[kk][1] = h < g ? __ldg(q32 + (kk * 16 + 8 + 2 * (lane & 3)) / 2) : 0u;
+        }
+    }
+
+    float o[KT][4];
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    const int mi = lane >> 3, ri = lane & 7;
+    const int rowK = (mi & 1) * 8 + ri, hiK = mi >> 1;   // S^T A operand (K, row-major)
+    const int rowV = (mi >> 1) * 8 + ri, hiV = mi & 1;   // O^T A operand (V^T via .trans)
+    const int r0 = lane >> 2;
+
+    for (int i = 0; i < NS && i < my_tiles; ++i) issue(i);
+
+    bool ok = true;
+    for (int i = 0; i < my_tiles; ++i) {
+        const uint32_t st = (uses + i) % NS;
+        const uint32_t bar = bar0 + (warp * NS + st) * 8;
+        if (!mbar_wait_bounded(bar, ((uses + i) / NS) & 1u)) {
+            // Give the copies already issued a bounded chance to land, then stop.
+            for (int j = i + 1; j < my_tiles && j < i + NS; ++j)
+                mbar_wait_bounded(bar0 + (warp * NS + (uses + j) % NS) * 8, ((uses + j) / NS) & 1u);
+            if (lane == 0) atomicOr(p.status, kWaitTimeout);
+            ok = false;
+            break;
+        }
+        const uint32_t kb = stage0 + st * SM::kStageBytes;
+        const uint32_t vb = kb + SM::kTileBytes;
+        const int tt = t0 + (warp + i * NW) * kTile;
+        const int nvalid = min(kTile, t1 - tt);
+        if (nvalid < kTile) {
+            // Rows past the sequence end hold whatever the block holds; zero
+            // their V so that 0 * garbage cannot reach the accumulator.
+            uint8_t *vrow = smem + (vb - smem_u32(smem));
+            const int first = nvalid * D * 2, bytes = kTile * D * 2 - first;
+            for (int off = lane * 16; off < bytes; off += 32 * 16)
+                *reinterpret_cast<uint4 *>(vrow + first + off) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // S^T[16 tokens][8 heads] = K[16][D] . Q^T[D][8]
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(a, kb + swz<D>(rowK, kk * 16 + hiK * 8));
+            Mma<T>::run(s, a, qf[kk][0], qf[kk][1]);
+        }
+        // lane: tokens r0 and r0+8, heads 2*(lane%4) and +1; log2-domain logits
+        const float y0 = r0 < nvalid ? s[0] * p.scale_log2 : -INFINITY;
+        const float y1 = r0 < nvalid ? s[1] * p.scale_log2 : -INFINITY;
+        const float y2 = r0 + 8 < nvalid ? s[2] * p.scale_log2 : -INFINITY;
+        const float y3 = r0 + 8 < nvalid ? s[3] * p.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);
+        const float p0 = ex2(y0 - mn0), p1 = ex2(y1 - mn1);
+        const float p2 = ex2(y2 - mn0), p3 = ex2(y3 - mn1);
+        l0 = l0 * a0 + (p0 + p2);
+        l1 = l1 * a1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
+        }
+        // P^T operand: transpose the (token, head) pairs into (head, token) pairs.
+        const uint32_t b0 = movmatrix_t(Mma<T>::pack(p0, p1));
+        const uint32_t b1 = movmatrix_t(Mma<T>::pack(p2, p3));
+        // O^T[D][8 heads] += V^T[D][16] . P^T[16][8]
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_t(a, vb + swz<D>(rowV, mt * 16 + hiV * 8));
+            Mma<T>::run(o[mt], a, b0, b1);
+        }
+        __syncwarp();
+        if (i + NS < my_tiles) issue(i + NS);
+    }
+    uses += my_tiles;
+    if (!ok) *s_abort = 1;   // benign race: every writer stores 1
+
+    // Per-lane exp-sums cover the lane's tokens: sum over the 8 lanes of a head.
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+
+    __syncthreads();   // every warp is done reading its stages
+    float *sm_o = reinterpret_cast<float *>(smem);              // [NW][8][D]
+    float *sm_m = sm_o + NW * kHeadsPad * D;                     // [NW][8]
+    float *sm_l = sm_m + NW * kHeadsPad;                         // [NW][8]
+    if (lane < 4) {
+        sm_m[warp * kHeadsPad + 2 * lane] = m0;
+        sm_m[warp * kHeadsPad + 2 * lane + 1] = m1;
+        sm_l[warp * kHeadsPad + 2 * lane] = l0;
+        sm_l[warp * kHeadsPad + 2 * lane + 1] = l1;
+    }
+    {
+        const int h0 = 2 * (lane & 3);
+        float *w0 = sm_o + (warp * kHeadsPad + h0) * D;
+        float *w1 = w0 + D;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+            const int dim = mt * 16 + r0;
+            w0[dim] = o[mt][0];
+            w1[dim] = o[mt][1];
+            w0[dim + 8] = o[mt][2];
+            w1[dim + 8] = o[mt][3];
+        }
+    }
+    __syncthreads();
+    const bool write = (*s_abort == 0);
+    const int Hq = p.num_q_heads;
+    for (int e = threadIdx.x; e < g * D && write; e += NW * 32) {
+        const int h = e / D, dim = e - (e / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * kHeadsPad + h]);
+        float Ls = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float wt = ex2(sm_m[w * kHeadsPad + h] - M);
+                Ls += wt * sm_l[w * kHeadsPad + h];
+                acc += wt * sm_o[(w * kHeadsPad + h) * D + dim];
+            }
+        }
+        const float res = Ls > 0.f ? acc / Ls : 0.f;
+        const int head = kvh * g + h;
+        if (out_kind == kOutFinal) {
+            static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + head) * D + dim] =
+                Mma<T>::cvt(res);
+        } else {
+            size_t srow;
+            if (out_kind == kOutPartialDense)
+                srow = (static_cast<size_t>(seq) * Hq + head) * p.max_parts + part;
+            else
+                srow = static_cast<size_t>(slot) * Hq + head;
+            p.tmp_out[srow * D + dim] = res;
+            if (dim == 0) {
+                p.exp_sums[srow] = Ls;
+                p.max_logits[srow] = M == -INFINITY ? -INFINITY : M * kLn2;
+            }
+        }
+    }
+    // The merge wrote this memory through the generic proxy; order those
+    // writes before any later TMA into it, then let every thread finish.
+    fence_proxy_async_smem();
+    __syncthreads();
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Attention kernel: single-pass grid, partitioned grid, or persistent work list.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int NW, int NS, int MODE>
+__global__ void __launch_bounds__(NW * 32)
+    pa_attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using SM = Smem<D, NW, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ int s_abort;
+    __shared__ int s_next;
+    const uint32_t bar0 = smem_u32(smem + SM::kBarOffset);
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        s_abort = 0;
+    }
+    if (threadIdx.x < NW * NS) mbar_init(bar0 + threadIdx.x * 8, 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    uint32_t uses = 0;
+    const int cap = p.max_blocks * p.block_size;
+    if constexpr (MODE == kModeSingle) {
+        const int kvh = blockIdx.x, seq = blockIdx.y;
+        const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+        attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, 0, L, kOutFinal, 0,
+                                  0, &s_abort);
+    } else if constexpr (MODE == kModePartitioned) {
+        const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+        const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+        const int P = p.partition_size;
+        int n = (L + P - 1) / P;
+        if (n > p.max_parts) {
+            if (part == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kTooManyParts);
+            n = p.max_parts;
+        }
+        if (part >= n) return;
+        const int t0 = part * P;
+        const int t1 = min(t0 + P, L);
+        attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, t0, t1,
+                                  kOutPartialDense, part, 0, &s_abort);
+    } else {
+        const int total = *p.unit_count;
+        if (threadIdx.x == 0) s_next = atomicAdd(p.unit_counter, 1);
+        __syncthreads();
+        int u = s_next;
+        while (u < total) {
+            int nxt = 0;
+            if (threadIdx.x == 0) nxt = atomicAdd(p.unit_counter, 1);   // prefetch the next unit
+            const int4 d = p.units[u];
+            const int seq = d.x, kvh = d.y, part = d.z, kind = d.w;
+            const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+            bool ok;
+            if (kind == kOutFinal) {
+                ok = attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, 0, L,
+                                               kOutFinal, 0, 0, &s_abort);
+            } else {
+                const int P = p.partition_size;
+                const int t0 = part * P;
+                const int t1 = min(t0 + P, L);
+                ok = attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, t0, t1,
+                                               kOutPartialCompact, part,
+                                               __ldg(p.part_base + seq) + part, &s_abort);
+            }
+            if (threadIdx.x == 0) s_next = nxt;
+            __syncthreads();
+            if (!ok || s_abort) break;   // s_abort is CTA-uniform here
+            u = s_next;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Phase 2: log-sum-exp merge of the partials of one (sequence, query head).
+// ---------------------------------------------------------------------------
+constexpr int kReduceThreads = 256;
+constexpr int kReduceChunk = 2048;   // partition weights staged per pass
+
+template <typename T, int D, bool COMPACT>
+__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
+    constexpr int NWR = kReduceThreads / 32;
+    constexpr int VEC = D / 32;   // floats per lane
+    __shared__ float s_w[kReduceChunk];
+    __shared__ float s_red[NWR];
+    __shared__ float s_acc[NWR][D];
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int Hq = r.num_q_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
+    size_t stat0, pstride;   // stats index of partition 0 and the stride between partitions
+    int n = (L + r.partition_size - 1) / r.partition_size;
+    if constexpr (COMPACT) {
+        if (L <= r.single_pass_max_len) return;   // written directly by the attention kernel
+        const int base = __ldg(r.part_base + s);
+        if (base < 0) return;
+        stat0 = static_cast<size_t>(base) * Hq + h;
+        pstride = Hq;
+    } else {
+        stat0 = (static_cast<size_t>(s) * Hq + h) * r.max_parts;
+        pstride = 1;
+    }
+    if (n > r.max_parts) n = r.max_parts;
+    T *out = static_cast<T *>(r.out) + (static_cast<size_t>(s) * Hq + h) * D;
+    if (n <= 0) {
+        for (int i = threadIdx.x; i < D; i += kReduceThreads) out[i] = Mma<T>::cvt(0.f);
+        return;
+    }
+    // global max of the partition maxima
+    float M = -INFINITY;
+    for (int q = threadIdx.x; q < n; q += kReduceThreads)
+        M = fmaxf(M, __ldg(r.max_logits + stat0 + q * pstride));
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    if (lane == 0) s_red[warp] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < NWR; ++w) M = fmaxf(M, s_red[w]);
+    __syncthreads();
+
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    float total = 0.f;   // per-thread part of sum_p w_p (threads stride the partitions)
+    for (int c0 = 0; c0 < n; c0 += kReduceChunk) {
+        const int cn = min(kReduceChunk, n - c0);
+        for (int q = threadIdx.x; q < cn; q += kReduceThreads) {
+            const size_t si = stat0 + (c0 + q) * pstride;
+            const float w = ex2((__ldg(r.max_logits + si) - M) * kLog2e) * __ldg(r.exp_sums + si);
+            s_w[q] = w;
+            total += w;
+        }
+        __syncthreads();
+        // warp `warp` takes partitions warp, warp+NWR, ...; lane takes dims lane*VEC...
+#pragma unroll 4
+        for (int q = warp; q < cn; q += NWR) {
+            const float w = s_w[q];
+            const float *src = r.tmp_out + (stat0 + (c0 + q) * pstride) * D + lane * VEC;
+            if constexpr (VEC == 2) {
+                const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; v += 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4 *>(src + v));
+                    acc[v] += w * x.x;
+                    acc[v + 1] += w * x.y;
+                    acc[v + 2] += w * x.z;
+                    acc[v + 3] += w * x.w;
+                }
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) total += __shfl_xor_sync(0xffffffffu, total, x);
+    if (lane == 0) s_red[warp] = total;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) s_acc[warp][lane * VEC + v] = acc[v];
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWR; ++w) tot += s_red[w];
+    for (int i = threadIdx.x; i < D; i += kReduceThreads) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWR; ++w) a += s_acc[w][i];
+        out[i] = Mma<T>::cvt(tot > 0.f ? a / tot : 0.f);
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,110 @@
+// pa_launch.cuh -- host-side launchers of the decode kernels.  Each dtype's
+// translation unit includes this file and instantiates the launchers for its
+// type (explicit instantiation), so the heavy templates compile in parallel.
+#pragma once
+
+#include <atomic>
+
+#include "pa_kernels.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+// CTA shape of the attention kernel per head_dim: NW warps, NS stages per warp.
+template <int D> struct AttnCfg;
+template <> struct AttnCfg<64> { static constexpr int NW = 4, NS = 4; };
+template <> struct AttnCfg<128> { static constexpr int NW = 4, NS = 2; };
+template <> struct AttnCfg<256> { static constexpr int NW = 4, NS = 2; };
+
+constexpr int kMaxDevices = 64;
+
+// Opt a kernel into its dynamic shared memory size once per device.
+template <typename K>
+inline cudaError_t ensure_smem(K kernel, int bytes, std::atomic<int> *done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+template <typename T, int D, int MODE>
+inline cudaError_t launch_attn_d(const CUtensorMap &tmK, const CUtensorMap &tmV, const Params &p,
+                                 dim3 grid, cudaStream_t st) {
+    using C = AttnCfg<D>;
+    using SM = Smem<D, C::NW, C::NS>;
+    static std::atomic<int> done[kMaxDevices];
+    auto k = pa_attn_kernel<T, D, C::NW, C::NS, MODE>;
+    cudaError_t e = ensure_smem(k, SM::kLaunchBytes, done);
+    if (e != cudaSuccess) return e;
+    k<<<grid, C::NW * 32, SM::kLaunchBytes, st>>>(tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+inline int attn_ctas_per_sm_d() {
+    using C = AttnCfg<D>;
+    using SM = Smem<D, C::NW, C::NS>;
+    static std::atomic<int> done[kMaxDevices];
+    auto k = pa_attn_kernel<T, D, C::NW, C::NS, kModeWorklist>;
+    if (ensure_smem(k, SM::kLaunchBytes, done) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, C::NW * 32, SM::kLaunchBytes) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <typename T>
+cudaError_t launch_attn(int D, int mode, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                        const Params &p, dim3 grid, cudaStream_t st) {
+#define PA_MODES(DD)                                                                   \
+    if (D == DD) {                                                                     \
+        if (mode == kModeSingle) return launch_attn_d<T, DD, kModeSingle>(tmK, tmV, p, grid, st); \
+        if (mode == kModePartitioned)                                                  \
+            return launch_attn_d<T, DD, kModePartitioned>(tmK, tmV, p, grid, st);      \
+        if (mode == kModeWorklist)                                                     \
+            return launch_attn_d<T, DD, kModeWorklist>(tmK, tmV, p, grid, st);         \
+    }
+    PA_MODES(64)
+    PA_MODES(128)
+    PA_MODES(256)
+#undef PA_MODES
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+int attn_ctas_per_sm(int D) {
+    if (D == 64) return attn_ctas_per_sm_d<T, 64>();
+    if (D == 128) return attn_ctas_per_sm_d<T, 128>();
+    if (D == 256) return attn_ctas_per_sm_d<T, 256>();
+    return 0;
+}
+
+template <typename T>
+cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st) {
+#define PA_RED(DD)                                                                            \
+    if (D == DD) {                                                                            \
+        if (compact)                                                                          \
+            pa_reduce_kernel<T, DD, true><<<grid, kReduceThreads, 0, st>>>(r);                \
+        else                                                                                  \
+            pa_reduce_kernel<T, DD, false><<<grid, kReduceThreads, 0, st>>>(r);               \
+        return cudaGetLastError();                                                            \
+    }
+    PA_RED(64)
+    PA_RED(128)
+    PA_RED(256)
+#undef PA_RED
+    return cudaErrorInvalidValue;
+}
+
+#define PA_INSTANTIATE_LAUNCHERS(T)                                                             \
+    template cudaError_t launch_attn<T>(int, int, const CUtensorMap &, const CUtensorMap &,     \
+                                        const Params &, dim3, cudaStream_t);                    \
+    template int attn_ctas_per_sm<T>(int);                                                      \
+    template cudaError_t launch_reduce<T>(int, bool, const ReduceParams &, dim3, cudaStream_t);
+
+}  // namespace pa

@@ -1,0 +1,26 @@
+// pa_launch.h -- declarations of the kernel launchers.  The attention and
+// reduce launchers are templates explicitly instantiated per dtype in
+// pa_inst_bf16.cu / pa_inst_f16.cu; the planner and gather launchers live in
+// pa_aux.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pa_types.h"
+
+namespace pa {
+
+template <typename T>
+cudaError_t launch_attn(int D, int mode, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                        const Params &p, dim3 grid, cudaStream_t st);
+template <typename T>
+int attn_ctas_per_sm(int D);
+template <typename T>
+cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st);
+
+cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);
+cudaError_t launch_gather(int D, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const GatherParams &gp, dim3 grid, cudaStream_t st);
+
+}  // namespace pa

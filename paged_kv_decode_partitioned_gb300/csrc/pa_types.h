@@ -1,0 +1,73 @@
+// pa_types.h -- constants and launch-parameter structs shared by the host
+// API and the device code of the paged-attention decode library.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kTile = 16;       // tokens per pipeline tile (the MMA M of S^T)
+constexpr int kHeadsPad = 8;    // query heads per KV head, padded to the MMA N
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s
+
+// Flags of the device status word (mirrors PA_DEV_* in pa_decode.h).
+enum : int { kBadBlock = 1, kLenClamped = 2, kWaitTimeout = 4, kTooManyParts = 8 };
+
+// Unit kinds.
+enum : int { kOutFinal = 0, kOutPartialDense = 1, kOutPartialCompact = 2 };
+
+// Grid modes of the attention kernel.
+enum : int { kModeSingle = 0, kModePartitioned = 1, kModeWorklist = 2 };
+
+struct Params {
+    const void *q;              // [S][Hq][D]
+    void *out;                  // [S][Hq][D]
+    float *tmp_out;             // dense [S][Hq][max_parts][D] or compact [slot][Hq][D]
+    float *exp_sums;            // dense [S][Hq][max_parts]    or compact [slot][Hq]
+    float *max_logits;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    const int4 *units;          // work list (seq, kvh, part, kind)
+    int *unit_counter;          // dynamic work-list cursor
+    const int *unit_count;
+    const int32_t *part_base;   // compact slot of partition 0 of each sequence, -1 if none
+    int *status;
+    int num_seqs, num_q_heads, num_kv_heads, group, block_size, max_blocks, num_blocks;
+    int partition_size, max_parts, single_pass_max_len;
+    float scale_log2;           // scale * log2(e)
+};
+
+struct ReduceParams {
+    void *out;
+    const float *tmp_out;
+    const float *exp_sums;
+    const float *max_logits;
+    const int32_t *seq_lens;
+    const int32_t *part_base;   // compact layout only
+    int *status;
+    int num_q_heads, partition_size, max_parts, single_pass_max_len, len_cap;
+};
+
+struct PlanParams {
+    const int32_t *seq_lens;
+    int4 *units;
+    int *unit_counter;
+    int *unit_count;
+    int32_t *part_base;
+    int *status;
+    int num_seqs, num_kv_heads, partition_size, single_pass_max_len, len_cap, max_parts;
+};
+
+struct GatherParams {
+    void *k_dense;
+    void *v_dense;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    int *status;
+    int num_kv_heads, block_size, max_blocks, num_blocks, max_len;
+};
+
+}  // namespace pa

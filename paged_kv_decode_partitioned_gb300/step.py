@@ -1,0 +1,119 @@
+"""A decode step with its buffers allocated once: the way a serving loop calls the library.
+
+``DecodeStep`` binds the inputs of one batch (device tensors), picks the
+entry points for a mode and owns the output, the partial buffers and the
+workspace, so that repeated calls launch kernels and nothing else.
+
+Modes (project_6 commit cd0d9e1 "qwen3_6_scripts", the forward_decode
+heuristic and the V2 description):
+
+* ``"single"``      -- ``pa_decode``: every sequence in one pass (V1);
+* ``"partitioned"`` -- ``pa_decode_partitioned`` then ``pa_partition_reduce``
+  with one partition size for every sequence (V2, phase 1 + phase 2);
+* ``"auto"``        -- ``pa_decode_auto``: sequences up to
+  ``single_pass_max_len`` tokens in one pass, longer ones partitioned and
+  merged, one work list on the device.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import (PHASE_ATTEND, PHASE_PLAN, PHASE_REDUCE, auto_workspace_bytes, decode,
+               decode_auto, decode_partitioned, num_partitions, partition_reduce)
+
+MODES = ("single", "partitioned", "auto")
+
+
+class DecodeStep:
+    def __init__(self, mode: str, query, key_cache, value_cache, block_tables, seq_lens,
+                 scale: float, *, max_seq_len: int, partition_size: int = 512,
+                 single_pass_max_len: int = 8192, out: Optional[torch.Tensor] = None):
+        if mode not in MODES:
+            raise ValueError(f"mode must be one of {MODES}")
+        self.mode = mode
+        self.query, self.key_cache, self.value_cache = query, key_cache, value_cache
+        self.block_tables, self.seq_lens = block_tables, seq_lens
+        self.scale = float(scale)
+        self.max_seq_len = int(max_seq_len)
+        self.partition_size = int(partition_size)
+        self.single_pass_max_len = int(single_pass_max_len)
+        self.out = torch.empty_like(query) if out is None else out
+        S, Hq, D = query.shape
+        Hkv = key_cache.shape[2]
+        dev = query.device
+        self.tmp_out = self.exp_sums = self.max_logits = self.workspace = None
+        if mode == "partitioned":
+            self.max_num_partitions = max(1, num_partitions(self.max_seq_len, partition_size))
+            NP = self.max_num_partitions
+            self.tmp_out = torch.empty((S, Hq, NP, D), dtype=torch.float32, device=dev)
+            self.exp_sums = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+            self.max_logits = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+        elif mode == "auto":
+            need = auto_workspace_bytes(S, Hq, Hkv, D, self.max_seq_len,
+                                        self.single_pass_max_len, partition_size)
+            self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    @property
+    def kernels_per_call(self) -> int:
+        """Kernel launches one call makes (single: 1; partitioned: 2; auto: 3 or 2)."""
+        if self.mode == "single":
+            return 1
+        if self.mode == "partitioned":
+            return 2
+        return 3 if self.max_seq_len > self.single_pass_max_len else 2
+
+    @property
+    def attention_kernel(self) -> str:
+        """Name of the kernel that reads the KV cache (the step's dominant kernel)."""
+        return {"single": "pa_attn_kernel<single>", "partitioned": "pa_attn_kernel<partitioned>",
+                "auto": "pa_attn_kernel<worklist>"}[self.mode]
+
+    def launches(self):
+        """The step as (label, callable) pairs in launch order, one kernel each.
+
+        Running them in order on one stream is exactly one ``__call__``; a
+        caller can record stream events between them to time one kernel.
+        The attention kernel's label is ``"attention"``.
+        """
+        if self.mode == "single":
+            return [("attention", self.__call__)]
+        if self.mode == "partitioned":
+            def attend():
+                decode_partitioned(self.query, self.key_cache, self.value_cache,
+                                   self.block_tables, self.seq_lens, self.scale,
+                                   self.partition_size, self.max_num_partitions, self.tmp_out,
+                                   self.exp_sums, self.max_logits)
+
+            def reduce():
+                partition_reduce(self.tmp_out, self.exp_sums, self.max_logits, self.seq_lens,
+                                 self.partition_size, out=self.out, dtype=self.out.dtype)
+            return [("attention", attend), ("reduce", reduce)]
+
+        def phase(mask):
+            return lambda: decode_auto(self.query, self.key_cache, self.value_cache,
+                                       self.block_tables, self.seq_lens, self.scale,
+                                       self.max_seq_len, self.single_pass_max_len,
+                                       self.partition_size, workspace=self.workspace,
+                                       out=self.out, phases=mask)
+        steps = [("plan", phase(PHASE_PLAN)), ("attention", phase(PHASE_ATTEND))]
+        if self.max_seq_len > self.single_pass_max_len:
+            steps.append(("reduce", phase(PHASE_REDUCE)))
+        return steps
+
+    def __call__(self) -> torch.Tensor:
+        if self.mode == "single":
+            return decode(self.query, self.key_cache, self.value_cache, self.block_tables,
+                          self.seq_lens, self.scale, out=self.out)
+        if self.mode == "partitioned":
+            decode_partitioned(self.query, self.key_cache, self.value_cache, self.block_tables,
+                               self.seq_lens, self.scale, self.partition_size,
+                               self.max_num_partitions, self.tmp_out, self.exp_sums,
+                               self.max_logits)
+            return partition_reduce(self.tmp_out, self.exp_sums, self.max_logits, self.seq_lens,
+                                    self.partition_size, out=self.out, dtype=self.out.dtype)
+        return decode_auto(self.query, self.key_cache, self.value_cache, self.block_tables,
+                           self.seq_lens, self.scale, self.max_seq_len,
+                           self.single_pass_max_len, self.partition_size,
+                           workspace=self.workspace, out=self.out)

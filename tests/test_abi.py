@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_partitioned_gb300 import build
+    build.build()
+    import paged_kv_decode_partitioned_gb300 as pa
+    return pa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("pa_decode", "pa_decode_partitioned", "pa_partition_reduce"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from libpadecode.so"
+
+
+def test_binding_signatures_cover_header():
+    import paged_kv_decode_partitioned_gb300 as pa
+    assert sorted(n for n, _, _ in pa.SIGNATURES) == declared_functions()
+
+
+def test_status_strings(lib):
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(-2) == b"PA_ERR_UNSUPPORTED"
+    assert lib.pa_status_string(-99) == b"PA_ERR_UNKNOWN"
+    assert lib.pa_version() >= 10000
+
+
+# Fake, aligned, never-dereferenced device addresses: the library must reject
+# the call on the host before it would use them.
+A = 1 << 20
+
+
+def _decode(lib, **kw):
+    args = dict(out=A, q=A, k=A, v=A, bt=A, sl=A, S=2, Hq=24, Hkv=4, D=128, bs=16, nb=10,
+                mb=4, scale=0.1, dtype=1)
+    args.update(kw)
+    return lib.pa_decode(args["out"], args["q"], args["k"], args["v"], args["bt"], args["sl"],
+                         args["S"], args["Hq"], args["Hkv"], args["D"], args["bs"], args["nb"],
+                         args["mb"], args["scale"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), -2),                 # head_dim not supported
+    (dict(bs=8), -2),                 # block_size not a multiple of 16
+    (dict(Hq=24, Hkv=2), -2),         # GQA group 12 > 8
+    (dict(Hq=10, Hkv=4), -1),         # Hq not a multiple of Hkv
+    (dict(S=-1), -1),
+    (dict(dtype=7), -1),
+    (dict(q=0), -1),                  # null query
+    (dict(out=0), -1),                # null out
+    (dict(nb=0), -1),                 # empty cache
+    (dict(k=A + 8), -3),              # misaligned cache
+    (dict(out=A + 2), -3),            # misaligned out
+    (dict(S=0), 0),                   # nothing to do
+])
+def test_decode_rejects_on_host(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def test_partitioned_rejects_partition_not_multiple_of_block(lib):
+    st = lib.pa_decode_partitioned(A, A, A, A, A, A, A, A, 2, 24, 4, 128, 16, 10, 4,
+                                   ctypes.c_float(0.1), 40, 4, 1, None)
+    assert st == -2
+    st = lib.pa_decode_partitioned(A, A, A, A, A, A, A, A, 2, 24, 4, 128, 16, 10, 4,
+                                   ctypes.c_float(0.1), 0, 4, 1, None)
+    assert st == -1
+
+
+def test_reduce_rejects_on_host(lib):
+    assert lib.pa_partition_reduce(A, A, A, A, A, 2, 24, 100, 512, 4, 1, None) == -2
+    assert lib.pa_partition_reduce(A, A, A, A, A, 2, 24, 128, 0, 4, 1, None) == -1
+    assert lib.pa_partition_reduce(A, A + 4, A, A, A, 2, 24, 128, 512, 4, 1, None) == -3
+    assert lib.pa_partition_reduce(A, A, A, A, A, 0, 24, 128, 512, 4, 1, None) == 0
+
+
+def test_auto_rejects_small_workspace_before_launch(lib):
+    need = lib.pa_auto_workspace_bytes(8, 24, 4, 128, 100000, 8192, 512)
+    assert need > 0
+    st = lib.pa_decode_auto(A, A, A, A, A, A, 8, 24, 4, 128, 16, 10, 6250, ctypes.c_float(0.1),
+                            100000, 8192, 512, A, need - 1, 1, None)
+    assert st == -4
+    st = lib.pa_decode_auto(A, A, A, A, A, A, 8, 24, 4, 128, 16, 10, 6250, ctypes.c_float(0.1),
+                            100000, 8192, 512, A + 16, need, 1, None)
+    assert st == -3
+
+
+def test_auto_workspace_size_formula(lib):
+    # 8 sequences of <=100000 tokens, P=512: 196 partition slots each.
+    S, Hq, Hkv, D, P = 8, 24, 4, 128, 512
+    need = lib.pa_auto_workspace_bytes(S, Hq, Hkv, D, 100000, 8192, P)
+    slots = S * 196
+    payload = slots * Hq * (D + 2) * 4 + slots * Hkv * 16 + S * 4
+    assert payload <= need <= payload + 6 * 256
+    # nothing longer than the single-pass limit: no partial buffers at all
+    small = lib.pa_auto_workspace_bytes(S, Hq, Hkv, D, 8192, 8192, P)
+    assert small <= S * Hkv * 16 + S * 4 + 6 * 256
+    assert lib.pa_auto_workspace_bytes(S, Hq, Hkv, D, 100, 8192, 0) == 0
+
+
+def test_default_threshold_uses_sm_count(lib):
+    # 64 seqs x 4 KV heads = 256 units: enough for 2 x 100 SMs, not for 2 x 152
+    assert lib.pa_default_single_pass_max_len(64, 4, 512, 100) == 8192
+    assert lib.pa_default_single_pass_max_len(64, 4, 512, 152) == 512
+    assert lib.pa_default_single_pass_max_len(256, 4, 512, 152) == 8192
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    """The package never imports the oracle and has no non-CUDA compute path."""
+    pkg = os.path.join(ROOT, "paged_kv_decode_partitioned_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "pa_oracle" not in text, f
