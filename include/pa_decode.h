@@ -2,17 +2,17 @@
  * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-attention decode library
  * (libpadecode.so).
  *
- * The operation (project_6, commit cd0d9e1 "qwen3_6_scripts"):
+ * The operation (page: project_6 commit cd0d9e1, "qwen3_6_scripts"):
  *   One query token per sequence attends over that sequence's keys and
  *   values, which live in a block-paged cache: logical block j of sequence s
- *   is the physical block block_tables[s][j] ("_forward_prefix_pytorch:
- *   Pre-gather ALL context K/V": key_cache[blk_ids]).  The result is
+ *   is the physical block block_tables[s][j] (the prefix-prefill rewrite's
+ *   pre-gather of context K/V through the block table).  The result is
  *       out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) * v_t,
- *   t over the sequence's seq_lens[s] tokens.  "forward_decode: V2 enabled via
- *   original heuristic" runs short sequences in one pass (V1) and long ones
- *   split into PARTITION_SIZE-token partitions (V2): "Phase 1: Per-partition
- *   attention" stores a partial output, max logit and exp-sum per partition,
- *   and "Phase 2: Cross-partition reduction (log-sum-exp)" merges them.
+ *   t over the sequence's seq_lens[s] tokens.  The forward_decode heuristic
+ *   runs short sequences in one pass (V1) and splits long ones into
+ *   partition_size-token partitions (V2): phase 1 keeps a partial output, its
+ *   maximum logit and its exp-sum per partition, and phase 2 merges the
+ *   partitions with a log-sum-exp rescale.
  *
  * Conventions shared by every entry point:
  *   - All array pointers are DEVICE pointers, owned by the caller, dense and
@@ -98,8 +98,8 @@ PA_API int pa_decode(void *out, const void *query, const void *key_cache,
               int max_blocks_per_seq, float scale, pa_dtype_t dtype, void *stream);
 
 /*
- * pa_decode_partitioned -- phase 1 of the split-KV decode ("Phase 1:
- * Per-partition attention"; "V2: splits into PARTITION_SIZE=512 chunks").
+ * pa_decode_partitioned -- phase 1 of the split-KV decode (V2 description,
+ * phase 1; the page's partition size is 512).
  * For partition p < ceil(seq_lens[s] / partition_size) covering tokens
  * [p*P, min((p+1)*P, L)) and every query head h:
  *   max_logits[s][h][p] = m_p = max_t scale * q.k_t
@@ -120,8 +120,8 @@ PA_API int pa_decode_partitioned(float *tmp_out, float *exp_sums, float *max_log
                           pa_dtype_t dtype, void *stream);
 
 /*
- * pa_partition_reduce -- phase 2 ("Phase 2: Cross-partition reduction
- * (log-sum-exp)").  With n = ceil(seq_lens[s] / partition_size):
+ * pa_partition_reduce -- phase 2 of the split-KV decode (V2 description,
+ * phase 2: the log-sum-exp merge across partitions).  With n = ceil(seq_lens[s] / partition_size):
  *   M = max_p m_p,  w_p = exp(m_p - M) * l_p,
  *   out[s][h][:] = sum_{p<n} w_p * tmp_out[s][h][p][:] / sum_{p<n} w_p
  * rounded to dtype; n = 0 gives zeros.  Reads only slots p < n.
@@ -135,11 +135,11 @@ PA_API int pa_partition_reduce(void *out, const float *tmp_out, const float *exp
 /*
  * pa_default_single_pass_max_len -- the launch heuristic's threshold.
  * Sequences longer than the returned length are partitioned by
- * pa_decode_auto.  It is the pages' 8192 ("seq_len > 8192 -> V2 (partitioned,
- * better parallelism); seq_len <= 8192 -> V1") when num_seqs * num_kv_heads
- * single-pass units fill every SM of the device at least twice, and
- * partition_size otherwise (too few units: split everything longer than one
- * partition so the SMs have work).  num_sms <= 0 queries the current device.
+ * pa_decode_auto.  It is 8192, the forward_decode heuristic's boundary
+ * between V1 and V2, when num_seqs * num_kv_heads single-pass units fill
+ * every SM of the device at least twice, and partition_size otherwise (too
+ * few units: split everything longer than one partition so that the SMs have
+ * work).  num_sms <= 0 queries the current device.
  */
 PA_API int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int partition_size,
                                    int num_sms);
@@ -155,7 +155,7 @@ PA_API size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_
 
 /*
  * pa_decode_auto -- the whole decode step with a per-sequence choice of path
- * ("forward_decode: V2 enabled via original heuristic").  A sequence with
+ * (the forward_decode heuristic).  A sequence with
  * seq_len <= single_pass_max_len is computed in one pass and written to out
  * directly; a longer one is split into ceil(L/partition_size) partitions whose
  * partials (kept in `workspace`) are merged by the log-sum-exp reduce.  The

@@ -6,10 +6,9 @@ shares no code with it; the C source ``pa_oracle.c`` is the whole computation,
 this module only compiles it with the host C compiler and marshals arrays.
 
 What each function computes, and the passage it follows, is stated in
-``pa_oracle.c`` (project_6 commit cd0d9e1 "qwen3_6_scripts": the V1/V2
-decode heuristic, "Phase 1: Per-partition attention", "Phase 2:
-Cross-partition reduction (log-sum-exp)", and the pre-gather of context K/V
-through the block table).
+``pa_oracle.c`` (page: project_6 commit cd0d9e1, "qwen3_6_scripts": the
+forward_decode heuristic, phases 1 and 2 of the V2 description, and the
+pre-gather of context K/V through the block table).
 
 Arrays are numpy arrays or CPU torch tensors.  16-bit floating-point inputs
 (query, key/value caches) are passed as their bit patterns; the oracle widens

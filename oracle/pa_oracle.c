@@ -7,29 +7,29 @@
  * or helper.  Every loop below is the textbook definition written out, with
  * no blocking, fusion or reordering beyond what the definition states.
  *
- * Passages followed (project_6, commit cd0d9e1 "qwen3_6_scripts"):
- *   [gather]   "_forward_prefix_pytorch: Pre-gather ALL context K/V":
- *              key_cache[blk_ids] -- a sequence's logical block j lives in
- *              the physical block block_tables[s][j] of the cache.
- *   [v1/v2]    "forward_decode: V2 enabled via original heuristic": V1 runs
- *              the whole KV range in one pass, V2 splits it; both compute the
- *              same attention output for the one decode query.
- *   [phase 1]  "V2: splits into PARTITION_SIZE=512 chunks ... Phase 1:
- *              Per-partition attention -- for each (seq, head, partition):
- *              QK^T, softmax, weighted V sum; store tmp_output, exp_sums,
- *              max_logits".
- *   [phase 2]  "Phase 2: Cross-partition reduction (log-sum-exp)": the global
- *              max over partitions, a per-partition rescale of
- *              exp(partition max - global max) times the partition exp-sum,
- *              and the output as the rescale-weighted sum of the partition
- *              outputs divided by the total.
+ * Passages followed (page: project_6 commit cd0d9e1, "qwen3_6_scripts"):
+ *   [gather]   the prefix-prefill rewrite's pre-gather of all context K/V:
+ *              logical block j of a sequence is the physical cache block
+ *              named by entry j of its block-table row.
+ *   [v1/v2]    the forward_decode heuristic: the single-pass path (V1) and
+ *              the partitioned path (V2) are two schedules of one attention
+ *              result for the single decode query.
+ *   [phase 1]  the V2 description, phase 1: every (sequence, head,
+ *              partition) computes its scaled logits, their softmax and the
+ *              weighted V sum, and keeps three partial results: the partial
+ *              output, the exp-sum and the maximum logit.
+ *   [phase 2]  the V2 description, phase 2: the maximum over partitions is
+ *              taken, each partition is weighted by exp(its max - that
+ *              maximum) times its exp-sum, and the output is the weighted
+ *              mean of the partial outputs.
  *
  * Readings where the pages are silent (each one is listed in the design
  * notes): query head h reads KV head h / (Hq/Hkv); max_logits are maxima of
  * the *scaled* logits scale*q.k; exp_sums are taken relative to the
- * partition's own max; tmp_output is normalised by its own exp_sum (this is
- * what makes the phase-2 rescale by the exp_sum correct); the partition
- * count is ceil(L/P); a sequence with L = 0 produces a zero output.
+ * partition's own max; the partial output is normalised by its own exp-sum
+ * (this is what makes the phase-2 weight, which multiplies by the exp-sum,
+ * correct); the partition count is ceil(L/P); a sequence with L = 0
+ * produces a zero output.
  *
  * Layouts (all row-major, element offsets):
  *   query        [S][Hq][d]                 16-bit float bit patterns

@@ -5,11 +5,11 @@ the current CUDA stream) and calls the C ABI declared in ``include/pa_decode.h``
 all of the computation runs in the library's CUDA kernels.  There is no other
 code path: if the compiled library is missing, importing a function raises.
 
-The operation (project_6, commit cd0d9e1 "qwen3_6_scripts"): one decode query
-per sequence attends over a block-paged KV cache through a per-sequence block
-table; long sequences are split into partitions whose partial results are
-merged with a log-sum-exp rescale (the "V2" path of the forward_decode
-heuristic, "Phase 1" / "Phase 2").
+The operation (page: project_6 commit cd0d9e1, "qwen3_6_scripts"): one decode
+query per sequence attends over a block-paged KV cache through a
+per-sequence block table; long sequences are split into partitions whose
+partial results are merged with a log-sum-exp rescale (the V2 path of the
+forward_decode heuristic, phases 1 and 2).
 """
 from __future__ import annotations
 

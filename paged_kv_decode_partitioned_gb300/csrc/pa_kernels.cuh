@@ -1,20 +1,19 @@
 // pa_kernels.cuh -- device code of the paged-attention decode library for
 // GB300 (sm_103a).
 //
-// The method (project_6, commit cd0d9e1 "qwen3_6_scripts"):
-//   * "forward_decode: V2 enabled via original heuristic" -- a decode query
-//     attends over its sequence's whole KV range in one pass (V1), or
-//   * "V2: splits into PARTITION_SIZE=512 chunks, runs them in parallel, then
-//     reduces with log-sum-exp": "Phase 1: Per-partition attention" stores a
-//     normalised partial output, its max logit and its exp-sum, and "Phase 2:
-//     Cross-partition reduction (log-sum-exp)" merges them with the rescale
-//     exp(partition_max - global_max) * partition_exp_sum;
-//   * "The online softmax tiling is the same as Flash Attention's
-//     partitioning" and "The reduction pattern is identical to CCCL's
-//     block_reduce_warp_reductions (combine partial statistics from
-//     independent segments)": inside a partition, each warp keeps a running
-//     (max, exp-sum, output) over its tiles, and the warps' states are merged
-//     with the same rescale as phase 2.
+// The method (page: project_6 commit cd0d9e1, "qwen3_6_scripts"):
+//   * forward_decode heuristic: a decode query attends over its sequence's
+//     whole KV range in one pass (V1) when the sequence is short, and over
+//     fixed-size partitions processed in parallel (V2) when it is long;
+//   * V2 description, phase 1: each partition yields a partial output
+//     normalised by its own exp-sum, that exp-sum, and its maximum logit;
+//     phase 2 merges the partitions with weights exp(partition max - global
+//     max) * partition exp-sum;
+//   * the same page notes that the tiling is Flash-Attention-style online
+//     softmax and that the merge is the usual combination of partial
+//     (max, sum) statistics of independent segments.  Here that merge is
+//     used twice: between the warps of a CTA inside a partition, and between
+//     partitions in the reduce kernel.
 //
 // GB300 design (how, not what):
 //   * One work unit = (sequence, KV head, token range).  All query heads that

@@ -4,7 +4,7 @@
 entry points for a mode and owns the output, the partial buffers and the
 workspace, so that repeated calls launch kernels and nothing else.
 
-Modes (project_6 commit cd0d9e1 "qwen3_6_scripts", the forward_decode
+Modes (page: project_6 commit cd0d9e1, "qwen3_6_scripts": the forward_decode
 heuristic and the V2 description):
 
 * ``"single"``      -- ``pa_decode``: every sequence in one pass (V1);

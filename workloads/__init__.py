@@ -5,11 +5,12 @@ format; it holds none of the attention arithmetic.  It is the one module that
 both the oracle-side tests and the CUDA-side tests and benchmark use, so that
 both sides see identical input bits.
 
-Shapes and value distributions follow the serving workload described in
-project_6 (commit 490ff98 "Dockerfile": "max-num-seqs 1->256: benchmark sweeps
-[128,256] concurrent seqs"; blame of optimizations/prefix_prefill_patch.py:
-head_dim 128 primary and 256 rare, GQA, fp16/bf16, max-model-len 100K) and the
-five decode workloads below.  Recipe, for every workload:
+Shapes and value distributions follow the serving workload the pages
+describe (page: project_6 commit 490ff98, "Dockerfile", the
+computility-run.yaml notes: up to 256 concurrent sequences; page: blame of
+optimizations/prefix_prefill_patch.py, the attention notes: head_dim 128
+mostly and 256 rarely, GQA, fp16 or bf16, contexts up to 100K tokens) and
+the five decode workloads below.  Recipe, for every workload:
 
 * lengths are drawn on the host with ``torch.Generator`` seeded
   ``20261200 + workload id`` (uniform integers, log-uniform rounded, or fixed);
