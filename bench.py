@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--partition-size", type=int, default=None,
                     help="override the workload's (first) partition size")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="reduced batch of the same workload rule (for profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target oracle CPU time of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -253,9 +255,9 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def make_inputs(wid, device):
+def make_inputs(wid, device, num_seqs=None):
     from workloads import WORKLOADS, make_case
-    return make_case(WORKLOADS[wid], device=device)
+    return make_case(WORKLOADS[wid], device=device, num_seqs=num_seqs)
 
 
 def run_reference(args, rank, world):
@@ -266,7 +268,7 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    case = make_inputs(args.workload, dev)
+    case = make_inputs(args.workload, dev, args.num_seqs)
     w = case.workload
     per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     sample, tok = oracle_sample_plan(case, per_step)
@@ -325,7 +327,7 @@ def main():
     import paged_kv_decode_partitioned_gb300 as pa
     from paged_kv_decode_partitioned_gb300.step import DecodeStep
 
-    case = make_inputs(args.workload, "cuda")
+    case = make_inputs(args.workload, "cuda", args.num_seqs)
     w = case.workload
     P = args.partition_size or w.partition_sizes[0]
     step = DecodeStep(w.mode, case.query, case.key_cache, case.value_cache, case.block_tables,
@@ -338,9 +340,15 @@ def main():
 
     sampler = ClockSampler(local_rank)
     sampler.start()
-    for _ in range(args.warmup):
+    # W warm-up steps, continued for at least 1 s so the clock sampler sees
+    # the same load before the timed region starts.
+    t_soak, n = time.time(), 0
+    while n < args.warmup or time.time() - t_soak < 1.0:
         flush.fill_(1)
         step()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     if pa.device_status() != 0:
         raise SystemExit("device status flags raised during warm-up")
@@ -451,7 +459,9 @@ def main():
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if w.dtype.__repr__().endswith("bfloat16") else "f16", "data": "synthetic",
-        "config": {"workload": w.name, "global_batch": world * case.num_seqs,
+        "config": {"workload": w.name if args.num_seqs is None else
+                   f"{w.name} (reduced to {case.num_seqs} sequences)",
+                   "global_batch": world * case.num_seqs,
                    "seq_len": case.max_seq_len, "total_tokens": case.total_tokens,
                    "mode": w.mode, "partition_size": P,
                    "single_pass_max_len": w.single_pass_max_len,
