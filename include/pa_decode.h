@@ -199,6 +199,45 @@ PA_API int pa_decode_auto_phases(void *out, const void *query, const void *key_c
                                  pa_dtype_t dtype, void *stream, int phases);
 
 /*
+ * pa_decode_auto_static -- pa_decode_auto for callers that cannot allocate
+ * device memory.  (The source pages describe no counterpart of this entry
+ * point; it exists for the calling environments below.)
+ *
+ * Some callers cannot hand this library a workspace: a serving engine that
+ * reserves almost all device memory for its KV cache at start-up (a later
+ * cudaMalloc would fail), a hot loop that must not pay for the implicit
+ * device-wide synchronisation a cudaMalloc / cudaFree can cause, or a plugin
+ * host that passes in its tensors but exposes no allocator.  This entry point
+ * takes the same arguments as pa_decode_auto minus the workspace, and keeps
+ * its scratch (work list and partition partials) in one fixed array of
+ * PA_STATIC_SCRATCH_BYTES in device memory that belongs to the library.
+ * Every GPU that loads the library holds that array until the process exits.
+ * The call allocates nothing.
+ *
+ *   - Limit: a batch whose pa_auto_workspace_bytes(...) exceeds
+ *     PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE_TOO_SMALL
+ *     before anything is launched (use pa_decode_auto with your own
+ *     workspace for it).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current).  Make that first call before any
+ *     stream capture.
+ *   - Sharing: all calls on a device share the one array, and it keeps the
+ *     previous call's contents; each call re-initialises what must start at
+ *     zero (the work-list cursor) in its first kernel.  Calls whose kernels
+ *     overlap on the GPU (for example on two streams) race on the array:
+ *     serialise them.
+ */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_cache,
+                                 const void *value_cache, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, int max_blocks_per_seq, float scale,
+                                 int max_seq_len, int single_pass_max_len,
+                                 int partition_size, pa_dtype_t dtype, void *stream);
+
+/*
  * pa_gather_kv -- test entry: copies each sequence's K and V rows, fetched
  * through the block table with the same tile loader the attention kernels
  * use, into dense arrays k_dense/v_dense [num_seqs][max_len][num_kv_heads]

@@ -52,6 +52,7 @@ SIGNATURES = [
                                                     _vp]),
     ("pa_decode_auto_phases", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t,
                                                            _i, _vp, _i]),
+    ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _i, _vp]),
     ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
     ("pa_device_status", _i, [_vp, ctypes.POINTER(_i)]),
     ("pa_status_string", ctypes.c_char_p, [_i]),
@@ -247,6 +248,31 @@ def decode_auto(query, key_cache, value_cache, block_tables, seq_lens, scale: fl
         else:
             st = _load().pa_decode_auto_phases(*args, int(phases))
     _check(st, "pa_decode_auto")
+    return out
+
+
+def decode_auto_static(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
+                       max_seq_len: int, single_pass_max_len: int = 8192,
+                       partition_size: int = 512,
+                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``pa_decode_auto_static``: ``decode_auto`` with the library's fixed scratch.
+
+    For callers that cannot allocate device memory: no workspace is passed and
+    none is allocated.  Batches needing more than the library's fixed scratch
+    are rejected (PaError with PA_ERR_WORKSPACE_TOO_SMALL).  Calls on one device
+    share that scratch, so calls that overlap on the GPU must be serialised.
+    """
+    S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
+    if out is None:
+        out = torch.empty_like(query)
+    with torch.cuda.device(query.device):
+        st = _load().pa_decode_auto_static(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
+            _i32(seq_lens, "seq_lens"), S, Hq, Hkv, D, bs, nb, mb, float(scale),
+            int(max_seq_len), int(single_pass_max_len), int(partition_size),
+            _dtype_code(query), _stream(query))
+    _check(st, "pa_decode_auto_static")
     return out
 
 
