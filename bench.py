@@ -356,8 +356,24 @@ def main():
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
           for _ in range(K)]
+    # Host cost of enqueuing one step (flush + launches + events), measured
+    # while the GPU is busy, sizes the stream hold below.
+    t0 = time.perf_counter()
+    for _ in range(4):
+        flush.fill_(1)
+        for _, fn in launches:
+            fn()
+    host_step = (time.perf_counter() - t0) / 4
     barrier()
     torch.cuda.synchronize()
+
+    def hold_stream(steps):
+        # A spin kernel holds the stream while the host enqueues the timed
+        # steps, so no host-side launch gap can fall inside a step's events.
+        secs = min(2.0, 1.5 * steps * host_step + 0.005)
+        torch.cuda._sleep(int(secs * 2.2e9))
+
+    hold_stream(K)
     t_wall0 = time.time()
     for k in range(K):
         flush.fill_(k & 0xFF)
@@ -410,6 +426,7 @@ def main():
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         barrier()
+        hold_stream(K)
         for k in range(K):
             flush.fill_(k & 0xFF)
             e0[k].record(stream)

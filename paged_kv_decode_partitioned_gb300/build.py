@@ -41,7 +41,7 @@ def _inputs() -> list:
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or os.environ.get("PA_NVCC_FLAGS"):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _inputs())
@@ -58,6 +58,8 @@ def build(force: bool = False, ptxas_verbose: bool = False, verbose: bool = Fals
               "-I", INCLUDE, "-I", CSRC]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
+    # extra nvcc flags (e.g. the -DPA_NW_D256=2 CTA-shape overrides used when tuning)
+    common += os.environ.get("PA_NVCC_FLAGS", "").split()
 
     def compile_one(src: str):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

@@ -121,6 +121,19 @@ int check_attention(const Shape &s, pa_dtype_t dtype, const void *query, const v
     return PA_OK;
 }
 
+// CTAs per (sequence, KV head) of the single-pass grid: enough that the
+// launch has about PA_SINGLE_CLUSTER_FACTOR times as many CTAs as can be
+// resident, at most 8 (the portable cluster size).
+#ifndef PA_SINGLE_CLUSTER_FACTOR
+#define PA_SINGLE_CLUSTER_FACTOR 2
+#endif
+int single_pass_cluster(int units, int resident_ctas) {
+    if (units <= 0 || resident_ctas <= 0) return 1;
+    const int64_t want = static_cast<int64_t>(PA_SINGLE_CLUSTER_FACTOR) * resident_ctas;
+    const int64_t c = (want + units - 1) / units;
+    return c < 1 ? 1 : (c > 8 ? 8 : static_cast<int>(c));
+}
+
 Params base_params(const Shape &s, const void *query, const int32_t *bt, const int32_t *sl,
                    float scale, int *status) {
     Params p{};
@@ -136,6 +149,7 @@ Params base_params(const Shape &s, const void *query, const int32_t *bt, const i
     p.max_blocks = s.max_blocks;
     p.num_blocks = s.num_blocks;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.cluster = 1;
     return p;
 }
 
@@ -237,7 +251,12 @@ int pa_decode(void *out, const void *query, const void *key_cache, const void *v
         return rc;
     Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
     p.out = out;
-    const dim3 grid(num_kv_heads, num_seqs);
+    // Split each (sequence, KV head) over a cluster of CTAs when the batch has
+    // too few units to keep every SM streaming (few or unequal sequences).
+    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim)
+                                        : attn_ctas_per_sm<__half>(head_dim);
+    p.cluster = single_pass_cluster(num_seqs * num_kv_heads, per_sm * di->num_sms);
+    const dim3 grid(p.cluster, num_kv_heads, num_seqs);
     return attn(dtype, head_dim, kModeSingle, tk, tv, p, grid, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? PA_OK

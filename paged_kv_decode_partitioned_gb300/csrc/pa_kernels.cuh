@@ -178,6 +178,30 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
     return static_cast<uint32_t>(r128 * 128 + ((chunk ^ (r128 & 7)) << 4) + ((col & 7) << 1));
 }
 
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ int clamp_len(const int32_t *seq_lens, int s, int cap, int *status) {
     int L = __ldg(seq_lens + s);
     if (L < 0 || L > cap) {
@@ -196,34 +220,44 @@ struct Smem {
     static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
     static constexpr int kStagesBytes = NW * NS * kStageBytes;
     static constexpr int kMergeBytes = NW * kHeadsPad * (D + 2) * 4;
+    // CTA result handed to the cluster leader: o [8][D], m [8], l [8], abort flag
+    static constexpr int kClusterOffset = (kMergeBytes + 15) / 16 * 16;
+    static constexpr int kClusterBytes = kHeadsPad * (D + 2) * 4 + 16;
+    static constexpr int kUsed = kClusterOffset + kClusterBytes;
     static constexpr int kBarOffset =
-        ((kStagesBytes > kMergeBytes ? kStagesBytes : kMergeBytes) + 15) / 16 * 16;
+        ((kStagesBytes > kUsed ? kStagesBytes : kUsed) + 15) / 16 * 16;
     static constexpr int kBytes = kBarOffset + NW * NS * 8 + 16;
     static constexpr int kLaunchBytes = kBytes + 1024;          // slack for 1024-byte alignment
 };
 
 // ---------------------------------------------------------------------------
 // One work unit: tokens [t0, t1) of (seq, kvh), all heads of the GQA group.
-// Returns false if a pipeline wait gave up (the CTA must stop).
+// With a cluster of `csize` CTAs (single-pass grid only), CTA `crank` takes
+// every csize-th group of NW tiles and the leader merges the CTAs' states
+// through distributed shared memory.  Returns false if a pipeline wait gave
+// up (the CTA must stop).
 // ---------------------------------------------------------------------------
 template <typename T, int D, int NW, int NS>
 __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *tmK,
                                             const CUtensorMap *tmV, uint8_t *smem, uint32_t bar0,
                                             uint32_t &uses, int seq, int kvh, int t0, int t1,
-                                            int out_kind, int part, int slot, int *s_abort) {
+                                            int out_kind, int part, int slot, int *s_abort,
+                                            int crank = 0, int csize = 1) {
     using SM = Smem<D, NW, NS>;
     constexpr int KT = D / 16;   // k-steps of S^T, m-tiles of O^T
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = p.group;
     const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-    const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+    const int woff = crank * NW + warp;    // this warp's first tile
+    const int wstride = csize * NW;        // tiles between two of this warp's tiles
+    const int my_tiles = woff < ntiles ? (ntiles - woff + wstride - 1) / wstride : 0;
     const int32_t *bt_row = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
 
     // Block-table window: lane l holds the physical block of local tile base+l.
     auto fetch = [&](int i) -> int {
         if (i >= my_tiles) return 0;
-        const int tok = t0 + (warp + i * NW) * kTile;
+        const int tok = t0 + (woff + i * wstride) * kTile;
         const int b = __ldg(bt_row + tok / p.block_size);
         if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
             atomicOr(p.status, kBadBlock);
@@ -248,7 +282,7 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
             const uint32_t st = (uses + i) % NS;
             const uint32_t bar = bar0 + (warp * NS + st) * 8;
             const uint32_t dk = stage0 + st * SM::kStageBytes;
-            const int row = (t0 + (warp + i * NW) * kTile) % p.block_size;
+            const int row = (t0 + (woff + i * wstride) * kTile) % p.block_size;
             mbar_expect_tx(bar, SM::kStageBytes);
             tma_load_5d(dk, tmK, bar, 0, 0, kvh, row, b);
             tma_load_5d(dk + SM::kTileBytes, tmV, bar, 0, 0, kvh, row, b);
@@ -296,7 +330,7 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
         }
         const uint32_t kb = stage0 + st * SM::kStageBytes;
         const uint32_t vb = kb + SM::kTileBytes;
-        const int tt = t0 + (warp + i * NW) * kTile;
+        const int tt = t0 + (woff + i * wstride) * kTile;
         const int nvalid = min(kTile, t1 - tt);
         if (nvalid < kTile) {
             // Rows past the sequence end hold whatever the block holds; zero
@@ -392,6 +426,13 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
     __syncthreads();
     const bool write = (*s_abort == 0);
     const int Hq = p.num_q_heads;
+    // Cluster mode: each CTA parks its merged state for the leader instead of
+    // writing the output.
+    const bool to_leader = csize > 1;
+    float *cl_o = reinterpret_cast<float *>(smem + SM::kClusterOffset);   // [8][D]
+    float *cl_m = cl_o + kHeadsPad * D;                                    // [8]
+    float *cl_l = cl_m + kHeadsPad;                                        // [8]
+    int *cl_abort = reinterpret_cast<int *>(cl_l + kHeadsPad);
     for (int e = threadIdx.x; e < g * D && write; e += NW * 32) {
         const int h = e / D, dim = e - (e / D) * D;
         float M = -INFINITY;
@@ -408,7 +449,13 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
         }
         const float res = Ls > 0.f ? acc / Ls : 0.f;
         const int head = kvh * g + h;
-        if (out_kind == kOutFinal) {
+        if (to_leader) {
+            cl_o[h * D + dim] = res;
+            if (dim == 0) {
+                cl_m[h] = M;
+                cl_l[h] = Ls;
+            }
+        } else if (out_kind == kOutFinal) {
             static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + head) * D + dim] =
                 Mma<T>::cvt(res);
         } else {
@@ -423,6 +470,34 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
                 p.max_logits[srow] = M == -INFINITY ? -INFINITY : M * kLn2;
             }
         }
+    }
+    if (to_leader) {
+        if (threadIdx.x == 0) *cl_abort = write ? 0 : 1;
+        cluster_sync();   // every CTA's state is in its shared memory
+        if (crank == 0) {
+            bool any_abort = false;
+            for (int r = 0; r < csize; ++r)
+                any_abort |= dsmem_ld_s32(dsmem_addr(smem_u32(cl_abort), r)) != 0;
+            for (int e = threadIdx.x; e < g * D && !any_abort; e += NW * 32) {
+                const int h = e / D, dim = e - (e / D) * D;
+                float M = -INFINITY;
+                for (int r = 0; r < csize; ++r)
+                    M = fmaxf(M, dsmem_ld_f32(dsmem_addr(smem_u32(cl_m + h), r)));
+                float Ls = 0.f, acc = 0.f;
+                if (M != -INFINITY) {
+                    for (int r = 0; r < csize; ++r) {
+                        const float mr = dsmem_ld_f32(dsmem_addr(smem_u32(cl_m + h), r));
+                        const float wt =
+                            ex2(mr - M) * dsmem_ld_f32(dsmem_addr(smem_u32(cl_l + h), r));
+                        Ls += wt;
+                        acc += wt * dsmem_ld_f32(dsmem_addr(smem_u32(cl_o + h * D + dim), r));
+                    }
+                }
+                static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + kvh * g + h) * D + dim] =
+                    Mma<T>::cvt(Ls > 0.f ? acc / Ls : 0.f);
+            }
+        }
+        cluster_sync();   // the leader has finished reading the other CTAs
     }
     // The merge wrote this memory through the generic proxy; order those
     // writes before any later TMA into it, then let every thread finish.
@@ -457,10 +532,11 @@ __global__ void __launch_bounds__(NW * 32)
     uint32_t uses = 0;
     const int cap = p.max_blocks * p.block_size;
     if constexpr (MODE == kModeSingle) {
-        const int kvh = blockIdx.x, seq = blockIdx.y;
+        // grid (cluster size, Hkv, S); the CTAs of one cluster share a unit
+        const int crank = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
         const int L = clamp_len(p.seq_lens, seq, cap, p.status);
         attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, 0, L, kOutFinal, 0,
-                                  0, &s_abort);
+                                  0, &s_abort, crank, p.cluster);
     } else if constexpr (MODE == kModePartitioned) {
         const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
         const int L = clamp_len(p.seq_lens, seq, cap, p.status);
@@ -511,6 +587,7 @@ __global__ void __launch_bounds__(NW * 32)
 // ---------------------------------------------------------------------------
 constexpr int kReduceThreads = 256;
 constexpr int kReduceChunk = 2048;   // partition weights staged per pass
+constexpr int kReduceUnroll = 8;     // partitions loaded per thread before accumulating
 
 template <typename T, int D, bool COMPACT>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
@@ -567,25 +644,38 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
             total += w;
         }
         __syncthreads();
-        // warp `warp` takes partitions warp, warp+NWR, ...; lane takes dims lane*VEC...
-#pragma unroll 4
-        for (int q = warp; q < cn; q += NWR) {
-            const float w = s_w[q];
-            const float *src = r.tmp_out + (stat0 + (c0 + q) * pstride) * D + lane * VEC;
-            if constexpr (VEC == 2) {
-                const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-            } else {
+        // warp `warp` takes partitions warp, warp+NWR, ...; lane takes dims
+        // lane*VEC ... +VEC-1.  kReduceUnroll partitions are loaded before any
+        // is accumulated so each thread keeps that many loads in flight.
+        for (int q0 = warp; q0 < cn; q0 += NWR * kReduceUnroll) {
+            float x[kReduceUnroll][VEC];
+            float wq[kReduceUnroll];
 #pragma unroll
-                for (int v = 0; v < VEC; v += 4) {
-                    const float4 x = __ldg(reinterpret_cast<const float4 *>(src + v));
-                    acc[v] += w * x.x;
-                    acc[v + 1] += w * x.y;
-                    acc[v + 2] += w * x.z;
-                    acc[v + 3] += w * x.w;
+            for (int u = 0; u < kReduceUnroll; ++u) {
+                // past the chunk end: reload the last partition with weight 0
+                const int q = q0 + u * NWR;
+                const int qc = q < cn ? q : cn - 1;
+                wq[u] = q < cn ? s_w[q] : 0.f;
+                const float *src = r.tmp_out + (stat0 + (c0 + qc) * pstride) * D + lane * VEC;
+#pragma unroll
+                for (int v = 0; v < VEC; v += (VEC >= 4 ? 4 : 2)) {
+                    if constexpr (VEC >= 4) {
+                        const float4 t = __ldg(reinterpret_cast<const float4 *>(src + v));
+                        x[u][v] = t.x;
+                        x[u][v + 1] = t.y;
+                        x[u][v + 2] = t.z;
+                        x[u][v + 3] = t.w;
+                    } else {
+                        const float2 t = __ldg(reinterpret_cast<const float2 *>(src + v));
+                        x[u][v] = t.x;
+                        x[u][v + 1] = t.y;
+                    }
                 }
             }
+#pragma unroll
+            for (int u = 0; u < kReduceUnroll; ++u)
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) acc[v] += wq[u] * x[u][v];
         }
         __syncthreads();
     }

@@ -10,11 +10,30 @@
 
 namespace pa {
 
-// CTA shape of the attention kernel per head_dim: NW warps, NS stages per warp.
+// CTA shape of the attention kernel per head_dim: NW warps, NS stages per warp
+// (build-time overridable with -DPA_NW_D<D>=... -DPA_NS_D<D>=... for tuning).
+#ifndef PA_NW_D64
+#define PA_NW_D64 4
+#endif
+#ifndef PA_NS_D64
+#define PA_NS_D64 4
+#endif
+#ifndef PA_NW_D128
+#define PA_NW_D128 4
+#endif
+#ifndef PA_NS_D128
+#define PA_NS_D128 2
+#endif
+#ifndef PA_NW_D256
+#define PA_NW_D256 4
+#endif
+#ifndef PA_NS_D256
+#define PA_NS_D256 1   // 64 KB of stages: 3 CTAs (12 warps) per SM beat 1 CTA with 2 stages
+#endif
 template <int D> struct AttnCfg;
-template <> struct AttnCfg<64> { static constexpr int NW = 4, NS = 4; };
-template <> struct AttnCfg<128> { static constexpr int NW = 4, NS = 2; };
-template <> struct AttnCfg<256> { static constexpr int NW = 4, NS = 2; };
+template <> struct AttnCfg<64> { static constexpr int NW = PA_NW_D64, NS = PA_NS_D64; };
+template <> struct AttnCfg<128> { static constexpr int NW = PA_NW_D128, NS = PA_NS_D128; };
+template <> struct AttnCfg<256> { static constexpr int NW = PA_NW_D256, NS = PA_NS_D256; };
 
 constexpr int kMaxDevices = 64;
 
@@ -40,6 +59,24 @@ inline cudaError_t launch_attn_d(const CUtensorMap &tmK, const CUtensorMap &tmV,
     auto k = pa_attn_kernel<T, D, C::NW, C::NS, MODE>;
     cudaError_t e = ensure_smem(k, SM::kLaunchBytes, done);
     if (e != cudaSuccess) return e;
+    if (MODE == kModeSingle && p.cluster > 1) {
+        // the p.cluster CTAs of one unit form a thread-block cluster
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(C::NW * 32);
+        cfg.dynamicSmemBytes = SM::kLaunchBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k, tmK, tmV, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     k<<<grid, C::NW * 32, SM::kLaunchBytes, st>>>(tmK, tmV, p);
     return cudaGetLastError();
 }

@@ -37,6 +37,7 @@ struct Params {
     int *status;
     int num_seqs, num_q_heads, num_kv_heads, group, block_size, max_blocks, num_blocks;
     int partition_size, max_parts, single_pass_max_len;
+    int cluster;                // CTAs per unit of the single-pass grid (1..8)
     float scale_log2;           // scale * log2(e)
 };
 
