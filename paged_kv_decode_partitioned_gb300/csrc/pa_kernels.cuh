@@ -584,17 +584,21 @@ __global__ void __launch_bounds__(NW * 32)
 
 // ---------------------------------------------------------------------------
 // Phase 2: log-sum-exp merge of the partials of one (sequence, query head).
+// The merge weights are exp(m_p - M) * l_p with M the maximum over the
+// partitions.  Each warp streams its partitions once, keeping a running
+// maximum and rescaling its running sums when the maximum grows (the same
+// value up to rounding), then the warps' states are merged with the same
+// weights.  Loads of kReduceUnroll partitions are issued before any is used.
 // ---------------------------------------------------------------------------
-constexpr int kReduceThreads = 256;
-constexpr int kReduceChunk = 2048;   // partition weights staged per pass
-constexpr int kReduceUnroll = 8;     // partitions loaded per thread before accumulating
+constexpr int kReduceThreads = 512;
+constexpr int kReduceUnroll = 4;
 
 template <typename T, int D, bool COMPACT>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
     constexpr int NWR = kReduceThreads / 32;
-    constexpr int VEC = D / 32;   // floats per lane
-    __shared__ float s_w[kReduceChunk];
-    __shared__ float s_red[NWR];
+    constexpr int VEC = D / 32;   // floats per lane: 2, 4 or 8
+    __shared__ float s_m[NWR];
+    __shared__ float s_l[NWR];
     __shared__ float s_acc[NWR][D];
     const int h = blockIdx.x, s = blockIdx.y;
     const int Hq = r.num_q_heads;
@@ -618,80 +622,69 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
         for (int i = threadIdx.x; i < D; i += kReduceThreads) out[i] = Mma<T>::cvt(0.f);
         return;
     }
-    // global max of the partition maxima
-    float M = -INFINITY;
-    for (int q = threadIdx.x; q < n; q += kReduceThreads)
-        M = fmaxf(M, __ldg(r.max_logits + stat0 + q * pstride));
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-    if (lane == 0) s_red[warp] = M;
-    __syncthreads();
-    M = s_red[0];
-#pragma unroll
-    for (int w = 1; w < NWR; ++w) M = fmaxf(M, s_red[w]);
-    __syncthreads();
 
+    float m_run = -INFINITY, l_run = 0.f;   // log2-domain running max, weight sum
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    float total = 0.f;   // per-thread part of sum_p w_p (threads stride the partitions)
-    for (int c0 = 0; c0 < n; c0 += kReduceChunk) {
-        const int cn = min(kReduceChunk, n - c0);
-        for (int q = threadIdx.x; q < cn; q += kReduceThreads) {
-            const size_t si = stat0 + (c0 + q) * pstride;
-            const float w = ex2((__ldg(r.max_logits + si) - M) * kLog2e) * __ldg(r.exp_sums + si);
-            s_w[q] = w;
-            total += w;
-        }
-        __syncthreads();
-        // warp `warp` takes partitions warp, warp+NWR, ...; lane takes dims
-        // lane*VEC ... +VEC-1.  kReduceUnroll partitions are loaded before any
-        // is accumulated so each thread keeps that many loads in flight.
-        for (int q0 = warp; q0 < cn; q0 += NWR * kReduceUnroll) {
-            float x[kReduceUnroll][VEC];
-            float wq[kReduceUnroll];
+    for (int q0 = warp; q0 < n; q0 += NWR * kReduceUnroll) {
+        float mq[kReduceUnroll], lq[kReduceUnroll], x[kReduceUnroll][VEC];
 #pragma unroll
-            for (int u = 0; u < kReduceUnroll; ++u) {
-                // past the chunk end: reload the last partition with weight 0
-                const int q = q0 + u * NWR;
-                const int qc = q < cn ? q : cn - 1;
-                wq[u] = q < cn ? s_w[q] : 0.f;
-                const float *src = r.tmp_out + (stat0 + (c0 + qc) * pstride) * D + lane * VEC;
+        for (int u = 0; u < kReduceUnroll; ++u) {
+            const int q = q0 + u * NWR;
+            const int qc = q < n ? q : n - 1;   // in range; its weight is dropped below
+            const size_t si = stat0 + qc * pstride;
+            mq[u] = q < n ? __ldg(r.max_logits + si) * kLog2e : -INFINITY;
+            lq[u] = __ldg(r.exp_sums + si);
+            const float *src = r.tmp_out + si * D + lane * VEC;
 #pragma unroll
-                for (int v = 0; v < VEC; v += (VEC >= 4 ? 4 : 2)) {
-                    if constexpr (VEC >= 4) {
-                        const float4 t = __ldg(reinterpret_cast<const float4 *>(src + v));
-                        x[u][v] = t.x;
-                        x[u][v + 1] = t.y;
-                        x[u][v + 2] = t.z;
-                        x[u][v + 3] = t.w;
-                    } else {
-                        const float2 t = __ldg(reinterpret_cast<const float2 *>(src + v));
-                        x[u][v] = t.x;
-                        x[u][v + 1] = t.y;
-                    }
+            for (int v = 0; v < VEC; v += (VEC >= 4 ? 4 : 2)) {
+                if constexpr (VEC >= 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4 *>(src + v));
+                    x[u][v] = t.x;
+                    x[u][v + 1] = t.y;
+                    x[u][v + 2] = t.z;
+                    x[u][v + 3] = t.w;
+                } else {
+                    const float2 t = __ldg(reinterpret_cast<const float2 *>(src + v));
+                    x[u][v] = t.x;
+                    x[u][v + 1] = t.y;
                 }
             }
-#pragma unroll
-            for (int u = 0; u < kReduceUnroll; ++u)
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) acc[v] += wq[u] * x[u][v];
         }
-        __syncthreads();
-    }
+        float mb = m_run;
 #pragma unroll
-    for (int x = 16; x > 0; x >>= 1) total += __shfl_xor_sync(0xffffffffu, total, x);
-    if (lane == 0) s_red[warp] = total;
+        for (int u = 0; u < kReduceUnroll; ++u) mb = fmaxf(mb, mq[u]);
+        const float sc = ex2(m_run - mb);   // 0 while nothing is accumulated yet
+        l_run *= sc;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] *= sc;
+#pragma unroll
+        for (int u = 0; u < kReduceUnroll; ++u) {
+            const float w = ex2(mq[u] - mb) * lq[u];   // 0 for dropped slots
+            l_run += w;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] += w * x[u][v];
+        }
+        m_run = mb;
+    }
+    if (lane == 0) {
+        s_m[warp] = m_run;
+        s_l[warp] = l_run;
+    }
 #pragma unroll
     for (int v = 0; v < VEC; ++v) s_acc[warp][lane * VEC + v] = acc[v];
     __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWR; ++w) M = fmaxf(M, s_m[w]);
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWR; ++w) tot += s_red[w];
+    for (int w = 0; w < NWR; ++w) tot += ex2(s_m[w] - M) * s_l[w];
     for (int i = threadIdx.x; i < D; i += kReduceThreads) {
         float a = 0.f;
 #pragma unroll
-        for (int w = 0; w < NWR; ++w) a += s_acc[w][i];
+        for (int w = 0; w < NWR; ++w) a += ex2(s_m[w] - M) * s_acc[w][i];
         out[i] = Mma<T>::cvt(tot > 0.f ? a / tot : 0.f);
     }
 }
