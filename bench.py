@@ -395,9 +395,13 @@ def main():
     t_wall1 = time.time()
     rows = sampler.stop()
 
-    attn_idx = [name for name, _ in launches].index("attention")
+    names = [name for name, _ in launches]
+    attn_idx = names.index("attention")
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
     attn_ms = [ev[k][attn_idx].elapsed_time(ev[k][attn_idx + 1]) for k in range(K)]
+    # mean event time of each launch of the step (includes the gap before it)
+    launch_ms = {n: round(sum(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)) / K, 4)
+                 for j, n in enumerate(names)}
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -506,6 +510,7 @@ def main():
                      "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "launch_ms": launch_ms,
         "gpu_launches": K * len(launches),
         "clocks": clocks,
     }

@@ -13,6 +13,10 @@
 #include "pa_decode.h"
 #include "pa_launch.h"
 
+#ifndef PA_TILE_PIECES
+#define PA_TILE_PIECES 1
+#endif
+
 namespace {
 
 using namespace pa;
@@ -70,9 +74,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 5-D view of a cache [num_blocks][bs][Hkv][D] for TMA: (64-element piece,
-// piece index, KV head, row in block, block); one box = 16 rows of one KV
-// head, 128-byte swizzled.  Out-of-range boxes read zeros.
+// 5-D view of a cache [num_blocks][bs][Hkv][D] for TMA: (element within a
+// 64-element piece, piece index, KV head, row in block, block); one box = one
+// 64-element piece of 16 rows of one KV head (2 KB), 128-byte swizzled.
+// Out-of-range boxes read zeros.
 int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv, int bs,
                    int num_blocks) {
     EncodeTiledFn fn = encode_fn();
@@ -82,7 +87,11 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
                           static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(num_blocks)};
     cuuint64_t strides[4] = {64 * e, D * e, static_cast<cuuint64_t>(Hkv) * D * e,
                              static_cast<cuuint64_t>(bs) * Hkv * D * e};
+#if PA_TILE_PIECES
+    cuuint32_t box[5] = {64, 1, 1, static_cast<cuuint32_t>(kTile), 1};
+#else
     cuuint32_t box[5] = {64, static_cast<cuuint32_t>(D / 64), 1, static_cast<cuuint32_t>(kTile), 1};
+#endif
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -167,7 +176,7 @@ cudaError_t reduce(pa_dtype_t dt, int D, bool compact, const ReduceParams &r, di
 
 // Workspace layout of pa_decode_auto.
 struct AutoLayout {
-    size_t counter, units, part_base, exp_sums, max_logits, tmp_out, total;
+    size_t counter, units, part_base, pseq_list, exp_sums, max_logits, tmp_out, total;
     int max_parts, max_slots, max_units;
 };
 
@@ -183,11 +192,13 @@ bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P,
     L->max_slots = static_cast<int>(slots);
     L->max_units = static_cast<int>(units);
     size_t off = 0;
-    L->counter = off;
-    off = align256(off + 2 * sizeof(int));
+    L->counter = off;   // work-list cursor, unit count, partitioned-sequence count
+    off = align256(off + 3 * sizeof(int));
     L->units = off;
     off = align256(off + static_cast<size_t>(units) * sizeof(int4));
     L->part_base = off;
+    off = align256(off + static_cast<size_t>(S) * sizeof(int32_t));
+    L->pseq_list = off;
     off = align256(off + static_cast<size_t>(S) * sizeof(int32_t));
     L->exp_sums = off;
     off = align256(off + static_cast<size_t>(slots) * Hq * sizeof(float));
@@ -403,6 +414,7 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     int *counter = reinterpret_cast<int *>(ws + L.counter);
     int4 *units = reinterpret_cast<int4 *>(ws + L.units);
     int32_t *part_base = reinterpret_cast<int32_t *>(ws + L.part_base);
+    int32_t *pseq_list = reinterpret_cast<int32_t *>(ws + L.pseq_list);
     float *es = reinterpret_cast<float *>(ws + L.exp_sums);
     float *ml = reinterpret_cast<float *>(ws + L.max_logits);
     float *tmp = reinterpret_cast<float *>(ws + L.tmp_out);
@@ -415,6 +427,8 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     pp.unit_counter = counter;
     pp.unit_count = counter + 1;
     pp.part_base = part_base;
+    pp.pseq_list = pseq_list;
+    pp.pseq_count = counter + 2;
     pp.status = di->status;
     pp.num_seqs = num_seqs;
     pp.num_kv_heads = num_kv_heads;
@@ -455,13 +469,19 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
         r.max_logits = ml;
         r.seq_lens = seq_lens;
         r.part_base = part_base;
+        r.pseq_list = pseq_list;
+        r.pseq_count = counter + 2;
         r.status = di->status;
         r.num_q_heads = num_q_heads;
         r.partition_size = partition_size;
         r.max_parts = L.max_parts;
         r.single_pass_max_len = thr;
         r.len_cap = len_cap;
-        if (reduce(dtype, head_dim, true, r, dim3(num_q_heads, num_seqs), st) != cudaSuccess)
+        // about 4 CTAs per SM, each looping over partitioned sequences
+        int rows = (4 * di->num_sms + num_q_heads - 1) / num_q_heads;
+        if (rows > num_seqs) rows = num_seqs;
+        if (rows < 1) rows = 1;
+        if (reduce(dtype, head_dim, true, r, dim3(num_q_heads, rows), st) != cudaSuccess)
             return PA_ERR_CUDA;
     }
     return PA_OK;

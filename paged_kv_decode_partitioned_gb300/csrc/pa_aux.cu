@@ -75,11 +75,15 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
         const int base_unit = singles_all * Hkv + slots_before * Hkv;
         for (int k = threadIdx.x; k < np * Hkv; k += kPlanThreads)
             pp.units[base_unit + k] = make_int4(s, k % Hkv, k / Hkv, kOutPartialCompact);
-        if (threadIdx.x == 0) pp.part_base[s] = slots_before;
+        if (threadIdx.x == 0) {
+            pp.part_base[s] = slots_before;
+            pp.pseq_list[s - singles_before] = s;   // rank among the partitioned sequences
+        }
     }
     if (s == 0 && threadIdx.x == 0) {
         *pp.unit_count = (singles_all + slots_all) * Hkv;
         *pp.unit_counter = 0;
+        *pp.pseq_count = pp.num_seqs - singles_all;
     }
 }
 
@@ -113,8 +117,8 @@ __global__ void __launch_bounds__(32)
         if (static_cast<unsigned>(b) >= static_cast<unsigned>(gp.num_blocks))
             atomicOr(gp.status, kBadBlock);
         mbar_expect_tx(bar, 2 * kTileBytes);
-        tma_load_5d(smem_u32(smem), &tmK, bar, 0, 0, kvh, tt % gp.block_size, b);
-        tma_load_5d(smem_u32(smem) + kTileBytes, &tmV, bar, 0, 0, kvh, tt % gp.block_size, b);
+        tma_load_tile<D>(smem_u32(smem), &tmK, bar, kvh, tt % gp.block_size, b);
+        tma_load_tile<D>(smem_u32(smem) + kTileBytes, &tmV, bar, kvh, tt % gp.block_size, b);
     }
     if (!mbar_wait_bounded(bar, 0)) {
         if (lane == 0) atomicOr(gp.status, kWaitTimeout);

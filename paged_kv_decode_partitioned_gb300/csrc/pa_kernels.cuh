@@ -167,15 +167,53 @@ template <> struct Mma<__half> {
     static __device__ __forceinline__ __half cvt(float x) { return __float2half_rn(x); }
 };
 
-// Byte offset of element (row, col) of one 16-row tile as TMA lays it out:
-// rows of D elements split into 64-element (128-byte) pieces, row-major over
-// (row, piece), with the 128-byte swizzle (16-byte chunk index XOR the
-// 128-byte row index mod 8).  Tiles start on 1024-byte boundaries.
+// Byte offset of element (row, col) of one 16-row tile as the TMA loads lay
+// it out.  Piecewise layout (default): one 2 KB block per 64-element
+// (128-byte) piece of the head dimension, holding that piece of the 16 rows
+// as consecutive 128-byte rows, with the 128-byte swizzle (16-byte chunk
+// index XOR row mod 8): the eight rows an ldmatrix reads hit eight different
+// bank groups.  Row-major layout (PA_TILE_PIECES=0): the 16 rows of D
+// elements one after the other, one TMA per tile; rows of 256 or 512 bytes
+// make the swizzle repeat every 4 or 2 rows (2- or 4-way bank conflicts).
+// Tiles start on 1024-byte boundaries.
+#ifndef PA_TILE_PIECES
+#define PA_TILE_PIECES 1
+#endif
+constexpr int kPieceBytes = kTile * 128;
+constexpr bool kPiecewise = PA_TILE_PIECES != 0;
+
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int col) {
-    const int r128 = row * (D / 64) + (col >> 6);
     const int chunk = (col & 63) >> 3;
-    return static_cast<uint32_t>(r128 * 128 + ((chunk ^ (r128 & 7)) << 4) + ((col & 7) << 1));
+    if constexpr (kPiecewise) {
+        return static_cast<uint32_t>((col >> 6) * kPieceBytes + row * 128 +
+                                     ((chunk ^ (row & 7)) << 4) + ((col & 7) << 1));
+    } else {
+        const int r128 = row * (D / 64) + (col >> 6);
+        return static_cast<uint32_t>(r128 * 128 + ((chunk ^ (r128 & 7)) << 4) + ((col & 7) << 1));
+    }
+}
+
+// Byte offset of row `row` of piece `c` (the V rows past a sequence end are
+// zeroed through it): contiguous 128-byte rows in both layouts.
+template <int D>
+__device__ __forceinline__ uint32_t row_piece_offset(int row, int c) {
+    return kPiecewise ? static_cast<uint32_t>(c * kPieceBytes + row * 128)
+                      : static_cast<uint32_t>((row * (D / 64) + c) * 128);
+}
+
+// Load one 16-row tile of (block b, rows row..row+15, KV head kvh), all
+// completing on `bar`: one TMA per 64-element piece, or one for the tile.
+template <int D>
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                              int kvh, int row, int b) {
+    if constexpr (kPiecewise) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_5d(dst + c * kPieceBytes, map, bar, 0, c, kvh, row, b);
+    } else {
+        tma_load_5d(dst, map, bar, 0, 0, kvh, row, b);
+    }
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -284,8 +322,8 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
             const uint32_t dk = stage0 + st * SM::kStageBytes;
             const int row = (t0 + (woff + i * wstride) * kTile) % p.block_size;
             mbar_expect_tx(bar, SM::kStageBytes);
-            tma_load_5d(dk, tmK, bar, 0, 0, kvh, row, b);
-            tma_load_5d(dk + SM::kTileBytes, tmV, bar, 0, 0, kvh, row, b);
+            tma_load_tile<D>(dk, tmK, bar, kvh, row, b);
+            tma_load_tile<D>(dk + SM::kTileBytes, tmV, bar, kvh, row, b);
         }
     };
 
@@ -335,10 +373,14 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
         if (nvalid < kTile) {
             // Rows past the sequence end hold whatever the block holds; zero
             // their V so that 0 * garbage cannot reach the accumulator.
-            uint8_t *vrow = smem + (vb - smem_u32(smem));
-            const int first = nvalid * D * 2, bytes = kTile * D * 2 - first;
-            for (int off = lane * 16; off < bytes; off += 32 * 16)
-                *reinterpret_cast<uint4 *>(vrow + first + off) = make_uint4(0, 0, 0, 0);
+            uint8_t *vtile = smem + (vb - smem_u32(smem));
+            // (16 - nvalid) rows x (D/64) pieces of 128 bytes, 8 uint4 each
+            const int n16 = (kTile - nvalid) * (D / 64) * 8;
+            for (int e = lane; e < n16; e += 32) {
+                const int rp = e >> 3, row = nvalid + rp / (D / 64), c = rp % (D / 64);
+                *reinterpret_cast<uint4 *>(vtile + row_piece_offset<D>(row, c) + (e & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
             fence_proxy_async_smem();
             __syncwarp();
         }
@@ -591,32 +633,19 @@ __global__ void __launch_bounds__(NW * 32)
 // weights.  Loads of kReduceUnroll partitions are issued before any is used.
 // ---------------------------------------------------------------------------
 constexpr int kReduceThreads = 512;
-constexpr int kReduceUnroll = 4;
+constexpr int kReduceUnroll = 8;
 
-template <typename T, int D, bool COMPACT>
-__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
+// One (sequence, query head): the merged output of its n partitions.
+template <typename T, int D>
+__device__ __forceinline__ void reduce_one(const ReduceParams &r, int s, int h, size_t stat0,
+                                           size_t pstride, int n) {
     constexpr int NWR = kReduceThreads / 32;
     constexpr int VEC = D / 32;   // floats per lane: 2, 4 or 8
     __shared__ float s_m[NWR];
     __shared__ float s_l[NWR];
     __shared__ float s_acc[NWR][D];
-    const int h = blockIdx.x, s = blockIdx.y;
     const int Hq = r.num_q_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
-    size_t stat0, pstride;   // stats index of partition 0 and the stride between partitions
-    int n = (L + r.partition_size - 1) / r.partition_size;
-    if constexpr (COMPACT) {
-        if (L <= r.single_pass_max_len) return;   // written directly by the attention kernel
-        const int base = __ldg(r.part_base + s);
-        if (base < 0) return;
-        stat0 = static_cast<size_t>(base) * Hq + h;
-        pstride = Hq;
-    } else {
-        stat0 = (static_cast<size_t>(s) * Hq + h) * r.max_parts;
-        pstride = 1;
-    }
-    if (n > r.max_parts) n = r.max_parts;
     T *out = static_cast<T *>(r.out) + (static_cast<size_t>(s) * Hq + h) * D;
     if (n <= 0) {
         for (int i = threadIdx.x; i < D; i += kReduceThreads) out[i] = Mma<T>::cvt(0.f);
@@ -686,6 +715,34 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceP
 #pragma unroll
         for (int w = 0; w < NWR; ++w) a += ex2(s_m[w] - M) * s_acc[w][i];
         out[i] = Mma<T>::cvt(tot > 0.f ? a / tot : 0.f);
+    }
+    __syncthreads();   // the shared arrays are reused by the CTA's next item
+}
+
+// Dense layout: grid (Hq, S), one (sequence, head) per CTA.  Compact layout
+// (the mixed step): grid (Hq, G); CTA row y takes the partitioned sequences
+// y, y + G, ... of the planner's list, so no CTA is spent on sequences that
+// were finished in one pass.
+template <typename T, int D, bool COMPACT>
+__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
+    const int h = blockIdx.x;
+    const int Hq = r.num_q_heads;
+    if constexpr (COMPACT) {
+        const int count = *r.pseq_count;
+        for (int y = blockIdx.y; y < count; y += gridDim.y) {
+            const int s = __ldg(r.pseq_list + y);
+            const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
+            const int base = __ldg(r.part_base + s);
+            int n = (L + r.partition_size - 1) / r.partition_size;
+            if (n > r.max_parts) n = r.max_parts;
+            reduce_one<T, D>(r, s, h, static_cast<size_t>(base) * Hq + h, Hq, n);
+        }
+    } else {
+        const int s = blockIdx.y;
+        const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
+        int n = (L + r.partition_size - 1) / r.partition_size;
+        if (n > r.max_parts) n = r.max_parts;
+        reduce_one<T, D>(r, s, h, (static_cast<size_t>(s) * Hq + h) * r.max_parts, 1, n);
     }
 }
 

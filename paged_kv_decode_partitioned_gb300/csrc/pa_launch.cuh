@@ -126,9 +126,9 @@ cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid,
 #define PA_RED(DD)                                                                            \
     if (D == DD) {                                                                            \
         if (compact)                                                                          \
-            pa_reduce_kernel<T, DD, true><<<grid, kReduceThreads, 0, st>>>(r);                \
+            pa_reduce_kernel<T, DD, true><<<grid, kReduceThreads, 0, st>>>(r);       \
         else                                                                                  \
-            pa_reduce_kernel<T, DD, false><<<grid, kReduceThreads, 0, st>>>(r);               \
+            pa_reduce_kernel<T, DD, false><<<grid, kReduceThreads, 0, st>>>(r);      \
         return cudaGetLastError();                                                            \
     }
     PA_RED(64)

@@ -190,3 +190,19 @@ def test_too_few_partition_slots_raise_flag(pa):
     pa.decode_partitioned(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
                           dev.seq_lens, host.scale, P, NP)
     assert pa.device_status() & pa.DEV_TOO_MANY_PARTITIONS
+
+
+def test_single_pass_with_many_equal_length_classes(pa):
+    """Single-pass grid slots map to sequences longest first; ties (equal
+    lengths or length classes) must still cover every sequence exactly once."""
+    lengths = [100, 16, 100, 5000, 17, 100, 0, 5001, 16, 1, 4096, 4097, 100, 33, 5000, 2] * 3
+    w = custom_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                        dtype=torch.bfloat16)
+    host = make_case(w, lengths=lengths, seed=77)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    out = pa.decode(dev.query, dev.key_cache, dev.value_cache, dev.block_tables, dev.seq_lens,
+                    host.scale)
+    assert_out_close(out, ref, "pa_decode, tied lengths")
+    assert pa.device_status() == 0
