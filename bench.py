@@ -54,6 +54,10 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--partition-size", type=int, default=None,
                     help="override the workload's (first) partition size")
+    ap.add_argument("--mode", choices=["single", "partitioned", "auto"], default=None,
+                    help="override the workload's decode mode")
+    ap.add_argument("--single-pass-max-len", type=int, default=None,
+                    help="override the workload's single-pass limit (auto mode)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="reduced batch of the same workload rule (for profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -255,9 +259,40 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def make_inputs(wid, device, num_seqs=None):
+def rank_seed(wid: int, rank: int) -> int:
+    """Seed of a rank's batch: rank 0 uses the workload's own seed and every
+    other rank draws an independent batch of the same workload rule."""
+    from workloads import SEED_BASE
+    return SEED_BASE + wid + 1000 * rank
+
+
+def make_inputs(wid, device, num_seqs=None, rank=0):
     from workloads import WORKLOADS, make_case
-    return make_case(WORKLOADS[wid], device=device, num_seqs=num_seqs)
+    return make_case(WORKLOADS[wid], device=device, num_seqs=num_seqs, seed=rank_seed(wid, rank))
+
+
+def across_ranks(world: int, device, max_vals=(), sum_vals=()):
+    """Max over ranks of each value of max_vals and sum over ranks of each of
+    sum_vals (plain lists when world == 1).  Only timing and byte counts cross
+    ranks; the decode itself has no collective."""
+    max_vals, sum_vals = [float(v) for v in max_vals], [float(v) for v in sum_vals]
+    if world == 1:
+        return max_vals, sum_vals
+    import torch
+    import torch.distributed as dist
+    out = []
+    for vals, op in ((max_vals, dist.ReduceOp.MAX), (sum_vals, dist.ReduceOp.SUM)):
+        t = torch.tensor(vals + [0.0], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=op)
+        out.append(t.tolist()[:len(vals)])
+    return out[0], out[1]
+
+
+def whole_job(total_ms_max: float, steps: int, kv_bytes_sum: float, seqs_sum: float):
+    """(ms per step, KV-read GB/s, decode tokens/s) of the whole job: every
+    rank's bytes and sequences over the slowest rank's time (weak scaling)."""
+    ms = total_ms_max / steps
+    return ms, kv_bytes_sum / (ms * 1e-3) / 1e9, seqs_sum / (ms * 1e-3)
 
 
 def run_reference(args, rank, world):
@@ -327,12 +362,14 @@ def main():
     import paged_kv_decode_partitioned_gb300 as pa
     from paged_kv_decode_partitioned_gb300.step import DecodeStep
 
-    case = make_inputs(args.workload, "cuda", args.num_seqs)
+    case = make_inputs(args.workload, "cuda", args.num_seqs, rank)
     w = case.workload
     P = args.partition_size or w.partition_sizes[0]
-    step = DecodeStep(w.mode, case.query, case.key_cache, case.value_cache, case.block_tables,
+    mode = args.mode or w.mode
+    thr = w.single_pass_max_len if args.single_pass_max_len is None else args.single_pass_max_len
+    step = DecodeStep(mode, case.query, case.key_cache, case.value_cache, case.block_tables,
                       case.seq_lens, w.scale, max_seq_len=case.max_seq_len, partition_size=P,
-                      single_pass_max_len=w.single_pass_max_len)
+                      single_pass_max_len=thr)
     launches = step.launches()
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
@@ -402,15 +439,10 @@ def main():
     # mean event time of each launch of the step (includes the gap before it)
     launch_ms = {n: round(sum(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)) / K, 4)
                  for j, n in enumerate(names)}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / K
     kvb = kv_bytes(case)
-    value = world * kvb / (ms_per_step * 1e-3) / 1e9
-    tok_s = world * case.num_seqs / (ms_per_step * 1e-3)
+    (total_ms,), (kvb_all, seqs_all) = across_ranks(world, "cuda", [sum(step_ms)],
+                                                    [kvb, case.num_seqs])
+    ms_per_step, value, tok_s = whole_job(total_ms, K, kvb_all, seqs_all)
     peak, peak_src = measured_peaks()
     alg = kvb + qo_bytes(case)
     attn_mean_ms = sum(attn_ms) / K
@@ -446,12 +478,9 @@ def main():
             e2e_step()
             e1[k].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = sum(e0[k].elapsed_time(e1[k]) for k in range(K))
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(world * kvb / (e2e_ms / K * 1e-3) / 1e9, 3), "unit": "GB/s",
+        (e2e_ms,), _ = across_ranks(world, "cuda", [sum(e0[k].elapsed_time(e1[k])
+                                                      for k in range(K))])
+        e2e = {"value": round(whole_job(e2e_ms, K, kvb_all, seqs_all)[1], 3), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "kv_cache": "resident in HBM (decode state); per-step inputs copied"}
 
@@ -491,16 +520,16 @@ def main():
         if w.dtype.__repr__().endswith("bfloat16") else "f16", "data": "synthetic",
         "config": {"workload": w.name if args.num_seqs is None else
                    f"{w.name} (reduced to {case.num_seqs} sequences)",
-                   "global_batch": world * case.num_seqs,
+                   "global_batch": int(seqs_all),
                    "seq_len": case.max_seq_len, "total_tokens": case.total_tokens,
-                   "mode": w.mode, "partition_size": P,
-                   "single_pass_max_len": w.single_pass_max_len,
+                   "mode": mode, "partition_size": P,
+                   "single_pass_max_len": thr,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between steps (outside the events): {flush_w.numel() >> 20} "
                          f"MiB written, then {flush_r.numel() * 4 >> 20} MiB read; "
                          f"K/V inputs {kvb / 2**30:.2f} GiB > L2"},
         "decode_tokens_per_s": round(tok_s, 1),
-        "hbm_frac_kv": round(value / world / peak, 4),
+        "hbm_frac_kv": round(value / world / peak, 4),   # per GPU
         "hbm_frac_kvqo": round((alg / (ms_per_step * 1e-3) / 1e9) / peak, 4),
         "roofline": {"bound": "hbm", "kernel": step.attention_kernel,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
