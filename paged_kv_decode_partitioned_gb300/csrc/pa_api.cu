@@ -199,7 +199,7 @@ bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P,
     L->part_base = off;
     off = align256(off + static_cast<size_t>(S) * sizeof(int32_t));
     L->pseq_list = off;
-    off = align256(off + static_cast<size_t>(S) * sizeof(int32_t));
+    off = align256(off + static_cast<size_t>(S) * sizeof(int4));
     L->exp_sums = off;
     off = align256(off + static_cast<size_t>(slots) * Hq * sizeof(float));
     L->max_logits = off;
@@ -264,8 +264,8 @@ int pa_decode(void *out, const void *query, const void *key_cache, const void *v
     p.out = out;
     // Split each (sequence, KV head) over a cluster of CTAs when the batch has
     // too few units to keep every SM streaming (few or unequal sequences).
-    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim)
-                                        : attn_ctas_per_sm<__half>(head_dim);
+    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim, kModeSingle)
+                                        : attn_ctas_per_sm<__half>(head_dim, kModeSingle);
     p.cluster = single_pass_cluster(num_seqs * num_kv_heads, per_sm * di->num_sms);
     const dim3 grid(p.cluster, num_kv_heads, num_seqs);
     return attn(dtype, head_dim, kModeSingle, tk, tv, p, grid, static_cast<cudaStream_t>(stream)) ==
@@ -414,7 +414,7 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     int *counter = reinterpret_cast<int *>(ws + L.counter);
     int4 *units = reinterpret_cast<int4 *>(ws + L.units);
     int32_t *part_base = reinterpret_cast<int32_t *>(ws + L.part_base);
-    int32_t *pseq_list = reinterpret_cast<int32_t *>(ws + L.pseq_list);
+    int4 *pseq_list = reinterpret_cast<int4 *>(ws + L.pseq_list);
     float *es = reinterpret_cast<float *>(ws + L.exp_sums);
     float *ml = reinterpret_cast<float *>(ws + L.max_logits);
     float *tmp = reinterpret_cast<float *>(ws + L.tmp_out);
@@ -450,8 +450,8 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     p.partition_size = partition_size;
     p.max_parts = L.max_parts;
     p.single_pass_max_len = thr;
-    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim)
-                                        : attn_ctas_per_sm<__half>(head_dim);
+    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim, kModeWorklist)
+                                        : attn_ctas_per_sm<__half>(head_dim, kModeWorklist);
     if (per_sm <= 0) return PA_ERR_CUDA;
     int64_t ctas = static_cast<int64_t>(per_sm) * di->num_sms;
     if (ctas > L.max_units) ctas = L.max_units;
@@ -477,10 +477,9 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
         r.max_parts = L.max_parts;
         r.single_pass_max_len = thr;
         r.len_cap = len_cap;
-        // about 4 CTAs per SM, each looping over partitioned sequences
-        int rows = (4 * di->num_sms + num_q_heads - 1) / num_q_heads;
-        if (rows > num_seqs) rows = num_seqs;
-        if (rows < 1) rows = 1;
+        // one CTA per (partitioned sequence, head): rows past the planner's
+        // count exit at once
+        const int rows = num_seqs;
         if (reduce(dtype, head_dim, true, r, dim3(num_q_heads, rows), st) != cudaSuccess)
             return PA_ERR_CUDA;
     }

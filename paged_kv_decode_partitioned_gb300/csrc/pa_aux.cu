@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
             pp.units[base_unit + k] = make_int4(s, k % Hkv, k / Hkv, kOutPartialCompact);
         if (threadIdx.x == 0) {
             pp.part_base[s] = slots_before;
-            pp.pseq_list[s - singles_before] = s;   // rank among the partitioned sequences
+            // entry at the sequence's rank among the partitioned sequences
+            pp.pseq_list[s - singles_before] = make_int4(s, slots_before, np, 0);
         }
     }
     if (s == 0 && threadIdx.x == 0) {

@@ -632,38 +632,58 @@ __global__ void __launch_bounds__(NW * 32)
 // value up to rounding), then the warps' states are merged with the same
 // weights.  Loads of kReduceUnroll partitions are issued before any is used.
 // ---------------------------------------------------------------------------
-constexpr int kReduceThreads = 512;
-constexpr int kReduceUnroll = 8;
+// Threads per (sequence, head): the dense reduce (few sequences with many
+// partitions) uses 512; the compact one (many sequences with fewer
+// partitions) uses 128 so that more sequences are in flight at once.
+template <bool COMPACT> struct ReduceThreads { static constexpr int value = COMPACT ? 128 : 512; };
+// Partitions each warp loads before accumulating (head_dim 256 keeps fewer
+// so that two CTAs fit per SM).
+template <int D> struct ReduceUnroll { static constexpr int value = D <= 128 ? 8 : 4; };
 
-// One (sequence, query head): the merged output of its n partitions.
-template <typename T, int D>
+// One (sequence, query head): the merged output of its n partitions.  The
+// first round of loads is issued for the first nb (an upper bound on n
+// known without reading seq_lens) partitions before n is needed, so the
+// length read and the partial reads overlap; slots at or past n are dropped
+// by selection (never by multiplying, so unwritten slots cannot leak in).
+template <typename T, int D, int kReduceThreads>
 __device__ __forceinline__ void reduce_one(const ReduceParams &r, int s, int h, size_t stat0,
-                                           size_t pstride, int n) {
+                                           size_t pstride, int nb, int n_known) {
     constexpr int NWR = kReduceThreads / 32;
     constexpr int VEC = D / 32;   // floats per lane: 2, 4 or 8
+    constexpr int U = ReduceUnroll<D>::value;
     __shared__ float s_m[NWR];
     __shared__ float s_l[NWR];
     __shared__ float s_acc[NWR][D];
     const int Hq = r.num_q_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     T *out = static_cast<T *>(r.out) + (static_cast<size_t>(s) * Hq + h) * D;
-    if (n <= 0) {
-        for (int i = threadIdx.x; i < D; i += kReduceThreads) out[i] = Mma<T>::cvt(0.f);
-        return;
-    }
 
     float m_run = -INFINITY, l_run = 0.f;   // log2-domain running max, weight sum
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    for (int q0 = warp; q0 < n; q0 += NWR * kReduceUnroll) {
-        float mq[kReduceUnroll], lq[kReduceUnroll], x[kReduceUnroll][VEC];
+    // n_known < 0: n comes from seq_lens[s], read after the first round's
+    // loads are issued
+    int n = -1;
+    const int len_raw = n_known < 0 ? __ldg(r.seq_lens + s) : 0;
+    auto resolve_n = [&]() {
+        if (n_known >= 0) return n_known;
+        int L = len_raw;
+        if (L < 0 || L > r.len_cap) {
+            if (threadIdx.x == 0) atomicOr(r.status, kLenClamped);
+            L = L < 0 ? 0 : r.len_cap;
+        }
+        const int np = (L + r.partition_size - 1) / r.partition_size;
+        return np < r.max_parts ? np : r.max_parts;
+    };
+    for (int q0 = warp; q0 < (n < 0 ? nb : n); q0 += NWR * U) {
+        float mq[U], lq[U], x[U][VEC];
 #pragma unroll
-        for (int u = 0; u < kReduceUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int q = q0 + u * NWR;
-            const int qc = q < n ? q : n - 1;   // in range; its weight is dropped below
+            const int qc = q < nb ? q : nb - 1;   // always a slot of the buffer
             const size_t si = stat0 + qc * pstride;
-            mq[u] = q < n ? __ldg(r.max_logits + si) * kLog2e : -INFINITY;
+            mq[u] = __ldg(r.max_logits + si);
             lq[u] = __ldg(r.exp_sums + si);
             const float *src = r.tmp_out + si * D + lane * VEC;
 #pragma unroll
@@ -681,22 +701,32 @@ __device__ __forceinline__ void reduce_one(const ReduceParams &r, int s, int h, 
                 }
             }
         }
+        if (n < 0) n = resolve_n();
+        bool live[U];
         float mb = m_run;
 #pragma unroll
-        for (int u = 0; u < kReduceUnroll; ++u) mb = fmaxf(mb, mq[u]);
+        for (int u = 0; u < U; ++u) {
+            live[u] = q0 + u * NWR < n;
+            mq[u] = live[u] ? mq[u] * kLog2e : -INFINITY;
+            mb = fmaxf(mb, mq[u]);
+        }
+        if (mb == -INFINITY) continue;   // no live partition in this round (past n)
         const float sc = ex2(m_run - mb);   // 0 while nothing is accumulated yet
         l_run *= sc;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) acc[v] *= sc;
 #pragma unroll
-        for (int u = 0; u < kReduceUnroll; ++u) {
-            const float w = ex2(mq[u] - mb) * lq[u];   // 0 for dropped slots
-            l_run += w;
+        for (int u = 0; u < U; ++u) {
+            if (live[u]) {
+                const float w = ex2(mq[u] - mb) * lq[u];
+                l_run += w;
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[v] += w * x[u][v];
+                for (int v = 0; v < VEC; ++v) acc[v] += w * x[u][v];
+            }
         }
         m_run = mb;
     }
+    if (n < 0) n = resolve_n();   // this warp had no first-round partition
     if (lane == 0) {
         s_m[warp] = m_run;
         s_l[warp] = l_run;
@@ -708,41 +738,42 @@ __device__ __forceinline__ void reduce_one(const ReduceParams &r, int s, int h, 
 #pragma unroll
     for (int w = 0; w < NWR; ++w) M = fmaxf(M, s_m[w]);
     float tot = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < NWR; ++w) tot += ex2(s_m[w] - M) * s_l[w];
+        for (int w = 0; w < NWR; ++w) tot += ex2(s_m[w] - M) * s_l[w];
+    }
     for (int i = threadIdx.x; i < D; i += kReduceThreads) {
         float a = 0.f;
+        if (tot > 0.f) {
 #pragma unroll
-        for (int w = 0; w < NWR; ++w) a += ex2(s_m[w] - M) * s_acc[w][i];
-        out[i] = Mma<T>::cvt(tot > 0.f ? a / tot : 0.f);
+            for (int w = 0; w < NWR; ++w) a += ex2(s_m[w] - M) * s_acc[w][i];
+        }
+        out[i] = Mma<T>::cvt(tot > 0.f ? a / tot : 0.f);   // n == 0 gives zeros
     }
     __syncthreads();   // the shared arrays are reused by the CTA's next item
 }
 
 // Dense layout: grid (Hq, S), one (sequence, head) per CTA.  Compact layout
-// (the mixed step): grid (Hq, G); CTA row y takes the partitioned sequences
-// y, y + G, ... of the planner's list, so no CTA is spent on sequences that
-// were finished in one pass.
+// (the mixed step): grid (Hq, G); CTA row y takes the entries y, y + G, ... of
+// the planner's list of partitioned sequences (sequence, first slot, count),
+// so no CTA is spent on sequences that were finished in one pass.
 template <typename T, int D, bool COMPACT>
-__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const ReduceParams r) {
+__global__ void __launch_bounds__(ReduceThreads<COMPACT>::value, 2)
+    pa_reduce_kernel(const ReduceParams r) {
+    constexpr int NT = ReduceThreads<COMPACT>::value;
     const int h = blockIdx.x;
     const int Hq = r.num_q_heads;
     if constexpr (COMPACT) {
         const int count = *r.pseq_count;
         for (int y = blockIdx.y; y < count; y += gridDim.y) {
-            const int s = __ldg(r.pseq_list + y);
-            const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
-            const int base = __ldg(r.part_base + s);
-            int n = (L + r.partition_size - 1) / r.partition_size;
-            if (n > r.max_parts) n = r.max_parts;
-            reduce_one<T, D>(r, s, h, static_cast<size_t>(base) * Hq + h, Hq, n);
+            const int4 e = r.pseq_list[y];   // (sequence, first slot, partitions, -)
+            reduce_one<T, D, NT>(r, e.x, h, static_cast<size_t>(e.y) * Hq + h, Hq, max(e.z, 1),
+                                 e.z);
         }
     } else {
         const int s = blockIdx.y;
-        const int L = clamp_len(r.seq_lens, s, r.len_cap, r.status);
-        int n = (L + r.partition_size - 1) / r.partition_size;
-        if (n > r.max_parts) n = r.max_parts;
-        reduce_one<T, D>(r, s, h, (static_cast<size_t>(s) * Hq + h) * r.max_parts, 1, n);
+        reduce_one<T, D, NT>(r, s, h, (static_cast<size_t>(s) * Hq + h) * r.max_parts, 1,
+                             r.max_parts, -1);
     }
 }
 

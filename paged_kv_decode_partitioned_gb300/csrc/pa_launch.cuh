@@ -30,10 +30,26 @@ namespace pa {
 #ifndef PA_NS_D256
 #define PA_NS_D256 1   // 64 KB of stages: 3 CTAs (12 warps) per SM beat 1 CTA with 2 stages
 #endif
-template <int D> struct AttnCfg;
-template <> struct AttnCfg<64> { static constexpr int NW = PA_NW_D64, NS = PA_NS_D64; };
-template <> struct AttnCfg<128> { static constexpr int NW = PA_NW_D128, NS = PA_NS_D128; };
-template <> struct AttnCfg<256> { static constexpr int NW = PA_NW_D256, NS = PA_NS_D256; };
+// The single-pass grid may use a deeper ring (-DPA_NS_SINGLE_D<D>=...).
+#ifndef PA_NS_SINGLE_D64
+#define PA_NS_SINGLE_D64 PA_NS_D64
+#endif
+#ifndef PA_NS_SINGLE_D128
+#define PA_NS_SINGLE_D128 PA_NS_D128
+#endif
+#ifndef PA_NS_SINGLE_D256
+#define PA_NS_SINGLE_D256 PA_NS_D256
+#endif
+template <int D, int MODE> struct AttnCfg;
+#define PA_CFG(DD)                                                                       \
+    template <int MODE> struct AttnCfg<DD, MODE> {                                       \
+        static constexpr int NW = PA_NW_D##DD;                                           \
+        static constexpr int NS = MODE == kModeSingle ? PA_NS_SINGLE_D##DD : PA_NS_D##DD; \
+    };
+PA_CFG(64)
+PA_CFG(128)
+PA_CFG(256)
+#undef PA_CFG
 
 constexpr int kMaxDevices = 64;
 
@@ -53,7 +69,7 @@ inline cudaError_t ensure_smem(K kernel, int bytes, std::atomic<int> *done) {
 template <typename T, int D, int MODE>
 inline cudaError_t launch_attn_d(const CUtensorMap &tmK, const CUtensorMap &tmV, const Params &p,
                                  dim3 grid, cudaStream_t st) {
-    using C = AttnCfg<D>;
+    using C = AttnCfg<D, MODE>;
     using SM = Smem<D, C::NW, C::NS>;
     static std::atomic<int> done[kMaxDevices];
     auto k = pa_attn_kernel<T, D, C::NW, C::NS, MODE>;
@@ -81,12 +97,12 @@ inline cudaError_t launch_attn_d(const CUtensorMap &tmK, const CUtensorMap &tmV,
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, int MODE>
 inline int attn_ctas_per_sm_d() {
-    using C = AttnCfg<D>;
+    using C = AttnCfg<D, MODE>;
     using SM = Smem<D, C::NW, C::NS>;
     static std::atomic<int> done[kMaxDevices];
-    auto k = pa_attn_kernel<T, D, C::NW, C::NS, kModeWorklist>;
+    auto k = pa_attn_kernel<T, D, C::NW, C::NS, MODE>;
     if (ensure_smem(k, SM::kLaunchBytes, done) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, C::NW * 32, SM::kLaunchBytes) !=
@@ -114,10 +130,17 @@ cudaError_t launch_attn(int D, int mode, const CUtensorMap &tmK, const CUtensorM
 }
 
 template <typename T>
-int attn_ctas_per_sm(int D) {
-    if (D == 64) return attn_ctas_per_sm_d<T, 64>();
-    if (D == 128) return attn_ctas_per_sm_d<T, 128>();
-    if (D == 256) return attn_ctas_per_sm_d<T, 256>();
+int attn_ctas_per_sm(int D, int mode) {
+#define PA_OCC(DD)                                                                        \
+    if (D == DD) {                                                                        \
+        if (mode == kModeSingle) return attn_ctas_per_sm_d<T, DD, kModeSingle>();         \
+        if (mode == kModePartitioned) return attn_ctas_per_sm_d<T, DD, kModePartitioned>(); \
+        return attn_ctas_per_sm_d<T, DD, kModeWorklist>();                                \
+    }
+    PA_OCC(64)
+    PA_OCC(128)
+    PA_OCC(256)
+#undef PA_OCC
     return 0;
 }
 
@@ -126,9 +149,9 @@ cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid,
 #define PA_RED(DD)                                                                            \
     if (D == DD) {                                                                            \
         if (compact)                                                                          \
-            pa_reduce_kernel<T, DD, true><<<grid, kReduceThreads, 0, st>>>(r);       \
+            pa_reduce_kernel<T, DD, true><<<grid, ReduceThreads<true>::value, 0, st>>>(r);    \
         else                                                                                  \
-            pa_reduce_kernel<T, DD, false><<<grid, kReduceThreads, 0, st>>>(r);      \
+            pa_reduce_kernel<T, DD, false><<<grid, ReduceThreads<false>::value, 0, st>>>(r);  \
         return cudaGetLastError();                                                            \
     }
     PA_RED(64)
@@ -141,7 +164,7 @@ cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid,
 #define PA_INSTANTIATE_LAUNCHERS(T)                                                             \
     template cudaError_t launch_attn<T>(int, int, const CUtensorMap &, const CUtensorMap &,     \
                                         const Params &, dim3, cudaStream_t);                    \
-    template int attn_ctas_per_sm<T>(int);                                                      \
+    template int attn_ctas_per_sm<T>(int, int);                                                 \
     template cudaError_t launch_reduce<T>(int, bool, const ReduceParams &, dim3, cudaStream_t);
 
 }  // namespace pa

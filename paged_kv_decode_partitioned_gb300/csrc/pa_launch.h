@@ -15,7 +15,7 @@ template <typename T>
 cudaError_t launch_attn(int D, int mode, const CUtensorMap &tmK, const CUtensorMap &tmV,
                         const Params &p, dim3 grid, cudaStream_t st);
 template <typename T>
-int attn_ctas_per_sm(int D);
+int attn_ctas_per_sm(int D, int mode);
 template <typename T>
 cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st);
 

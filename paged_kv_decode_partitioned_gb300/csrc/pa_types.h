@@ -48,8 +48,8 @@ struct ReduceParams {
     const float *max_logits;
     const int32_t *seq_lens;
     const int32_t *part_base;   // compact layout only
-    const int32_t *pseq_list;   // compact layout: the partitioned sequences
-    const int *pseq_count;      // compact layout: their number
+    const int4 *pseq_list;      // compact layout: (sequence, first slot, partitions, -)
+    const int *pseq_count;      // compact layout: number of entries
     int *status;
     int num_q_heads, partition_size, max_parts, single_pass_max_len, len_cap;
 };
@@ -60,7 +60,7 @@ struct PlanParams {
     int *unit_counter;
     int *unit_count;
     int32_t *part_base;
-    int32_t *pseq_list;
+    int4 *pseq_list;            // (sequence, first slot, partitions, 0) per partitioned sequence
     int *pseq_count;
     int *status;
     int num_seqs, num_kv_heads, partition_size, single_pass_max_len, len_cap, max_parts;
