@@ -251,6 +251,15 @@ PA_API int pa_gather_kv(void *k_dense, void *v_dense, const void *key_cache,
                  int max_len, pa_dtype_t dtype, void *stream);
 
 /*
+ * pa_selftest_wait_timeout -- test entry for the failure path: launches one
+ * warp that waits on a pipeline barrier which nothing completes (no copy is
+ * issued), gives up after limit_us microseconds (1 .. 1,000,000) and raises
+ * PA_DEV_WAIT_TIMEOUT, as the attention kernels do when a copy does not land.
+ * The device stays usable; read the flag with pa_device_status().
+ */
+PA_API int pa_selftest_wait_timeout(void *stream, int limit_us);
+
+/*
  * pa_device_status -- synchronises `stream`, returns in *flags the PA_DEV_*
  * flags raised by kernels on the current device since the last call, and
  * clears them.  Returns PA_OK, or PA_ERR_CUDA if synchronisation failed.

@@ -54,6 +54,7 @@ SIGNATURES = [
                                                            _i, _vp, _i]),
     ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _i, _vp]),
     ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
+    ("pa_selftest_wait_timeout", _i, [_vp, _i]),
     ("pa_device_status", _i, [_vp, ctypes.POINTER(_i)]),
     ("pa_status_string", ctypes.c_char_p, [_i]),
     ("pa_version", _i, []),
@@ -290,6 +291,16 @@ def gather_kv(key_cache, value_cache, block_tables, seq_lens, max_len: int):
             _dtype_code(key_cache), _stream(key_cache))
     _check(st, "pa_gather_kv")
     return kd, vd
+
+
+def selftest_wait_timeout(limit_us: int = 20000, device=None) -> None:
+    """Launch the failure-path test kernel (``pa_selftest_wait_timeout``)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    with torch.cuda.device(dev):
+        st = _load().pa_selftest_wait_timeout(torch.cuda.current_stream(dev).cuda_stream,
+                                              int(limit_us))
+    _check(st, "pa_selftest_wait_timeout")
 
 
 def device_status(device=None) -> int:

@@ -539,6 +539,17 @@ int pa_gather_kv(void *k_dense, void *v_dense, const void *key_cache, const void
                : PA_ERR_CUDA;
 }
 
+int pa_selftest_wait_timeout(void *stream, int limit_us) {
+    if (limit_us <= 0 || limit_us > 1000000) return PA_ERR_INVALID_ARGUMENT;
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    return launch_wait_timeout_test(di->status, 1000ull * static_cast<unsigned>(limit_us),
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 int pa_device_status(void *stream, int *flags) {
     if (!flags) return PA_ERR_INVALID_ARGUMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

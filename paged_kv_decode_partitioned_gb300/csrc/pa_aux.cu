@@ -138,6 +138,26 @@ __global__ void __launch_bounds__(32)
 }
 
 
+// Test kernel of the failure path: waits on an mbarrier that nothing will
+// complete (no copy is issued), gives up after limit_ns and raises the
+// time-out flag exactly as the attention kernel does.
+__global__ void __launch_bounds__(32) pa_wait_timeout_kernel(int *status,
+                                                             unsigned long long limit_ns) {
+    __shared__ alignas(8) uint64_t bar_storage;
+    const uint32_t bar = smem_u32(&bar_storage);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(bar, 0, limit_ns) && threadIdx.x == 0) atomicOr(status, kWaitTimeout);
+}
+
+cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, cudaStream_t st) {
+    pa_wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st) {
     if (pp.num_seqs <= 0) return cudaSuccess;
     pa_plan_kernel<<<pp.num_seqs, kPlanThreads, 0, st>>>(pp);

@@ -86,13 +86,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of an mbarrier; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 255u) == 0u && global_ns() - t0 > limit_ns) return false;
     }
 }
 

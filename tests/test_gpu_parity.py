@@ -206,3 +206,76 @@ def test_single_pass_with_many_equal_length_classes(pa):
                     host.scale)
     assert_out_close(out, ref, "pa_decode, tied lengths")
     assert pa.device_status() == 0
+
+
+def test_wait_timeout_raises_flag_and_device_stays_usable(pa):
+    """The bounded-wait failure path: a barrier nothing completes times out,
+    raises PA_DEV_WAIT_TIMEOUT, and later launches still compute correctly."""
+    assert pa.device_status() == 0
+    pa.selftest_wait_timeout(20000)
+    assert pa.device_status() & pa.DEV_WAIT_TIMEOUT
+    assert pa.device_status() == 0
+    host = _case(1)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    out = pa.decode(dev.query, dev.key_cache, dev.value_cache, dev.block_tables, dev.seq_lens,
+                    host.scale)
+    assert_out_close(out, ref, "decode after a time-out")
+
+
+def test_long_sequence_single_pass_cluster_split(pa):
+    """One 100K-token sequence in one pass: the cluster splits it 8 ways."""
+    w = custom_workload(num_q_heads=24, num_kv_heads=4, head_dim=128, block_size=16,
+                        dtype=torch.bfloat16, k_scale=3.0)
+    host = make_case(w, lengths=[100000, 3], seed=91)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    out = pa.decode(dev.query, dev.key_cache, dev.value_cache, dev.block_tables, dev.seq_lens,
+                    host.scale)
+    assert_out_close(out, ref, "single pass, 100K tokens")
+    assert pa.device_status() == 0
+
+
+@pytest.mark.parametrize("bs", [64, 256])
+def test_large_block_sizes(pa, bs):
+    w = custom_workload(num_q_heads=16, num_kv_heads=2, head_dim=128, block_size=bs,
+                        dtype=torch.float16)
+    host = make_case(w, lengths=[1, bs - 1, bs, bs + 1, 3 * bs + 17], seed=92 + bs)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    out = pa.decode(dev.query, dev.key_cache, dev.value_cache, dev.block_tables, dev.seq_lens,
+                    host.scale)
+    assert_out_close(out, ref, f"single pass, bs={bs}")
+    P = bs
+    NP = oracle.num_partitions(host.max_seq_len, P)
+    tmp, es, ml = pa.decode_partitioned(dev.query, dev.key_cache, dev.value_cache,
+                                        dev.block_tables, dev.seq_lens, host.scale, P, NP)
+    assert_out_close(pa.partition_reduce(tmp, es, ml, dev.seq_lens, P, dtype=torch.float16),
+                     ref, f"partitioned, bs={bs}")
+    out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
+                         dev.seq_lens, host.scale, host.max_seq_len, bs, 2 * bs)
+    assert_out_close(out, ref, f"auto, bs={bs}")
+    assert pa.device_status() == 0
+
+
+def test_many_short_sequences(pa):
+    """1000 sequences: the planner's per-sequence loops and the compact list."""
+    g = torch.Generator().manual_seed(93)
+    lengths = [int(x) for x in torch.randint(0, 300, (1000,), generator=g)]
+    w = custom_workload(num_q_heads=8, num_kv_heads=1, head_dim=64, block_size=16,
+                        dtype=torch.bfloat16)
+    host = make_case(w, lengths=lengths, seed=94)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    for thr in (0, 100, 10000):
+        out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
+                             dev.seq_lens, host.scale, host.max_seq_len, thr, 32)
+        assert_out_close(out, ref, f"auto, 1000 sequences, thr={thr}")
+    out = pa.decode(dev.query, dev.key_cache, dev.value_cache, dev.block_tables, dev.seq_lens,
+                    host.scale)
+    assert_out_close(out, ref, "single pass, 1000 sequences")
+    assert pa.device_status() == 0
