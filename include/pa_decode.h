@@ -136,10 +136,12 @@ PA_API int pa_partition_reduce(void *out, const float *tmp_out, const float *exp
  * pa_default_single_pass_max_len -- the launch heuristic's threshold.
  * Sequences longer than the returned length are partitioned by
  * pa_decode_auto.  It is 8192, the forward_decode heuristic's boundary
- * between V1 and V2, when num_seqs * num_kv_heads single-pass units fill
- * every SM of the device at least twice, and partition_size otherwise (too
- * few units: split everything longer than one partition so that the SMs have
- * work).  num_sms <= 0 queries the current device.
+ * between V1 and V2, when there are at least as many num_seqs * num_kv_heads
+ * single-pass units as SMs (the single-pass grid then splits each unit over a
+ * cluster to fill the device), and partition_size otherwise (too few units:
+ * split everything longer than one partition).  The crossover was measured
+ * on GB300 over 1..256 sequences of 1K..64K tokens.  num_sms <= 0 queries
+ * the current device.
  */
 PA_API int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int partition_size,
                                    int num_sms);
@@ -165,7 +167,9 @@ PA_API size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_
  * pa_default_single_pass_max_len.  workspace: device memory of at least
  * pa_auto_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller;
  * its contents need no initialisation and are scratch after the call.
- * Launches three kernels (plan, attention, reduce) on `stream`.
+ * Launches three kernels (plan, attention, reduce) on `stream`; when
+ * max_seq_len <= the single-pass limit it launches the single-pass grid of
+ * pa_decode alone.
  */
 PA_API int pa_decode_auto(void *out, const void *query, const void *key_cache,
                    const void *value_cache, const int32_t *block_tables,
@@ -184,7 +188,9 @@ enum { PA_PHASE_PLAN = 1, PA_PHASE_ATTEND = 2, PA_PHASE_REDUCE = 4 };
  * PA_PHASE_PLAN builds the work list in `workspace` from seq_lens;
  * PA_PHASE_ATTEND runs the attention kernel over it (single-pass sequences
  * write `out`, partitioned ones write their partials to `workspace`);
- * PA_PHASE_REDUCE merges the partials into `out`.  All arguments must be the
+ * PA_PHASE_REDUCE merges the partials into `out`.  When max_seq_len is at
+ * most the single-pass limit, PA_PHASE_ATTEND runs the single-pass grid and
+ * the other two phases do nothing.  All arguments must be the
  * same for the phases of one step and the phases must run in this order on
  * one stream.  phases = PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE is
  * exactly pa_decode_auto.  Other masks return PA_ERR_INVALID_ARGUMENT.

@@ -212,13 +212,31 @@ bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P,
 
 int default_thr(int S, int Hkv, int P, int num_sms) {
     const int64_t units = static_cast<int64_t>(S) * Hkv;
-    return units >= 2 * static_cast<int64_t>(num_sms) ? 8192 : P;
+    return units >= static_cast<int64_t>(num_sms) ? 8192 : P;
 }
 
 int num_sms_now() {
     DevInfo *d = nullptr;
     if (device_info(&d) != PA_OK) return 0;
     return d->num_sms;
+}
+
+
+// The single-pass grid: each (sequence, KV head) split over a cluster of CTAs
+// when the batch has too few units to keep every SM streaming (few or
+// unequal sequences).
+int launch_single_pass(const Shape &s, void *out, const void *query, const int32_t *bt,
+                       const int32_t *sl, float scale, pa_dtype_t dtype, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const DevInfo *di, cudaStream_t st) {
+    Params p = base_params(s, query, bt, sl, scale, di->status);
+    p.out = out;
+    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(s.D, kModeSingle)
+                                        : attn_ctas_per_sm<__half>(s.D, kModeSingle);
+    if (per_sm <= 0) return PA_ERR_CUDA;
+    p.cluster = single_pass_cluster(s.S * s.Hkv, per_sm * di->num_sms);
+    const dim3 grid(p.cluster, s.Hkv, s.S);
+    return attn(dtype, s.D, kModeSingle, tk, tv, p, grid, st) == cudaSuccess ? PA_OK
+                                                                             : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -260,18 +278,8 @@ int pa_decode(void *out, const void *query, const void *key_cache, const void *v
     if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
                              num_blocks)) != PA_OK)
         return rc;
-    Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
-    p.out = out;
-    // Split each (sequence, KV head) over a cluster of CTAs when the batch has
-    // too few units to keep every SM streaming (few or unequal sequences).
-    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim, kModeSingle)
-                                        : attn_ctas_per_sm<__half>(head_dim, kModeSingle);
-    p.cluster = single_pass_cluster(num_seqs * num_kv_heads, per_sm * di->num_sms);
-    const dim3 grid(p.cluster, num_kv_heads, num_seqs);
-    return attn(dtype, head_dim, kModeSingle, tk, tv, p, grid, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? PA_OK
-               : PA_ERR_CUDA;
+    return launch_single_pass(s, out, query, block_tables, seq_lens, scale, dtype, tk, tv, di,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int pa_decode_partitioned(float *tmp_out, float *exp_sums, float *max_logits, const void *query,
@@ -410,6 +418,14 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
                              num_blocks)) != PA_OK)
         return rc;
+    if (L.max_parts == 0) {
+        // Every sequence fits the single-pass limit: no work list and no
+        // partials, just the single-pass grid (the plan and reduce phases have
+        // nothing to do).
+        if (!(phases & PA_PHASE_ATTEND)) return PA_OK;
+        return launch_single_pass(s, out, query, block_tables, seq_lens, scale, dtype, tk, tv,
+                                  di, static_cast<cudaStream_t>(stream));
+    }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int *counter = reinterpret_cast<int *>(ws + L.counter);
     int4 *units = reinterpret_cast<int4 *>(ws + L.units);

@@ -57,12 +57,13 @@ class DecodeStep:
 
     @property
     def kernels_per_call(self) -> int:
-        """Kernel launches one call makes (single: 1; partitioned: 2; auto: 3 or 2)."""
+        """Kernel launches one call makes (single: 1; partitioned: 2; auto: 3, or 1 when
+        every sequence fits the single-pass limit)."""
         if self.mode == "single":
             return 1
         if self.mode == "partitioned":
             return 2
-        return 3 if self.max_seq_len > self.single_pass_max_len else 2
+        return 3 if self.max_seq_len > self.single_pass_max_len else 1
 
     @property
     def attention_kernel(self) -> str:
@@ -97,10 +98,10 @@ class DecodeStep:
                                        self.max_seq_len, self.single_pass_max_len,
                                        self.partition_size, workspace=self.workspace,
                                        out=self.out, phases=mask)
-        steps = [("plan", phase(PHASE_PLAN)), ("attention", phase(PHASE_ATTEND))]
-        if self.max_seq_len > self.single_pass_max_len:
-            steps.append(("reduce", phase(PHASE_REDUCE)))
-        return steps
+        if self.max_seq_len <= self.single_pass_max_len:   # one single-pass launch
+            return [("attention", phase(PHASE_PLAN | PHASE_ATTEND | PHASE_REDUCE))]
+        return [("plan", phase(PHASE_PLAN)), ("attention", phase(PHASE_ATTEND)),
+                ("reduce", phase(PHASE_REDUCE))]
 
     def __call__(self) -> torch.Tensor:
         if self.mode == "single":

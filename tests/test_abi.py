@@ -119,10 +119,11 @@ def test_auto_workspace_size_formula(lib):
 
 
 def test_default_threshold_uses_sm_count(lib):
-    # 64 seqs x 4 KV heads = 256 units: enough for 2 x 100 SMs, not for 2 x 152
-    assert lib.pa_default_single_pass_max_len(64, 4, 512, 100) == 8192
-    assert lib.pa_default_single_pass_max_len(64, 4, 512, 152) == 512
-    assert lib.pa_default_single_pass_max_len(256, 4, 512, 152) == 8192
+    # 64 seqs x 4 KV heads = 256 units: at least one per SM on 152 SMs, not on 300
+    assert lib.pa_default_single_pass_max_len(64, 4, 512, 152) == 8192
+    assert lib.pa_default_single_pass_max_len(64, 4, 512, 300) == 512
+    assert lib.pa_default_single_pass_max_len(16, 4, 512, 152) == 512
+    assert lib.pa_default_single_pass_max_len(256, 4, 256, 152) == 8192
 
 
 def test_product_path_has_no_oracle_or_cpu_fallback():
