@@ -72,6 +72,9 @@ def _load():
                 [_int] * 3
             lib.oracle_lse_merge.restype = _int
             lib.oracle_lse_merge.argtypes = [_dp, _dp, _dp, _dp, _i32p] + [_int] * 5
+            lib.oracle_prefill.restype = _int
+            lib.oracle_prefill.argtypes = [_dp, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p] + \
+                [_int] * 7 + [ctypes.c_float, _int]
             lib.oracle_gather.restype = _int
             lib.oracle_gather.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, _i32p] + \
                 [_int] * 7
@@ -213,6 +216,26 @@ def lse_merge(tmp_out, exp_sums, max_logits, seq_lens, partition_size) -> np.nda
         _ptr(ml, ctypes.c_double), _ptr(sl, ctypes.c_int32), S, Hq, d,
         int(partition_size), NP)
     _check(rc, "lse_merge")
+    return out
+
+
+def prefill(query, key_cache, value_cache, block_tables, seq_lens, q_start, scale,
+            dtype=None) -> np.ndarray:
+    """Prefix prefill output [q_start[-1], Hq, d] in fp64 (see ``oracle_prefill``)."""
+    code = _dtype_code(query, dtype)
+    q, k, v = _bits(query), _bits(key_cache), _bits(value_cache)
+    bt, sl, qs = _i32(block_tables), _i32(seq_lens), _i32(q_start)
+    R, Hq, d = q.shape
+    num_blocks, bs, Hkv, d2 = k.shape
+    S, mb = bt.shape
+    if d2 != d or qs.shape != (S + 1,) or qs[-1] != R:
+        raise ValueError("prefill shapes disagree")
+    out = np.empty((R, Hq, d), dtype=np.float64)
+    rc = _load().oracle_prefill(
+        _ptr(out, ctypes.c_double), _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+        _ptr(v, ctypes.c_uint16), _ptr(bt, ctypes.c_int32), _ptr(sl, ctypes.c_int32),
+        _ptr(qs, ctypes.c_int32), S, Hq, Hkv, d, bs, num_blocks, mb, ctypes.c_float(scale), code)
+    _check(rc, "prefill")
     return out
 
 

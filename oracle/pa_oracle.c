@@ -18,6 +18,9 @@
  *              partition) computes its scaled logits, their softmax and the
  *              weighted V sum, and keeps three partial results: the partial
  *              output, the exp-sum and the maximum logit.
+ *   [prefill]  the prefix-prefill rewrite: a chunk of new tokens attends to
+ *              the whole cached context of its sequence (gathered once) and,
+ *              causally, to the chunk itself.
  *   [phase 2]  the V2 description, phase 2: the maximum over partitions is
  *              taken, each partition is weighted by exp(its max - that
  *              maximum) times its exp-sum, and the output is the weighted
@@ -116,15 +119,14 @@ static int check_dims(int S, int Hq, int Hkv, int d, int bs, int num_blocks,
     return ORACLE_OK;
 }
 
-/* x[t - t0] = scale * sum_i q[s][h][i] * k_t[i] for t in [t0, t1), and the
- * query row widened once into qd[d]. */
-static int scaled_logits(double *x, double *qd, const uint16_t *q, const uint16_t *kc,
-                         const int32_t *bt, int s, int h, int kvh, int t0, int t1,
-                         int Hq, int Hkv, int d, int bs, int num_blocks, int max_blocks,
-                         double scale, int dtype)
+/* x[t - t0] = scale * sum_i qrow[i] * k_t[i] for t in [t0, t1) of sequence s,
+ * and the query row widened once into qd[d]. */
+static int scaled_logits(double *x, double *qd, const uint16_t *qrow, const uint16_t *kc,
+                         const int32_t *bt, int s, int kvh, int t0, int t1, int Hkv, int d,
+                         int bs, int num_blocks, int max_blocks, double scale, int dtype)
 {
     for (int i = 0; i < d; ++i)
-        qd[i] = oracle_half_bits_to_f64(q[((int64_t)s * Hq + h) * d + i], dtype);
+        qd[i] = oracle_half_bits_to_f64(qrow[i], dtype);
     for (int t = t0; t < t1; ++t) {
         int64_t b = phys_block(bt, s, t, bs, max_blocks, num_blocks);
         if (b < 0)
@@ -203,8 +205,8 @@ int oracle_attention(double *out, const uint16_t *q, const uint16_t *kc,
             continue;
         }
         int kvh = h / g;
-        int r = scaled_logits(x, qd, q, kc, bt, s, h, kvh, 0, L, Hq, Hkv, d, bs,
-                              num_blocks, max_blocks, (double)scale, dtype);
+        int r = scaled_logits(x, qd, q + ((int64_t)s * Hq + h) * d, kc, bt, s, kvh, 0, L,
+                              Hkv, d, bs, num_blocks, max_blocks, (double)scale, dtype);
         if (r == ORACLE_OK) {
             double m, l;
             softmax_v(o, &m, &l, x, vc, bt, s, kvh, 0, L, Hkv, d, bs, num_blocks,
@@ -263,8 +265,9 @@ int oracle_partials(double *tmp_out, double *exp_sums, double *max_logits,
         for (int p = 0; p < n; ++p) {
             int t0 = p * P;
             int t1 = (t0 + P < L) ? t0 + P : L;
-            int r = scaled_logits(x, qd, q, kc, bt, s, h, kvh, t0, t1, Hq, Hkv, d, bs,
-                                  num_blocks, max_blocks, (double)scale, dtype);
+            int r = scaled_logits(x, qd, q + ((int64_t)s * Hq + h) * d, kc, bt, s, kvh, t0,
+                                  t1, Hkv, d, bs, num_blocks, max_blocks, (double)scale,
+                                  dtype);
             if (r != ORACLE_OK) {
 #pragma omp atomic write
                 status = r;
@@ -318,6 +321,73 @@ int oracle_lse_merge(double *out, const double *tmp_out, const double *exp_sums,
             o[i] /= total;
     }
     return ORACLE_OK;
+}
+
+/*
+ * Prefix prefill [prefill]: sequence s holds L = seq_lens[s] tokens in the
+ * cache, the last n_s = q_start[s+1] - q_start[s] of which are new; query row
+ * r = q_start[s] + i (i < n_s) sits at position p = L - n_s + i and attends
+ * to the cache tokens 0..p of its sequence (the whole prefix, and the chunk
+ * causally):
+ *   out[r][h] = softmax_{t<=p}(scale * query[r][h] . k_t) weighted sum of v_t.
+ * query / out are [q_start[S]][Hq][d].  With n_s = 1 for every sequence this
+ * is the decode of oracle_attention.
+ */
+int oracle_prefill(double *out, const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
+                   const int32_t *bt, const int32_t *seq_lens, const int32_t *q_start, int S,
+                   int Hq, int Hkv, int d, int bs, int num_blocks, int max_blocks, float scale,
+                   int dtype)
+{
+    int rc = check_dims(S, Hq, Hkv, d, bs, num_blocks, max_blocks);
+    if (rc == ORACLE_OK)
+        rc = check_lengths(seq_lens, S, bs, max_blocks);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (q_start[0] != 0)
+        return ORACLE_BAD_ARGS;
+    for (int s = 0; s < S; ++s) {
+        int n = q_start[s + 1] - q_start[s];
+        if (n < 0 || n > seq_lens[s])
+            return ORACLE_BAD_ARGS;
+    }
+    int g = Hq / Hkv;
+    int status = ORACLE_OK;
+    int64_t rows = q_start[S];
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < rows * Hq; ++u) {
+        int64_t r = u / Hq;
+        int h = (int)(u % Hq);
+        int s = 0;
+        while (q_start[s + 1] <= r)
+            ++s;
+        int L = seq_lens[s];
+        int n = q_start[s + 1] - q_start[s];
+        int p = L - n + (int)(r - q_start[s]);
+        double *o = out + u * d;
+        double *x = (double *)malloc(sizeof(double) * (size_t)(p + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!x || !qd) {
+            free(x);
+            free(qd);
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+            continue;
+        }
+        int kvh = h / g;
+        int rr = scaled_logits(x, qd, q + (r * Hq + h) * d, kc, bt, s, kvh, 0, p + 1, Hkv, d, bs,
+                               num_blocks, max_blocks, (double)scale, dtype);
+        if (rr == ORACLE_OK) {
+            double m, l;
+            softmax_v(o, &m, &l, x, vc, bt, s, kvh, 0, p + 1, Hkv, d, bs, num_blocks,
+                      max_blocks, dtype);
+        } else {
+#pragma omp atomic write
+            status = rr;
+        }
+        free(x);
+        free(qd);
+    }
+    return status;
 }
 
 /*

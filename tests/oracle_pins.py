@@ -23,7 +23,7 @@ import numpy as np
 import torch
 import torch.nn.functional as F
 
-from workloads import make_dense_case
+from workloads import make_dense_case, make_dense_prefill_case
 
 TOL = 1e-12
 
@@ -229,7 +229,93 @@ def pin_zero_length(orc):
     assert not merged[0].any() and np.abs(merged[1] - ref).max() <= TOL
 
 
+PREFILL_SHAPES = [
+    # ctx_lens, q_lens, Hq, Hkv, d, bs, dtype
+    ([0, 5, 17], [3, 9, 1], 6, 2, 16, 4, torch.float16),
+    ([33, 0], [7, 12], 4, 1, 8, 16, torch.bfloat16),
+    ([2, 40], [1, 4], 8, 4, 32, 1, torch.float16),
+]
+
+
+def _prefill_mask(ctx, n, L):
+    """Visible cache tokens of each chunk row: t <= ctx + i (library-side mask)."""
+    t = torch.arange(L)[None, :]
+    i = torch.arange(n)[:, None]
+    return t <= (L - n) + i
+
+
+def pin_prefill_dense_sdpa(orc):
+    for k, (ctx, ql, Hq, Hkv, d, bs, dt) in enumerate(PREFILL_SHAPES):
+        pc, dk, dv = make_dense_prefill_case(ctx_lens=ctx, q_lens=ql, num_q_heads=Hq,
+                                             num_kv_heads=Hkv, head_dim=d, block_size=bs,
+                                             dtype=dt, seed=600 + k)
+        c = pc.case
+        scale = _scale_f32(d)
+        out = orc.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                          pc.q_start, scale)
+        g = Hq // Hkv
+        for s, (cx, n) in enumerate(zip(ctx, ql)):
+            L = cx + n
+            r0 = int(pc.q_start[s])
+            q = _f64(pc.query[r0:r0 + n]).permute(1, 0, 2)[None]           # [1, Hq, n, d]
+            kk = _f64(dk[s]).permute(1, 0, 2).repeat_interleave(g, dim=0)[None]
+            vv = _f64(dv[s]).permute(1, 0, 2).repeat_interleave(g, dim=0)[None]
+            ref = F.scaled_dot_product_attention(q, kk, vv, attn_mask=_prefill_mask(cx, n, L),
+                                                 scale=scale)[0].permute(1, 0, 2).numpy()
+            err = np.abs(out[r0:r0 + n] - ref).max()
+            assert err <= TOL, f"prefill shape {k} seq {s}: |oracle - sdpa| = {err}"
+
+
+def pin_prefill_no_prefix_is_causal(orc):
+    pc, dk, dv = make_dense_prefill_case(ctx_lens=[0, 0], q_lens=[13, 6], num_q_heads=4,
+                                         num_kv_heads=2, head_dim=16, block_size=4,
+                                         dtype=torch.bfloat16, seed=700)
+    c = pc.case
+    scale = _scale_f32(16)
+    out = orc.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                      pc.q_start, scale)
+    for s, n in enumerate([13, 6]):
+        r0 = int(pc.q_start[s])
+        q = _f64(pc.query[r0:r0 + n]).permute(1, 0, 2)[None]
+        kk = _f64(dk[s]).permute(1, 0, 2).repeat_interleave(2, dim=0)[None]
+        vv = _f64(dv[s]).permute(1, 0, 2).repeat_interleave(2, dim=0)[None]
+        ref = F.scaled_dot_product_attention(q, kk, vv, is_causal=True,
+                                             scale=scale)[0].permute(1, 0, 2).numpy()
+        assert np.abs(out[r0:r0 + n] - ref).max() <= TOL
+
+
+def pin_prefill_zero_query_prefix_means(orc):
+    pc, dk, dv = make_dense_prefill_case(ctx_lens=[11], q_lens=[6], num_q_heads=2,
+                                         num_kv_heads=1, head_dim=8, block_size=4,
+                                         dtype=torch.float16, seed=701)
+    pc.query.zero_()
+    c = pc.case
+    out = orc.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                      pc.q_start, 0.7)
+    v = _f64(dv[0])[:, 0]                                     # [L, d]
+    for i in range(6):
+        ref = v[:11 + i + 1].mean(dim=0).numpy()
+        assert np.abs(out[i, 0] - ref).max() <= TOL and np.abs(out[i, 1] - ref).max() <= TOL
+
+
+def pin_prefill_single_row_is_decode(orc):
+    """A chunk of one token per sequence is the decode of the pinned single pass."""
+    pc, dk, dv = make_dense_prefill_case(ctx_lens=[0, 30, 7], q_lens=[1, 1, 1], num_q_heads=6,
+                                         num_kv_heads=2, head_dim=16, block_size=4,
+                                         dtype=torch.bfloat16, seed=702)
+    c = pc.case
+    scale = _scale_f32(16)
+    a = orc.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                    pc.q_start, scale)
+    b = orc.attention(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, scale)
+    assert np.abs(a - b).max() <= TOL
+
+
 ALL_PINS = [
+    pin_prefill_dense_sdpa,
+    pin_prefill_no_prefix_is_causal,
+    pin_prefill_zero_query_prefix_means,
+    pin_prefill_single_row_is_decode,
     pin_decoder_exhaustive,
     pin_dense_attention,
     pin_gather,

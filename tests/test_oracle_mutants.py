@@ -36,7 +36,12 @@ MUTANTS = {
     "f16_subnormal_exponent": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "block_index_uses_modulo": ("int64_t b = bt[(int64_t)s * max_blocks + t / bs];",
                                 "int64_t b = bt[(int64_t)s * max_blocks + t % bs];"),
-    "query_head_not_used": ("q[((int64_t)s * Hq + h) * d + i]", "q[((int64_t)s * Hq + 0) * d + i]"),
+    "query_head_not_used": ("q + ((int64_t)s * Hq + h) * d", "q + ((int64_t)s * Hq + 0) * d"),
+    "prefill_causal_off_by_one": ("int p = L - n + (int)(r - q_start[s]);",
+                                  "int p = L - n + (int)(r - q_start[s]) + 1;"),
+    "prefill_prefix_ignored": ("int p = L - n + (int)(r - q_start[s]);",
+                               "int p = (int)(r - q_start[s]);"),
+    "prefill_wrong_query_row": ("q + (r * Hq + h) * d", "q + ((int64_t)s * Hq + h) * d"),
 }
 
 

@@ -240,3 +240,56 @@ def make_dense_case(*, lengths: Sequence[int], num_q_heads: int, num_kv_heads: i
         dense_v.append(dv)
     case = Case(w, q, kc, vc, bt, torch.tensor(lengths, dtype=torch.int32), lengths)
     return case, dense_k, dense_v
+
+
+@dataclass
+class PrefillCase:
+    """Inputs of a prefix-prefill batch: the cache holds every sequence's
+    context and its new chunk; ``query`` holds the chunk rows of all sequences
+    (rows q_start[s] .. q_start[s+1]-1 belong to sequence s)."""
+
+    case: Case                  # caches, tables, seq_lens (context + chunk lengths)
+    query: torch.Tensor         # [q_start[-1], Hq, d]
+    q_start: torch.Tensor       # [S + 1] int32
+    q_lens: list = field(default_factory=list)
+
+    def to(self, device) -> "PrefillCase":
+        return PrefillCase(self.case.to(device), self.query.to(device),
+                           self.q_start.to(device), list(self.q_lens))
+
+
+def make_prefill_case(w, *, ctx_lens: Sequence[int], q_lens: Sequence[int], device="cpu",
+                      seed: int = 0) -> PrefillCase:
+    """Prefix-prefill inputs: sequence s has ctx_lens[s] cached tokens followed by
+    q_lens[s] new ones (their K/V already in the cache); query rows are drawn
+    for the new tokens.  Same recipe as ``make_case`` for the cache."""
+    lengths = [int(c) + int(n) for c, n in zip(ctx_lens, q_lens)]
+    case = make_case(w, lengths=lengths, device=device, seed=seed)
+    gen = torch.Generator(device=torch.device(device)).manual_seed(seed + 1)
+    rows = int(sum(q_lens))
+    q = torch.empty((rows, w.num_q_heads, w.head_dim), dtype=w.dtype, device=device)
+    _fill_randn(q, gen)
+    qs = [0]
+    for n in q_lens:
+        qs.append(qs[-1] + int(n))
+    return PrefillCase(case, q, torch.tensor(qs, dtype=torch.int32, device=device),
+                       [int(n) for n in q_lens])
+
+
+def make_dense_prefill_case(*, ctx_lens: Sequence[int], q_lens: Sequence[int],
+                            num_q_heads: int, num_kv_heads: int, head_dim: int,
+                            block_size: int, dtype=torch.float16, seed: int = 0):
+    """Dense-first prefill inputs: returns ``(prefill_case, dense_k, dense_v)`` with
+    the per-sequence dense K/V the paged cache was scattered from."""
+    lengths = [int(c) + int(n) for c, n in zip(ctx_lens, q_lens)]
+    case, dk, dv = make_dense_case(lengths=lengths, num_q_heads=num_q_heads,
+                                   num_kv_heads=num_kv_heads, head_dim=head_dim,
+                                   block_size=block_size, dtype=dtype, seed=seed)
+    gen = torch.Generator().manual_seed(seed + 1)
+    rows = int(sum(q_lens))
+    q = torch.randn((rows, num_q_heads, head_dim), generator=gen).to(dtype)
+    qs = [0]
+    for n in q_lens:
+        qs.append(qs[-1] + int(n))
+    pc = PrefillCase(case, q, torch.tensor(qs, dtype=torch.int32), [int(n) for n in q_lens])
+    return pc, dk, dv
