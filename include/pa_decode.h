@@ -81,7 +81,9 @@ enum {
     PA_DEV_BAD_BLOCK = 1,           /* a block-table entry outside [0, num_blocks) */
     PA_DEV_LEN_CLAMPED = 2,         /* seq_len > max_blocks_per_seq*block_size or < 0 */
     PA_DEV_WAIT_TIMEOUT = 4,        /* a pipeline wait gave up; that output is not written */
-    PA_DEV_TOO_MANY_PARTITIONS = 8  /* ceil(seq_len/partition_size) > max_num_partitions */
+    PA_DEV_TOO_MANY_PARTITIONS = 8, /* ceil(seq_len/partition_size) > max_num_partitions */
+    PA_DEV_BAD_ROWS = 16            /* pa_prefill: q_start rows outside [0, num_rows] or
+                                       a chunk longer than its sequence (skipped) */
 };
 
 /*
@@ -242,6 +244,37 @@ PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_c
                                  int num_blocks, int max_blocks_per_seq, float scale,
                                  int max_seq_len, int single_pass_max_len,
                                  int partition_size, pa_dtype_t dtype, void *stream);
+
+/*
+ * pa_prefill -- prefix prefill over the paged cache (page: project_6 commit
+ * cd0d9e1, "qwen3_6_scripts", the prefix-prefill part of the paged_attn.py
+ * rewrite: the new chunk of each sequence attends to the sequence's whole
+ * cached context, gathered through the block table, and causally to itself).
+ *
+ * The chunk's own K/V must already be written to the cache: sequence s holds
+ * L = seq_lens[s] tokens, the last n_s = q_start[s+1] - q_start[s] of which
+ * are the chunk.  Query row r = q_start[s] + i (0 <= i < n_s) sits at
+ * position p = L - n_s + i and gets
+ *   out[r][h][:] = softmax_{t <= p}(scale * query[r][h] . k_t) weighted sum of v_t
+ * (t over the sequence's cache tokens 0..p; GQA as in pa_decode).  With
+ * n_s = 1 for every sequence this is pa_decode.
+ *
+ * Layouts: query, out [num_rows][num_q_heads][head_dim] (the sequences'
+ * chunks one after another); q_start int32 [num_seqs + 1], non-decreasing,
+ * q_start[0] = 0 and q_start[num_seqs] = num_rows; caches, block_tables,
+ * seq_lens as above.  max_q_len: an upper bound of every n_s (rows past it
+ * are not written and raise PA_DEV_LEN_CLAMPED).  q_start is read on the
+ * device only: a sequence whose rows fall outside [0, num_rows], or whose
+ * chunk is longer than seq_lens[s], is skipped and raises PA_DEV_BAD_ROWS.
+ * Supported: head_dim 64 or 128, block_size a multiple of 16, GQA group
+ * 1..128.  One kernel launch on `stream`; no workspace.
+ */
+PA_API int pa_prefill(void *out, const void *query, const void *key_cache,
+                      const void *value_cache, const int32_t *block_tables,
+                      const int32_t *seq_lens, const int32_t *q_start, int num_seqs,
+                      int num_rows, int max_q_len, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                      float scale, pa_dtype_t dtype, void *stream);
 
 /*
  * pa_gather_kv -- test entry: copies each sequence's K and V rows, fetched

@@ -23,8 +23,9 @@ import torch
 __all__ = [
     "PaError", "load_library", "library_path", "decode", "decode_partitioned",
     "partition_reduce", "decode_auto", "auto_workspace_bytes", "default_single_pass_max_len",
-    "gather_kv", "device_status", "num_partitions", "version",
+    "prefill", "gather_kv", "device_status", "num_partitions", "version",
     "DEV_BAD_BLOCK", "DEV_LEN_CLAMPED", "DEV_WAIT_TIMEOUT", "DEV_TOO_MANY_PARTITIONS",
+    "DEV_BAD_ROWS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +34,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libpadecode.so")
 PA_F16, PA_BF16 = 0, 1
 PHASE_PLAN, PHASE_ATTEND, PHASE_REDUCE = 1, 2, 4
 DEV_BAD_BLOCK, DEV_LEN_CLAMPED, DEV_WAIT_TIMEOUT, DEV_TOO_MANY_PARTITIONS = 1, 2, 4, 8
+DEV_BAD_ROWS = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +55,7 @@ SIGNATURES = [
     ("pa_decode_auto_phases", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t,
                                                            _i, _vp, _i]),
     ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _i, _vp]),
+    ("pa_prefill", _i, [_vp] * 7 + [_i] * 9 + [_f, _i, _vp]),
     ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
     ("pa_selftest_wait_timeout", _i, [_vp, _i]),
     ("pa_device_status", _i, [_vp, ctypes.POINTER(_i)]),
@@ -274,6 +277,33 @@ def decode_auto_static(query, key_cache, value_cache, block_tables, seq_lens, sc
             int(max_seq_len), int(single_pass_max_len), int(partition_size),
             _dtype_code(query), _stream(query))
     _check(st, "pa_decode_auto_static")
+    return out
+
+
+def prefill(query, key_cache, value_cache, block_tables, seq_lens, q_start, scale: float,
+            max_q_len: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefix prefill over the paged cache (``pa_prefill``); returns ``out`` [R, Hq, D].
+
+    ``query`` holds the chunks of all sequences, R rows in all; ``q_start``
+    (int32, S + 1) gives each sequence's first row, and ``max_q_len`` bounds
+    every chunk's length.  The chunks' K/V must already be in the cache.
+    """
+    R, Hq, D = query.shape
+    nb, bs, Hkv, D2 = key_cache.shape
+    if D2 != D:
+        raise ValueError("query and cache head_dim differ")
+    S, mb = block_tables.shape
+    if q_start.shape != (S + 1,):
+        raise ValueError("q_start must have num_seqs + 1 entries")
+    if out is None:
+        out = torch.empty_like(query)
+    with torch.cuda.device(query.device):
+        st = _load().pa_prefill(
+            _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
+            _i32(seq_lens, "seq_lens"), _i32(q_start, "q_start"), S, R, int(max_q_len), Hq,
+            Hkv, D, bs, nb, mb, float(scale), _dtype_code(query), _stream(query))
+    _check(st, "pa_prefill")
     return out
 
 

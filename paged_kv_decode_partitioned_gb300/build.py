@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libpadecode.so")
 
-SOURCES = ["pa_api.cu", "pa_aux.cu", "pa_inst_bf16.cu", "pa_inst_f16.cu", "pa_static.cu"]
+SOURCES = ["pa_api.cu", "pa_aux.cu", "pa_inst_bf16.cu", "pa_inst_f16.cu", "pa_prefill.cu",
+           "pa_static.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

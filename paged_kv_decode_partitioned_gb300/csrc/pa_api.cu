@@ -555,6 +555,68 @@ int pa_gather_kv(void *k_dense, void *v_dense, const void *key_cache, const void
                : PA_ERR_CUDA;
 }
 
+int pa_prefill(void *out, const void *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, const int32_t *q_start,
+               int num_seqs, int num_rows, int max_q_len, int num_q_heads, int num_kv_heads,
+               int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+               float scale, pa_dtype_t dtype, void *stream) {
+    if (num_seqs < 0 || num_rows < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARGUMENT;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size % kTile != 0) return PA_ERR_UNSUPPORTED;
+    if (group > kPrefillRows) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_rows) * num_q_heads * head_dim > (static_cast<int64_t>(1) << 40))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (num_seqs == 0 || num_rows == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !q_start)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+        !aligned(q_start, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    CUtensorMap tk, tv;
+    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                             num_blocks)) != PA_OK)
+        return rc;
+    PrefillParams p{};
+    p.q = query;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.q_start = q_start;
+    p.status = di->status;
+    p.num_seqs = num_seqs;
+    p.num_rows = num_rows;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.block_size = block_size;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.tokens_per_cta = kPrefillRows / group;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    const dim3 grid((max_q_len + p.tokens_per_cta - 1) / p.tokens_per_cta, num_kv_heads,
+                    num_seqs);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        dtype == PA_BF16 ? launch_prefill<__nv_bfloat16>(head_dim, tk, tv, p, grid, st)
+                         : launch_prefill<__half>(head_dim, tk, tv, p, grid, st);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_selftest_wait_timeout(void *stream, int limit_us) {
     if (limit_us <= 0 || limit_us > 1000000) return PA_ERR_INVALID_ARGUMENT;
     DevInfo *di = nullptr;

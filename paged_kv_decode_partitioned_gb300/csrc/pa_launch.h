@@ -1,7 +1,7 @@
 // pa_launch.h -- declarations of the kernel launchers.  The attention and
 // reduce launchers are templates explicitly instantiated per dtype in
-// pa_inst_bf16.cu / pa_inst_f16.cu; the planner and gather launchers live in
-// pa_aux.cu.
+// pa_inst_bf16.cu / pa_inst_f16.cu, the prefill launcher in pa_prefill.cu;
+// the planner and gather launchers live in pa_aux.cu.
 #pragma once
 
 #include <cuda.h>
@@ -18,6 +18,10 @@ template <typename T>
 int attn_ctas_per_sm(int D, int mode);
 template <typename T>
 cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st);
+
+template <typename T>
+cudaError_t launch_prefill(int D, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                           const PrefillParams &p, dim3 grid, cudaStream_t st);
 
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, cudaStream_t st);

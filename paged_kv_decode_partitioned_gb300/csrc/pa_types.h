@@ -9,12 +9,13 @@ namespace pa {
 
 constexpr int kTile = 16;       // tokens per pipeline tile (the MMA M of S^T)
 constexpr int kHeadsPad = 8;    // query heads per KV head, padded to the MMA N
+constexpr int kPrefillRows = 128;   // query rows (chunk token x group head) per prefill CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s
 
 // Flags of the device status word (mirrors PA_DEV_* in pa_decode.h).
-enum : int { kBadBlock = 1, kLenClamped = 2, kWaitTimeout = 4, kTooManyParts = 8 };
+enum : int { kBadBlock = 1, kLenClamped = 2, kWaitTimeout = 4, kTooManyParts = 8, kBadRows = 16 };
 
 // Unit kinds.
 enum : int { kOutFinal = 0, kOutPartialDense = 1, kOutPartialCompact = 2 };
@@ -64,6 +65,18 @@ struct PlanParams {
     int *pseq_count;
     int *status;
     int num_seqs, num_kv_heads, partition_size, single_pass_max_len, len_cap, max_parts;
+};
+
+struct PrefillParams {
+    const void *q;              // [num_rows][Hq][D]
+    void *out;                  // [num_rows][Hq][D]
+    const int32_t *block_tables;
+    const int32_t *seq_lens;    // cached tokens per sequence, the chunk included
+    const int32_t *q_start;     // [S + 1] first chunk row of each sequence
+    int *status;
+    int num_seqs, num_rows, num_q_heads, num_kv_heads, group, block_size, max_blocks, num_blocks;
+    int tokens_per_cta;         // chunk tokens per CTA (128 query rows / group)
+    float scale_log2;           // scale * log2(e)
 };
 
 struct GatherParams {

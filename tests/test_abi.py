@@ -135,3 +135,35 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "pa_oracle" not in text, f
+
+
+def _prefill(lib, **kw):
+    args = dict(out=A, q=A, k=A, v=A, bt=A, sl=A, qs=A, S=2, R=40, mq=30, Hq=24, Hkv=4, D=128,
+                bs=16, nb=10, mb=4, scale=0.1, dtype=1)
+    args.update(kw)
+    return lib.pa_prefill(args["out"], args["q"], args["k"], args["v"], args["bt"], args["sl"],
+                          args["qs"], args["S"], args["R"], args["mq"], args["Hq"], args["Hkv"],
+                          args["D"], args["bs"], args["nb"], args["mb"], args["scale"],
+                          args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=256), -2),                # head_dim not supported by the prefill kernel
+    (dict(D=96), -2),
+    (dict(bs=8), -2),                 # block_size not a multiple of 16
+    (dict(Hq=256, Hkv=1), -2),        # more than 128 query heads per KV head
+    (dict(Hq=10, Hkv=4), -1),         # Hq not a multiple of Hkv
+    (dict(R=-1), -1),
+    (dict(mq=-1), -1),
+    (dict(dtype=7), -1),
+    (dict(qs=0), -1),                 # null q_start
+    (dict(out=0), -1),
+    (dict(nb=0), -1),
+    (dict(q=A + 8), -3),              # misaligned query
+    (dict(qs=A + 2), -3),             # misaligned q_start
+    (dict(S=0), 0),                   # nothing to do
+    (dict(R=0), 0),
+    (dict(mq=0), 0),
+])
+def test_prefill_rejects_on_host(lib, kw, status):
+    assert _prefill(lib, **kw) == status

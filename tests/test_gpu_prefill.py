@@ -1,0 +1,206 @@
+"""Prefix prefill (``pa_prefill``) against the fp64 oracle, element by element.
+
+Sweeps head_dim, GQA group (1 to 128 query heads per KV head, so 128 down to 1
+chunk tokens per CTA), block size, dtype and ragged shapes: no prefix (pure
+causal), one-row chunks, chunks spanning several CTAs with a partial last
+one, empty chunks, contexts that end inside a 32-token stage.  Larger chunks
+are checked on sampled rows: row i of a chunk of n over L cached tokens is the
+decode of that row over the first L - n + i + 1 tokens (the prefill pages'
+causal reading), which the oracle's decode computes one row at a time.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_helpers import assert_out_close, to_f64
+from workloads import custom_workload, make_prefill_case
+
+pytestmark = pytest.mark.gpu
+
+# ctx_lens, q_lens, Hq, Hkv, D, bs, dtype
+SHAPES = [
+    ([0, 5, 100, 1000], [37, 1, 300, 64], 24, 4, 128, 16, torch.bfloat16),
+    ([31, 513], [200, 17], 8, 1, 128, 32, torch.float16),
+    ([64, 0, 2000], [129, 16, 33], 4, 4, 64, 16, torch.bfloat16),
+    ([250, 777], [90, 3], 32, 2, 64, 64, torch.float16),
+    ([15, 1, 40], [0, 50, 7], 12, 6, 128, 16, torch.bfloat16),
+    ([100], [10], 128, 1, 64, 16, torch.bfloat16),
+    ([3000, 47], [1, 1], 24, 8, 128, 16, torch.float16),
+]
+IDS = [f"d{s[4]}_g{s[2] // s[3]}_bs{s[5]}_{str(s[6])[6:]}" for s in SHAPES]
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_decode_partitioned_gb300 as pa
+    from paged_kv_decode_partitioned_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pa.load_library()
+    return pa
+
+
+def _workload(Hq, Hkv, D, bs, dt):
+    return custom_workload(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                           dtype=dt)
+
+
+def _run(pa, pc_dev, max_q_len=None):
+    c = pc_dev.case
+    mq = max(pc_dev.q_lens + [0]) if max_q_len is None else max_q_len
+    return pa.prefill(pc_dev.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                      pc_dev.q_start, c.scale, mq)
+
+
+def _oracle(pc):
+    c = pc.case
+    return oracle.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                          pc.q_start, c.scale)
+
+
+@pytest.mark.parametrize("i", range(len(SHAPES)), ids=IDS)
+def test_prefill_matches_oracle(pa, i):
+    ctx, ql, Hq, Hkv, D, bs, dt = SHAPES[i]
+    host = make_prefill_case(_workload(Hq, Hkv, D, bs, dt), ctx_lens=ctx, q_lens=ql,
+                             seed=3000 + i)
+    out = _run(pa, host.to("cuda"))
+    assert_out_close(out, _oracle(host), f"pa_prefill shape {i}")
+    assert pa.device_status() == 0
+
+
+def test_one_row_chunks_equal_decode(pa):
+    """n_s = 1 for every sequence: the prefill is the decode of the same query."""
+    w = _workload(24, 4, 128, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[0, 15, 16, 500, 4095], q_lens=[1] * 5, seed=3100)
+    dev = host.to("cuda")
+    out = _run(pa, dev)
+    c = dev.case
+    dec = pa.decode(dev.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, c.scale)
+    ref = oracle.attention(host.query, host.case.key_cache, host.case.value_cache,
+                           host.case.block_tables, host.case.seq_lens, host.case.scale)
+    assert_out_close(out, ref, "prefill of one-row chunks")
+    assert_out_close(dec, ref, "decode")
+    assert np.abs(to_f64(out) - to_f64(dec)).max() <= 2e-2
+    assert pa.device_status() == 0
+
+
+def test_nan_past_the_context_is_never_used(pa):
+    """Cache rows past each sequence's last token (and unused blocks) hold NaN:
+    the masked logits and the zeroed V rows of the last stage keep them out."""
+    w = _workload(16, 2, 128, 32, torch.float16)
+    host = make_prefill_case(w, ctx_lens=[7, 100, 33], q_lens=[20, 61, 1], seed=3200)
+    kc, vc = host.case.key_cache.clone(), host.case.value_cache.clone()
+    bs = kc.shape[1]
+    used = torch.zeros(kc.shape[0], dtype=torch.bool)
+    for s, L in enumerate(host.case.seq_lens_list):
+        nblk = -(-L // bs)
+        blocks = host.case.block_tables[s, :nblk].long()
+        used[blocks] = True
+        last = int(blocks[-1])
+        kc[last, L - (nblk - 1) * bs:] = float("nan")
+        vc[last, L - (nblk - 1) * bs:] = float("nan")
+    kc[~used] = float("nan")
+    vc[~used] = float("nan")
+    host.case.key_cache, host.case.value_cache = kc, vc
+    out = _run(pa, host.to("cuda"))
+    assert_out_close(out, _oracle(host), "prefill with NaN past the context")
+    assert pa.device_status() == 0
+
+
+def test_block_permutation_gives_identical_bits(pa):
+    """Which physical block holds a page does not change a single output bit."""
+    w = _workload(24, 4, 128, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[300, 50], q_lens=[80, 40], seed=3300)
+    dev = host.to("cuda")
+    out1 = _run(pa, dev)
+    nb = dev.case.key_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(5)).to("cuda")
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nb, device="cuda")
+    kc = dev.case.key_cache[perm].contiguous()   # new block j holds old block perm[j]
+    vc = dev.case.value_cache[perm].contiguous()
+    bt = dev.case.block_tables.clone()
+    valid = bt >= 0
+    bt[valid] = inv[bt[valid].long()].to(torch.int32)
+    out2 = pa.prefill(dev.query, kc, vc, bt, dev.case.seq_lens, dev.q_start, dev.case.scale,
+                      max(dev.q_lens))
+    assert torch.equal(out1, out2)
+    assert pa.device_status() == 0
+
+
+def _sampled_rows_check(pa, host, dev, out, rows_per_seq, seed):
+    """Compare sampled rows with the oracle's decode over the row's visible prefix."""
+    c = host.case
+    qs = host.q_start.tolist()
+    g = torch.Generator().manual_seed(seed)
+    checked = 0
+    for s, n in enumerate(host.q_lens):
+        if n == 0:
+            continue
+        L = c.seq_lens_list[s]
+        picks = {0, n - 1} | set(torch.randint(0, n, (rows_per_seq,), generator=g).tolist())
+        for i in sorted(picks):
+            r = qs[s] + i
+            p = L - n + i
+            ref = oracle.attention(host.query[r:r + 1], c.key_cache, c.value_cache,
+                                   c.block_tables[s:s + 1], torch.tensor([p + 1],
+                                                                         dtype=torch.int32),
+                                   c.scale)
+            assert_out_close(out[r:r + 1], ref, f"row {i} of sequence {s}")
+            checked += 1
+    return checked
+
+
+def test_long_chunk_over_long_context_sampled(pa):
+    """A 4096-token chunk after a 28K-token prefix (plus a second sequence
+    with no prefix), sampled rows against the oracle."""
+    w = _workload(24, 4, 128, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[28000, 0], q_lens=[4096, 3000], seed=3400)
+    dev = host.to("cuda")
+    out = _run(pa, dev)
+    assert _sampled_rows_check(pa, host, dev, out, 6, 11) >= 10
+    assert pa.device_status() == 0
+
+
+def test_rows_outside_the_query_raise_flag_and_are_skipped(pa):
+    w = _workload(8, 1, 64, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[10, 20, 30], q_lens=[5, 6, 7], seed=3500)
+    dev = host.to("cuda")
+    ref = _oracle(host)
+    bad = dev.q_start.clone()
+    bad[2] = 100   # sequence 1 would end and sequence 2 start past the 18 rows
+    out = torch.full_like(dev.query, 7.0)
+    c = dev.case
+    pa.prefill(dev.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, bad, c.scale,
+               7, out=out)
+    assert pa.device_status() & pa.DEV_BAD_ROWS
+    assert_out_close(out[:5], ref[:5], "sequence 0 still computed")
+    assert bool((out[5:] == 7.0).all())
+
+
+def test_chunk_longer_than_context_raises_flag(pa):
+    w = _workload(8, 1, 64, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[10, 20], q_lens=[5, 6], seed=3600)
+    dev = host.to("cuda")
+    c = dev.case
+    lens = c.seq_lens.clone()
+    lens[1] = 3   # 6 chunk rows but only 3 cached tokens
+    out = torch.full_like(dev.query, 7.0)
+    pa.prefill(dev.query, c.key_cache, c.value_cache, c.block_tables, lens, dev.q_start, c.scale,
+               6, out=out)
+    assert pa.device_status() & pa.DEV_BAD_ROWS
+    assert_out_close(out[:5], _oracle(host)[:5], "sequence 0 still computed")
+    assert bool((out[5:] == 7.0).all())
+
+
+def test_max_q_len_too_small_raises_flag(pa):
+    w = _workload(8, 1, 64, 16, torch.bfloat16)   # 16 chunk tokens per CTA
+    host = make_prefill_case(w, ctx_lens=[10], q_lens=[40], seed=3700)
+    dev = host.to("cuda")
+    c = dev.case
+    out = torch.full_like(dev.query, 7.0)
+    pa.prefill(dev.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, dev.q_start,
+               c.scale, 16, out=out)
+    assert pa.device_status() & pa.DEV_LEN_CLAMPED
+    assert_out_close(out[:16], _oracle(host)[:16], "rows covered by max_q_len")
