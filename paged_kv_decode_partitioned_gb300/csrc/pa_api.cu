@@ -101,6 +101,29 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// 4-D view of a prefill query [num_rows][Hq][D] for TMA: (element within a
+// 64-element piece, piece, query head, row); one box = one piece of the
+// `group` heads of a KV head for `tokens` consecutive rows, landing as
+// (row, head)-ordered 128-byte rows, 128-byte swizzled.  Rows past num_rows
+// read zeros.
+int make_query_map(CUtensorMap *m, const void *query, pa_dtype_t dtype, int D, int Hq,
+                   int num_rows, int group, int tokens) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PA_ERR_NO_DEVICE;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(Hq),
+                          static_cast<cuuint64_t>(num_rows)};
+    cuuint64_t strides[3] = {64 * e, D * e, static_cast<cuuint64_t>(Hq) * D * e};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tokens)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    4, const_cast<void *>(query), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Shape {
@@ -566,7 +589,7 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARGUMENT;
     const int group = num_q_heads / num_kv_heads;
-    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (block_size % kTile != 0) return PA_ERR_UNSUPPORTED;
     if (group > kPrefillRows) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
@@ -611,9 +634,13 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     const dim3 grid((max_q_len + p.tokens_per_cta - 1) / p.tokens_per_cta, num_kv_heads,
                     num_seqs);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap tq;
+    if ((rc = make_query_map(&tq, query, dtype, head_dim, num_q_heads, num_rows, group,
+                             p.tokens_per_cta)) != PA_OK)
+        return rc;
     const cudaError_t e =
-        dtype == PA_BF16 ? launch_prefill<__nv_bfloat16>(head_dim, tk, tv, p, grid, st)
-                         : launch_prefill<__half>(head_dim, tk, tv, p, grid, st);
+        dtype == PA_BF16 ? launch_prefill_tc<__nv_bfloat16>(head_dim, tq, tk, tv, p, grid, st)
+                         : launch_prefill_tc<__half>(head_dim, tq, tk, tv, p, grid, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -20,8 +20,9 @@ template <typename T>
 cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st);
 
 template <typename T>
-cudaError_t launch_prefill(int D, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                           const PrefillParams &p, dim3 grid, cudaStream_t st);
+cudaError_t launch_prefill_tc(int D, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                              const CUtensorMap &tmV, const PrefillParams &p, dim3 grid,
+                              cudaStream_t st);
 
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, cudaStream_t st);

@@ -1,0 +1,524 @@
+// pa_prefill_tc.cuh -- paged prefix-prefill attention on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory) for GB300 (sm_103a).
+//
+// The operation (page: project_6 commit cd0d9e1, "qwen3_6_scripts", the
+// prefix-prefill part of the paged_attn.py rewrite): a chunk of new tokens of
+// each sequence attends to the sequence's whole cached context and, causally,
+// to the chunk itself.  The chunk's K/V are already in the paged cache, so
+// chunk row i of sequence s (n chunk tokens, L cached tokens) sits at
+// position p = L - n + i and attends to cache tokens 0..p.  The pages' tile
+// loop (matmul, softmax, matmul per key tile with the running max and sum of
+// the online softmax) is what one CTA runs below.
+//
+// One CTA = 128 query rows of one (sequence, KV head): row = chunk token x
+// query head of the GQA group, so every row of the CTA uses every K/V tile
+// it loads.  Warp roles (192 threads):
+//   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
+//              x the CTA's chunk tokens), then N-token K and V tiles of the
+//              context through NS shared-memory stages, walking the block
+//              table through a lane-distributed window of 16-token box ids;
+//   warp 1     tensor-memory owner and MMA issuer (one thread): S_j = Q K_j^T
+//              into one of two S buffers in tensor memory and
+//              O += P_j V_j with P read from tensor memory (the S buffer it
+//              was written over) and O accumulating in tensor memory, each
+//              issued as soon as its inputs are ready; tcgen05.commit
+//              completes the mbarriers that free K and V stages separately;
+//   warps 2-5  softmax (one thread per row, the row's tensor-memory lane):
+//              S row -> causal mask -> scale -> running max -> exp2 -> P (bf16
+//              or f16) written back into tensor memory; O is rescaled in
+//              tensor memory only when a row's max grows by more than 2^8
+//              (exponents stay below 2^8 in between and the final division by
+//              the running sum is exact either way); finally O / l -> out.
+// Every mbarrier wait is bounded; a role that gives up raises
+// PA_DEV_WAIT_TIMEOUT and leaves its loop, in-flight copies and MMAs are
+// waited for (bounded) and tensor memory is freed before the CTA exits.
+#pragma once
+
+#include "pa_launch.cuh"
+#include "pa_tc05.cuh"
+
+namespace pa {
+
+// Tile plan per head_dim.  d64 / d128: 64-token K/V tiles and a 256-column
+// tensor-memory footprint, so two CTAs share an SM and one CTA's softmax
+// overlaps the other's MMAs.  d256: one CTA per SM.
+#ifndef PA_PREFILL_TC_N
+#define PA_PREFILL_TC_N 64
+#endif
+template <int D>
+struct PrefillTcCfg {
+    static constexpr int kRows = kPrefillRows;                   // 128 query rows (MMA M)
+    static constexpr int kN = D <= 128 ? PA_PREFILL_TC_N : 64;   // cache tokens per tile
+    static constexpr int kCtasPerSm = (D <= 128 && kN == 64) ? 2 : 1;
+    static constexpr int kStages = kCtasPerSm == 2 ? (D <= 64 ? 4 : 2)
+                                                   : (D <= 64 ? 6 : (D <= 128 ? 3 : 2));
+    static constexpr int kPieces = D / 64;
+    static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
+    static constexpr int kKvPiece = kN * 128;                    // bytes of one K (V) piece
+    static constexpr int kQBytes = kPieces * kQPiece;
+    static constexpr int kTileBytes = kPieces * kKvPiece;        // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
+    // barriers: q_full, o_full, vtail, mma_done, k_full[NS], v_full[NS],
+    // k_empty[NS], v_empty[NS], s_full[2], p_full[2], s_free[2]; then the
+    // tensor-memory slot
+    static constexpr int kNumBars = 4 + 4 * kStages + 6;
+    static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
+    static constexpr int kLaunchBytes = kSlotOffset + 16 + 1024;
+    static constexpr int kThreads = 192;
+    // tensor memory: S0 [0, N), S1 [N, 2N), O [2N, 2N + D), rounded up to a power of two
+    static constexpr int kOCol = 2 * kN;
+    static constexpr int kTmemCols = kOCol + D <= 256 ? 256 : 512;
+    static_assert(kLaunchBytes * kCtasPerSm <= 228 * 1024 - 1024 * kCtasPerSm,
+                  "shared memory plan too large");
+    static_assert(kOCol + D <= kTmemCols && kTmemCols * kCtasPerSm <= 512,
+                  "tensor memory plan too large");
+};
+
+template <typename T> struct TcType;
+template <> struct TcType<__nv_bfloat16> { static constexpr int code = 1; };
+template <> struct TcType<__half> { static constexpr int code = 0; };
+
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// Non-blocking test of phase `parity` of an mbarrier.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false after ~1e9 SM cycles (0.5 s
+// at 2 GHz).  The pipeline here waits several times per tile, so the limit
+// is kept with the SM's own cycle counter, which is cheap to read, not with
+// the global timer.
+__device__ __forceinline__ bool mbar_wait_cycles(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u && clock64() - t0 > 1000000000ll) return false;
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
+    pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+    using C = PrefillTcCfg<D>;
+    constexpr int N = C::kN, NS = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t base = smem_u32(smem);
+    const uint32_t q_smem = base;
+    const uint32_t stage0 = base + C::kQBytes;
+    const uint32_t bars = base + C::kBarOffset;
+    const uint32_t q_full = bars, o_full = bars + 8, vtail = bars + 16, mma_done = bars + 24;
+    const uint32_t k_full = bars + 32, v_full = k_full + NS * 8;
+    const uint32_t k_empty = v_full + NS * 8, v_empty = k_empty + NS * 8;
+    const uint32_t s_full = v_empty + NS * 8, p_full = s_full + 16, s_free = p_full + 16;
+    const uint32_t slot = base + C::kSlotOffset;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int g = p.group;
+
+    // ---- which rows and which context this CTA covers (uniform over the CTA) ----
+    const int cap = p.max_blocks * p.block_size;
+    const int L = clamp_len(p.seq_lens, s, cap, p.status);
+    const int row0 = __ldg(p.q_start + s), row1 = __ldg(p.q_start + s + 1);
+    const bool first = blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0;
+    if (row0 < 0 || row1 < row0 || row1 > p.num_rows) {   // rows outside the query
+        if (first) atomicOr(p.status, kBadRows);
+        return;
+    }
+    const int n = row1 - row0;
+    if (n > L) {   // a chunk longer than its whole context: the sequence is skipped
+        if (first) atomicOr(p.status, kBadRows);
+        return;
+    }
+    if (first && n > static_cast<int>(gridDim.x) * p.tokens_per_cta)
+        atomicOr(p.status, kLenClamped);   // chunk longer than max_q_len: its tail is not written
+    const int tok0 = qt * p.tokens_per_cta;
+    if (tok0 >= n) return;
+    const int ntok = min(p.tokens_per_cta, n - tok0);
+    const int pos_first = L - n + tok0;   // position of the CTA's first chunk token
+    const int kv_end = pos_first + ntok;  // cache tokens any row of the CTA sees
+    const int ntiles = (kv_end + N - 1) / N;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmQ);
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        mbar_init(q_full, 1);
+        mbar_init(o_full, 1);
+        mbar_init(vtail, 1);
+        mbar_init(mma_done, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full + i * 8, 1);
+            mbar_init(v_full + i * 8, 1);
+            mbar_init(k_empty + i * 8, 1);
+            mbar_init(v_empty + i * 8, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i * 8, 1);
+            mbar_init(p_full + i * 8, 4);   // one arrive per softmax warp
+            mbar_init(s_free + i * 8, 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tc05::alloc(slot, C::kTmemCols);
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kSlotOffset);
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+        const int nbox = (kv_end + kTile - 1) / kTile;
+        constexpr int kBoxes = N / kTile;   // 16-token boxes per tile
+        auto fetch = [&](int bx) -> int {
+            if (bx >= nbox) return 0;
+            const int b = __ldg(bt_row + (bx * kTile) / p.block_size);
+            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
+                atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
+            return b;
+        };
+        // Q rows the box does not cover (128 % group) are never loaded: zero
+        // them so those rows stay finite (and never force an O rescale).
+        const int qrows = g * p.tokens_per_cta;
+        if (qrows < C::kRows) {
+            for (int c = 0; c < C::kPieces; ++c)
+                for (int e = lane; e < (C::kRows - qrows) * 8; e += 32)
+                    *reinterpret_cast<uint4 *>(smem + c * C::kQPiece + qrows * 128 + e * 16) =
+                        make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        if (lane == 0) {
+            mbar_expect_tx(q_full, static_cast<uint32_t>(C::kPieces * 128 * qrows));
+#pragma unroll
+            for (int c = 0; c < C::kPieces; ++c)
+                tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
+        }
+        int win_cur = fetch(lane), win_next = fetch(32 + lane), win_base = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j % NS;
+            const uint32_t kdst = stage0 + st * C::kStageBytes, vdst = kdst + C::kTileBytes;
+            const bool last = j == ntiles - 1;
+            const uint32_t vbar = last ? vtail : v_full + st * 8;
+            int phys[kBoxes];
+            int boxes = 0;
+#pragma unroll
+            for (int k = 0; k < kBoxes; ++k) {
+                const int bx = j * kBoxes + k;
+                if (bx - win_base >= 32) {   // slide the block-table window
+                    win_cur = win_next;
+                    win_base += 32;
+                    win_next = fetch(win_base + 32 + lane);
+                }
+                phys[k] = __shfl_sync(0xffffffffu, win_cur, bx - win_base);
+                boxes += bx < nbox;
+            }
+            const uint32_t bytes = static_cast<uint32_t>(boxes * C::kPieces * 2048);
+            // K of tile j once QK of tile j - NS is done, V once its PV is done
+            if (j >= NS) {
+                const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NS) - 1) & 1u);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (lane == 0) {
+                mbar_expect_tx(k_full + st * 8, bytes);
+#pragma unroll
+                for (int k = 0; k < kBoxes; ++k)
+                    if (j * kBoxes + k < nbox) {
+                        const int row = ((j * kBoxes + k) * kTile) % p.block_size;
+#pragma unroll
+                        for (int c = 0; c < C::kPieces; ++c)
+                            tma_load_5d(kdst + c * C::kKvPiece + k * 2048, &tmK, k_full + st * 8,
+                                        0, c, kvh, row, phys[k]);
+                    }
+            }
+            if (j >= NS) {
+                const bool w = mbar_wait_cycles(v_empty + st * 8, ((j / NS) - 1) & 1u);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    issued = j;   // K of tile j is in flight: wait for it below
+                    (void)mbar_wait_cycles(k_full + st * 8, (j / NS) & 1u);
+                    break;
+                }
+            }
+            if (lane == 0) {
+                mbar_expect_tx(vbar, bytes);
+#pragma unroll
+                for (int k = 0; k < kBoxes; ++k)
+                    if (j * kBoxes + k < nbox) {
+                        const int row = ((j * kBoxes + k) * kTile) % p.block_size;
+#pragma unroll
+                        for (int c = 0; c < C::kPieces; ++c)
+                            tma_load_5d(vdst + c * C::kKvPiece + k * 2048, &tmV, vbar, 0, c, kvh,
+                                        row, phys[k]);
+                    }
+            }
+            issued = j + 1;
+            if (last) {
+                // V rows at or past kv_end hold cache data past the context (or
+                // nothing): zero them before the MMA reads V, since 0 * NaN != 0.
+                const bool w = mbar_wait_cycles(vtail, 0);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+                const int first_row = kv_end - j * N;
+                const int nchunks = (N - first_row) * 8;   // 16-byte chunks per piece
+                for (int c = 0; c < C::kPieces; ++c)
+                    for (int e = lane; e < nchunks; e += 32)
+                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + c * C::kKvPiece +
+                                                   first_row * 128 + e * 16) =
+                            make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(v_full + st * 8);
+            }
+        }
+        if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
+        // copies still landing must land before the CTA exits
+        (void)mbar_wait_cycles(q_full, 0);
+        for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
+            (void)mbar_wait_cycles(k_full + (j % NS) * 8, (j / NS) & 1u);
+            if (j != ntiles - 1)
+                (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
+        }
+        if (issued == ntiles) (void)mbar_wait_cycles(vtail, 0);
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
+            constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
+            bool ok = mbar_wait_cycles(q_full, 0);
+            // Issue whichever of QK (next tile) and PV (oldest tile with P ready)
+            // can go: a late K tile must not hold back the PV that frees a stage.
+            int qk = 0, pv = 0;
+            bool idle = false;
+            long long idle_since = 0;
+            while (ok && pv < ntiles) {
+                bool progress = false;
+                if (pv < qk && mbar_test(p_full + (pv & 1) * 8, (pv >> 1) & 1u) &&
+                    mbar_test(v_full + (pv % NS) * 8, (pv / NS) & 1u)) {
+                    tc05::fence_after_sync();
+                    const int bb = pv & 1;
+                    const uint32_t vst = stage0 + (pv % NS) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+                    for (int kt = 0; kt < N / 16; ++kt)
+                        tc05::mma_ts(tmem + C::kOCol, tmem + bb * N + kt * 8,
+                                     tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
+                                     idesc_pv, (pv > 0 || kt > 0) ? 1u : 0u);
+                    tc05::commit(s_free + bb * 8);
+                    tc05::commit(v_empty + (pv % NS) * 8);
+                    ++pv;
+                    progress = true;
+                }
+                // S buffer qk & 1 is free once PV of tile qk - 2 has completed
+                if (qk < ntiles && qk <= pv + 1 &&
+                    mbar_test(k_full + (qk % NS) * 8, (qk / NS) & 1u) &&
+                    (qk < 2 || mbar_test(s_free + (qk & 1) * 8, ((qk - 2) >> 1) & 1u))) {
+                    tc05::fence_after_sync();
+                    const uint32_t kst = stage0 + (qk % NS) * C::kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc05::mma_ss(tmem + (qk & 1) * N,
+                                     tc05::sw128_desc(q_smem + (kk >> 2) * C::kQPiece + (kk & 3) * 32,
+                                                      16, 1024),
+                                     tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32,
+                                                      16, 1024),
+                                     idesc_qk, kk > 0 ? 1u : 0u);
+                    tc05::commit(s_full + (qk & 1) * 8);
+                    tc05::commit(k_empty + (qk % NS) * 8);
+                    ++qk;
+                    progress = true;
+                }
+                if (progress) {
+                    idle = false;
+                } else if (!idle) {
+                    idle = true;
+                    idle_since = clock64();
+                } else if (clock64() - idle_since > 1000000000ll) {
+                    ok = false;
+                } else {
+                    __nanosleep(20);
+                }
+            }
+            if (ok) tc05::commit(o_full);
+            if (!ok) atomicOr(p.status, kWaitTimeout);
+            // every MMA issued has completed before tensor memory is freed
+            tc05::commit(mma_done);
+            (void)mbar_wait_cycles(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ softmax ------------------------------
+        const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
+        const int r = quarter * 32 + lane;
+        const int rows_used = g * ntok;
+        const bool valid = r < rows_used;
+        const int tq = valid ? r / g : ntok - 1, hq = valid ? r % g : 0;
+        const int pos = pos_first + tq;   // last cache token this row sees
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int b = j & 1;
+            const bool w = mbar_wait_cycles(s_full + b * 8, (j >> 1) & 1u);
+            if (!__all_sync(0xffffffffu, w)) {
+                ok = false;
+                break;
+            }
+            tc05::fence_after_sync();
+            const uint32_t sb = tmem + lane_base + b * N;
+            float x[N];
+            {
+                uint32_t rr[N];
+                if constexpr (N == 128) tc05::ld128(sb, rr);
+                else tc05::ld64(sb, rr);
+#pragma unroll
+                for (int c = 0; c < N; ++c) x[c] = __uint_as_float(rr[c]);
+            }
+            const int lim = pos - j * N;   // columns c <= lim are visible
+            float mx[8];   // eight independent max chains
+            if (lim >= N - 1) {
+#pragma unroll
+                for (int c = 0; c < N; ++c) {
+                    x[c] *= sl2;
+                    mx[c & 7] = c < 8 ? x[c] : fmaxf(mx[c & 7], x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < N; ++c) {
+                    x[c] = c <= lim ? x[c] * sl2 : -INFINITY;
+                    mx[c & 7] = c < 8 ? x[c] : fmaxf(mx[c & 7], x[c]);
+                }
+            }
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            if (j == 0) {
+                m = mt;   // column 0 (cache token 0) is visible to every row
+            } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
+                // O must hold P_{j-1} V_{j-1} before it is rescaled
+                const bool w2 = mbar_wait_cycles(s_free + ((j - 1) & 1) * 8, ((j - 1) >> 1) & 1u);
+                if (!__all_sync(0xffffffffu, w2)) {
+                    ok = false;
+                    break;
+                }
+                tc05::fence_after_sync();
+                const float mn = fmaxf(m, mt);
+                const float alpha = ex2(m - mn);
+                m = mn;
+                l *= alpha;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t rr[32];
+                    tc05::ld32(tmem + lane_base + C::kOCol + c0, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                    tc05::st32(tmem + lane_base + C::kOCol + c0, rr);
+                }
+            }
+            float sm[8];   // eight independent sum chains
+            uint32_t pk[N / 2];
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float e0 = ex2(x[2 * i] - m), e1 = ex2(x[2 * i + 1] - m);
+                sm[i & 7] = i < 8 ? e0 + e1 : sm[i & 7] + (e0 + e1);
+                pk[i] = Mma<T>::pack(e0, e1);
+            }
+            if constexpr (N == 128) tc05::st64(sb, pk);   // P over the first N/2 columns of S
+            else tc05::st32(sb, pk);
+            l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            tc05::wait_st();
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(p_full + b * 8);
+        }
+        if (ok) {
+            const bool w = mbar_wait_cycles(o_full, 0);
+            ok = __all_sync(0xffffffffu, w);
+        }
+        if (ok) {
+            tc05::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            T *orow = static_cast<T *>(p.out) +
+                      (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t rr[32];
+                tc05::ld32(tmem + lane_base + C::kOCol + c0, rr);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 v;
+                        v.x = Mma<T>::pack(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
+                        v.y = Mma<T>::pack(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
+                        v.z = Mma<T>::pack(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
+                        v.w = Mma<T>::pack(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + c0 + i) = v;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            atomicOr(p.status, kWaitTimeout);
+        }
+    }
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    if (warp == 1) tc05::dealloc(tmem, C::kTmemCols);
+}
+
+template <typename T, int D>
+inline cudaError_t launch_prefill_tc_d(const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                       const CUtensorMap &tmV, const PrefillParams &p, dim3 grid,
+                                       cudaStream_t st) {
+    using C = PrefillTcCfg<D>;
+    static std::atomic<int> done[kMaxDevices];
+    auto k = pa_prefill_tc_kernel<T, D>;
+    cudaError_t e = ensure_smem(k, C::kLaunchBytes, done);
+    if (e != cudaSuccess) return e;
+    k<<<grid, C::kThreads, C::kLaunchBytes, st>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prefill_tc(int D, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                              const CUtensorMap &tmV, const PrefillParams &p, dim3 grid,
+                              cudaStream_t st) {
+    if (D == 64) return launch_prefill_tc_d<T, 64>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 128) return launch_prefill_tc_d<T, 128>(tmQ, tmK, tmV, p, grid, st);
+    if (D == 256) return launch_prefill_tc_d<T, 256>(tmQ, tmK, tmV, p, grid, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,6 +1,6 @@
 """Prefix prefill (``pa_prefill``) against the fp64 oracle, element by element.
 
-Sweeps head_dim, GQA group (1 to 128 query heads per KV head, so 128 down to 1
+Sweeps head_dim (64, 128, 256), GQA group (1 to 128 query heads per KV head, so 128 down to 1
 chunk tokens per CTA), block size, dtype and ragged shapes: no prefix (pure
 causal), one-row chunks, chunks spanning several CTAs with a partial last
 one, empty chunks, contexts that end inside a 32-token stage.  Larger chunks
@@ -27,6 +27,8 @@ SHAPES = [
     ([15, 1, 40], [0, 50, 7], 12, 6, 128, 16, torch.bfloat16),
     ([100], [10], 128, 1, 64, 16, torch.bfloat16),
     ([3000, 47], [1, 1], 24, 8, 128, 16, torch.float16),
+    ([0, 300], [100, 45], 16, 2, 256, 16, torch.bfloat16),
+    ([129, 64], [64, 1], 8, 8, 256, 32, torch.float16),
 ]
 IDS = [f"d{s[4]}_g{s[2] // s[3]}_bs{s[5]}_{str(s[6])[6:]}" for s in SHAPES]
 
