@@ -7,8 +7,10 @@ this module only compiles it with the host C compiler and marshals arrays.
 
 What each function computes, and the passage it follows, is stated in
 ``pa_oracle.c`` (page: project_6 commit cd0d9e1, "qwen3_6_scripts": the
-forward_decode heuristic, phases 1 and 2 of the V2 description, and the
-pre-gather of context K/V through the block table).
+forward_decode heuristic, phases 1 and 2 of the V2 description, the
+pre-gather of context K/V through the block table, the prefix prefill, and
+the MoE sort-by-expert regrouping; page: commit 490ff98, "Dockerfile": the
+topk_softmax router).
 
 Arrays are numpy arrays or CPU torch tensors.  16-bit floating-point inputs
 (query, key/value caches) are passed as their bit patterns; the oracle widens
@@ -75,6 +77,14 @@ def _load():
             lib.oracle_prefill.restype = _int
             lib.oracle_prefill.argtypes = [_dp, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p] + \
                 [_int] * 7 + [ctypes.c_float, _int]
+            lib.oracle_topk_softmax.restype = _int
+            lib.oracle_topk_softmax.argtypes = [_dp, _i32p, _dp] + [_int] * 4
+            lib.oracle_moe_sort.restype = _int
+            lib.oracle_moe_sort.argtypes = [_i32p, _i32p, _i32p, _i32p, _int, _int]
+            lib.oracle_moe_gather.restype = _int
+            lib.oracle_moe_gather.argtypes = [_u16p, _u16p, _i32p] + [_int] * 4
+            lib.oracle_moe_scatter.restype = _int
+            lib.oracle_moe_scatter.argtypes = [_dp, _u16p, _i32p, _dp] + [_int] * 5
             lib.oracle_gather.restype = _int
             lib.oracle_gather.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, _i32p] + \
                 [_int] * 7
@@ -255,3 +265,70 @@ def gather(key_cache, value_cache, block_tables, seq_lens, max_len=None):
         S, Hkv, d, bs, nb, mb, int(max_len))
     _check(rc, "gather")
     return kd, vd
+
+
+def _logits_f64(logits) -> np.ndarray:
+    """Router logits (fp32, or 16-bit float bit patterns via their dtype) as exact fp64."""
+    if isinstance(logits, np.ndarray) and logits.dtype in (np.float32, np.float64):
+        return np.ascontiguousarray(logits, dtype=np.float64)
+    import torch
+    t = logits if isinstance(logits, torch.Tensor) else torch.as_tensor(logits)
+    t = t.detach().cpu()
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return bits_to_f64(t)
+    return np.ascontiguousarray(t.to(torch.float64).numpy())
+
+
+def topk_softmax(logits, k: int, renormalize: bool = False):
+    """Router (see ``oracle_topk_softmax``): returns (weights fp64 [T,k], ids int32 [T,k])."""
+    x = _logits_f64(logits)
+    T, E = x.shape
+    w = np.empty((T, k), dtype=np.float64)
+    ids = np.empty((T, k), dtype=np.int32)
+    rc = _load().oracle_topk_softmax(_ptr(w, ctypes.c_double), _ptr(ids, ctypes.c_int32),
+                                     _ptr(x, ctypes.c_double), T, E, int(k), int(bool(renormalize)))
+    _check(rc, "topk_softmax")
+    return w, ids
+
+
+def moe_sort(expert_ids, num_experts: int):
+    """Stable sort of the flat pairs by expert (see ``oracle_moe_sort``):
+    returns (sorted_pairs [P], offsets [E+1], pair_pos [P]), all int32."""
+    ids = _i32(expert_ids).reshape(-1)
+    P = ids.shape[0]
+    sp = np.empty(P, dtype=np.int32)
+    off = np.empty(num_experts + 1, dtype=np.int32)
+    pos = np.empty(P, dtype=np.int32)
+    rc = _load().oracle_moe_sort(_ptr(sp, ctypes.c_int32), _ptr(off, ctypes.c_int32),
+                                 _ptr(pos, ctypes.c_int32), _ptr(ids, ctypes.c_int32), P,
+                                 int(num_experts))
+    _check(rc, "moe_sort")
+    return sp, off, pos
+
+
+def moe_gather(hidden, sorted_pairs, k: int) -> np.ndarray:
+    """Rows of ``hidden`` [T,H] in sorted-pair order, as 16-bit bit patterns [P,H]."""
+    h = _bits(hidden)
+    T, H = h.shape
+    sp = _i32(sorted_pairs).reshape(-1)
+    out = np.empty((sp.shape[0], H), dtype=np.uint16)
+    rc = _load().oracle_moe_gather(_ptr(out, ctypes.c_uint16), _ptr(h, ctypes.c_uint16),
+                                   _ptr(sp, ctypes.c_int32), sp.shape[0], int(k), T, H)
+    _check(rc, "moe_gather")
+    return out
+
+
+def moe_scatter(y, pair_pos, weights, k: int, dtype=None) -> np.ndarray:
+    """Scatter-back (see ``oracle_moe_scatter``): fp64 [T,H] from per-pair rows ``y`` [P,H]."""
+    code = _dtype_code(y, dtype)
+    yb = _bits(y)
+    P, H = yb.shape
+    pos = _i32(pair_pos).reshape(-1)
+    w = np.ascontiguousarray(np.asarray(weights, dtype=np.float64).reshape(-1))
+    T = P // int(k)
+    out = np.empty((T, H), dtype=np.float64)
+    rc = _load().oracle_moe_scatter(_ptr(out, ctypes.c_double), _ptr(yb, ctypes.c_uint16),
+                                    _ptr(pos, ctypes.c_int32), _ptr(w, ctypes.c_double), T,
+                                    int(k), P, H, code)
+    _check(rc, "moe_scatter")
+    return out

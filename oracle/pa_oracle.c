@@ -421,3 +421,125 @@ int oracle_gather(uint16_t *k_dense, uint16_t *v_dense, const uint16_t *kc,
     }
     return ORACLE_OK;
 }
+
+/*
+ * MoE routing and token regrouping (page: project_6 commit cd0d9e1,
+ * "qwen3_6_scripts", the MoE prefill rewrite: 256 experts x top_k = 8; flatten
+ * the T x K token-expert pairs, sort them by expert id so that each expert's
+ * tokens are contiguous, gather the hidden rows in that order, and scatter the
+ * per-pair expert outputs back with index_add_; page: commit 490ff98,
+ * "Dockerfile", the _moe_C topk_softmax router kernel).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   [router]  p = softmax over all E experts of the token's logits; the k
+ *             experts with the largest logits are chosen (softmax is
+ *             monotonic, so these are the k largest p), ties going to the
+ *             lower expert index, in descending order; the weights are their
+ *             p, divided by the sum of the k chosen p when `renormalize`.
+ *   [sort]    the sort is stable: within one expert, pairs keep the order of
+ *             their flat index t*K + k.
+ *   [scatter] index_add_ accumulates w[t][k] * y[pair] into token t's row: the
+ *             routing weight is applied in the scatter-back.
+ */
+
+/* [router] weights [T][k] (fp64), ids [T][k]; logits [T][E] already widened. */
+int oracle_topk_softmax(double *weights, int32_t *ids, const double *logits, int T, int E,
+                        int k, int renormalize)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E)
+        return ORACLE_BAD_ARGS;
+    char *taken = (char *)malloc((size_t)E);
+    if (!taken)
+        return ORACLE_NO_MEMORY;
+    for (int t = 0; t < T; ++t) {
+        const double *x = logits + (int64_t)t * E;
+        double m = -INFINITY;
+        for (int e = 0; e < E; ++e)
+            if (x[e] > m)
+                m = x[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e)
+            z += exp(x[e] - m);
+        memset(taken, 0, (size_t)E);
+        double sel = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || x[e] > x[best]))
+                    best = e;
+            taken[best] = 1;
+            ids[(int64_t)t * k + j] = best;
+            weights[(int64_t)t * k + j] = exp(x[best] - m) / z;
+            sel += weights[(int64_t)t * k + j];
+        }
+        if (renormalize)
+            for (int j = 0; j < k; ++j)
+                weights[(int64_t)t * k + j] /= sel;
+    }
+    free(taken);
+    return ORACLE_OK;
+}
+
+/* [sort] sorted_pairs [P]: the flat pair indices in expert order (stable);
+ * offsets [E+1]: first sorted position of each expert, offsets[E] = P;
+ * pair_pos [P]: sorted position of each pair (the inverse permutation). */
+int oracle_moe_sort(int32_t *sorted_pairs, int32_t *offsets, int32_t *pair_pos,
+                    const int32_t *expert_ids, int P, int E)
+{
+    if (P < 0 || E <= 0)
+        return ORACLE_BAD_ARGS;
+    for (int p = 0; p < P; ++p)
+        if (expert_ids[p] < 0 || expert_ids[p] >= E)
+            return ORACLE_BAD_TABLE;
+    int r = 0;
+    for (int e = 0; e < E; ++e) {
+        offsets[e] = r;
+        for (int p = 0; p < P; ++p)
+            if (expert_ids[p] == e) {
+                sorted_pairs[r] = p;
+                pair_pos[p] = r;
+                ++r;
+            }
+    }
+    offsets[E] = r;
+    return ORACLE_OK;
+}
+
+/* [gather] out [P][H]: row r is hidden row sorted_pairs[r] / K (bit copy). */
+int oracle_moe_gather(uint16_t *out, const uint16_t *hidden, const int32_t *sorted_pairs,
+                      int P, int K, int T, int H)
+{
+    if (P < 0 || K <= 0 || T < 0 || H <= 0)
+        return ORACLE_BAD_ARGS;
+    for (int r = 0; r < P; ++r) {
+        int t = sorted_pairs[r] / K;
+        if (sorted_pairs[r] < 0 || t >= T)
+            return ORACLE_BAD_TABLE;
+        memcpy(out + (int64_t)r * H, hidden + (int64_t)t * H, (size_t)H * sizeof(uint16_t));
+    }
+    return ORACLE_OK;
+}
+
+/* [scatter] out [T][H] (fp64) = sum_k weights[t][k] * y[pair_pos[t*K + k]];
+ * y [P][H] holds the per-pair rows in sorted order (16-bit bit patterns). */
+int oracle_moe_scatter(double *out, const uint16_t *y, const int32_t *pair_pos,
+                       const double *weights, int T, int K, int P, int H, int dtype)
+{
+    if (T < 0 || K <= 0 || P != T * K || H <= 0)
+        return ORACLE_BAD_ARGS;
+    for (int t = 0; t < T; ++t) {
+        double *o = out + (int64_t)t * H;
+        for (int i = 0; i < H; ++i)
+            o[i] = 0.0;
+        for (int k = 0; k < K; ++k) {
+            int r = pair_pos[(int64_t)t * K + k];
+            if (r < 0 || r >= P)
+                return ORACLE_BAD_TABLE;
+            double w = weights[(int64_t)t * K + k];
+            const uint16_t *row = y + (int64_t)r * H;
+            for (int i = 0; i < H; ++i)
+                o[i] += w * oracle_half_bits_to_f64(row[i], dtype);
+        }
+    }
+    return ORACLE_OK;
+}

@@ -13,7 +13,12 @@ oracle disagrees with what the mathematics or a library routine fixes:
 * invariants (permuting physical blocks; partitioned + log-sum-exp merge equals
   single pass for any partition size; untouched unused partition slots);
 * per-partition statistics against ``torch.max`` / ``torch.logsumexp`` of
-  logits from a library matmul.
+  logits from a library matmul;
+* the MoE router and regrouping: closed forms (equal logits, logits ln(e+1)),
+  brute force over all k-subsets of a tiny router, torch.softmax / torch.topk,
+  a hand-worked sort, numpy's stable argsort, and the identity expert (the
+  scatter-back of the gathered rows with weights summing to one returns the
+  hidden states).
 """
 from __future__ import annotations
 
@@ -311,7 +316,128 @@ def pin_prefill_single_row_is_decode(orc):
     assert np.abs(a - b).max() <= TOL
 
 
+
+# --------------------------------------------------------------------------
+# MoE router (topk_softmax) and the sort-by-expert regrouping
+# --------------------------------------------------------------------------
+
+def pin_topk_equal_logits(o):
+    """All logits equal: every p is 1/E, ties go to the lowest expert ids."""
+    for E, k in [(256, 8), (7, 3)]:
+        x = np.full((3, E), 0.25, dtype=np.float32)
+        w, ids = o.topk_softmax(x, k)
+        assert (ids == np.arange(k, dtype=np.int32)[None, :]).all(), ids
+        assert np.abs(w - 1.0 / E).max() < TOL
+        w2, _ = o.topk_softmax(x, k, renormalize=True)
+        assert np.abs(w2 - 1.0 / k).max() < TOL
+
+
+def pin_topk_log_integers(o):
+    """logit_e = ln(e + 1): p_e = (e + 1) / (E (E + 1) / 2) in closed form, and the
+    top-k are the last k experts in descending order."""
+    E, k = 256, 8
+    x = np.log(np.arange(1, E + 1, dtype=np.float64))[None, :].repeat(2, axis=0)
+    w, ids = o.topk_softmax(x, k)
+    want_ids = np.arange(E - 1, E - 1 - k, -1)
+    assert (ids == want_ids[None, :]).all(), ids
+    want_w = (want_ids + 1) / (E * (E + 1) / 2)
+    assert np.abs(w - want_w[None, :]).max() < 1e-12
+    w2, _ = o.topk_softmax(x, k, renormalize=True)
+    assert np.abs(w2 - (want_ids + 1) / (want_ids + 1).sum()).max() < 1e-12
+
+
+def pin_topk_brute_force(o):
+    """Distinct random logits on a tiny router: the chosen set is the k-subset
+    with the largest probability mass (itertools over all subsets), ordered by
+    descending logit; weights from math.exp."""
+    import itertools
+    rng = np.random.default_rng(7)
+    E, k = 7, 3
+    x = rng.standard_normal((5, E)).astype(np.float32)
+    w, ids = o.topk_softmax(x, k)
+    for t in range(x.shape[0]):
+        xs = [float(v) for v in x[t]]
+        z = sum(math.exp(v) for v in xs)
+        best = max(itertools.combinations(range(E), k), key=lambda c: sum(math.exp(xs[i]) for i in c))
+        order = sorted(best, key=lambda i: -xs[i])
+        assert list(ids[t]) == order, (ids[t], order)
+        assert max(abs(w[t, j] - math.exp(xs[order[j]]) / z) for j in range(k)) < 1e-12
+
+
+def pin_topk_large_logits_and_library(o):
+    """Logits near 800 (exp overflows fp64 without the max shift) and a check
+    against torch.softmax / torch.topk in fp64 on distinct bf16 logits."""
+    x = np.array([[800.0, 799.0, 790.0, 0.0]], dtype=np.float32)
+    w, ids = o.topk_softmax(x, 2)
+    z = 1 + math.exp(-1) + math.exp(-10) + math.exp(-800)
+    assert list(ids[0]) == [0, 1]
+    assert abs(w[0, 0] - 1 / z) < 1e-12 and abs(w[0, 1] - math.exp(-1) / z) < 1e-12
+    g = torch.Generator().manual_seed(11)
+    xt = torch.randn((64, 256), generator=g).to(torch.bfloat16)
+    xd = xt.to(torch.float64)
+    distinct = torch.tensor([len(set(r.tolist())) == 256 for r in xd])
+    w, ids = o.topk_softmax(xt, 8)
+    p = torch.softmax(xd, dim=-1)
+    tv, ti = torch.topk(p, 8, dim=-1)
+    assert (torch.from_numpy(ids.astype(np.int64))[distinct] == ti[distinct]).all()
+    assert np.abs(w - tv.numpy()).max() < 1e-12
+
+
+def pin_moe_sort_worked_example(o):
+    """ids [3, 1, 3, 0, 1] over 4 experts, worked by hand: expert 0 holds pair 3,
+    expert 1 pairs 1 and 4, expert 2 none, expert 3 pairs 0 and 2."""
+    sp, off, pos = o.moe_sort(np.array([3, 1, 3, 0, 1], dtype=np.int32), 4)
+    assert list(sp) == [3, 1, 4, 0, 2]
+    assert list(off) == [0, 1, 3, 3, 5]
+    assert list(pos) == [3, 1, 4, 0, 2]
+
+
+def pin_moe_sort_stable_library(o):
+    """Random routing (16 tokens x 8 of 32 experts): numpy's stable argsort,
+    bincount offsets, and the inverse permutation."""
+    rng = np.random.default_rng(3)
+    ids = np.stack([rng.choice(32, 8, replace=False) for _ in range(16)]).astype(np.int32)
+    sp, off, pos = o.moe_sort(ids, 32)
+    flat = ids.reshape(-1)
+    assert (sp == np.argsort(flat, kind="stable")).all()
+    assert (off == np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=32))])).all()
+    assert (pos[sp] == np.arange(flat.size)).all()
+
+
+def pin_moe_gather_and_identity_scatter(o):
+    """Gather puts hidden row p // K at sorted position pos[p]; scattering the
+    gathered rows back with weights that sum to one per token returns the
+    hidden states (an identity expert); a hand-worked K = 2 case checks the
+    weighting."""
+    rng = np.random.default_rng(5)
+    T, K, E, H = 6, 3, 8, 16
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    hidden = torch.randn((T, H), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    sp, off, pos = o.moe_sort(ids, E)
+    y = o.moe_gather(hidden, sp, K)
+    hb = hidden.view(torch.int16).numpy().view(np.uint16)
+    for p in range(T * K):
+        assert (y[pos[p]] == hb[p // K]).all()
+    w = rng.random((T, K))
+    w /= w.sum(axis=1, keepdims=True)
+    out = o.moe_scatter(torch.from_numpy(y.view(np.int16)).view(torch.bfloat16), pos, w, K)
+    assert np.abs(out - hidden.to(torch.float64).numpy()).max() < 1e-12
+    # K = 2, two tokens, rows [1, 2] and [3, 4] per pair: out = w0 y0 + w1 y1
+    y2 = torch.tensor([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0], [7.0, 8.0]], dtype=torch.float16)
+    pos2 = np.array([2, 0, 3, 1], dtype=np.int32)   # token 0 -> rows 2, 0; token 1 -> rows 3, 1
+    w2 = np.array([[0.5, 0.25], [1.0, -1.0]])
+    out2 = o.moe_scatter(y2, pos2, w2, 2)
+    assert np.abs(out2 - np.array([[2.75, 3.5], [4.0, 4.0]])).max() < TOL
+
+
 ALL_PINS = [
+    pin_topk_equal_logits,
+    pin_topk_log_integers,
+    pin_topk_brute_force,
+    pin_topk_large_logits_and_library,
+    pin_moe_sort_worked_example,
+    pin_moe_sort_stable_library,
+    pin_moe_gather_and_identity_scatter,
     pin_prefill_dense_sdpa,
     pin_prefill_no_prefix_is_causal,
     pin_prefill_zero_query_prefix_means,

@@ -42,6 +42,20 @@ MUTANTS = {
     "prefill_prefix_ignored": ("int p = L - n + (int)(r - q_start[s]);",
                                "int p = (int)(r - q_start[s]);"),
     "prefill_wrong_query_row": ("q + (r * Hq + h) * d", "q + ((int64_t)s * Hq + h) * d"),
+    "topk_tie_goes_to_higher_index": ("(best < 0 || x[e] > x[best])",
+                                      "(best < 0 || x[e] >= x[best])"),
+    "topk_max_not_subtracted": ("if (x[e] > m)\n                m = x[e];",
+                                "if (x[e] > m)\n                m = 0.0;"),
+    "topk_renormalize_skipped": ("weights[(int64_t)t * k + j] /= sel;",
+                                 "weights[(int64_t)t * k + j] /= 1.0;"),
+    "sort_not_stable": ("for (int p = 0; p < P; ++p)\n            if (expert_ids[p] == e)",
+                        "for (int p = P - 1; p >= 0; --p)\n            if (expert_ids[p] == e)"),
+    "sort_offset_off_by_one": ("offsets[e] = r;", "offsets[e] = r + 1;"),
+    "gather_pair_index_as_token": ("int t = sorted_pairs[r] / K;", "int t = sorted_pairs[r] % K;"),
+    "scatter_weight_dropped": ("o[i] += w * oracle_half_bits_to_f64(row[i], dtype);",
+                               "o[i] += oracle_half_bits_to_f64(row[i], dtype);"),
+    "scatter_pair_index_not_position": ("int r = pair_pos[(int64_t)t * K + k];",
+                                        "int r = (int)((int64_t)t * K + k);"),
 }
 
 
