@@ -25,7 +25,8 @@ __all__ = [
     "partition_reduce", "decode_auto", "auto_workspace_bytes", "default_single_pass_max_len",
     "prefill", "gather_kv", "device_status", "num_partitions", "version",
     "DEV_BAD_BLOCK", "DEV_LEN_CLAMPED", "DEV_WAIT_TIMEOUT", "DEV_TOO_MANY_PARTITIONS",
-    "DEV_BAD_ROWS",
+    "DEV_BAD_ROWS", "DEV_BAD_EXPERT", "topk_softmax", "moe_sort", "moe_gather",
+    "moe_scatter_back", "moe_sort_workspace_bytes",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +36,8 @@ PA_F16, PA_BF16 = 0, 1
 PHASE_PLAN, PHASE_ATTEND, PHASE_REDUCE = 1, 2, 4
 DEV_BAD_BLOCK, DEV_LEN_CLAMPED, DEV_WAIT_TIMEOUT, DEV_TOO_MANY_PARTITIONS = 1, 2, 4, 8
 DEV_BAD_ROWS = 16
+DEV_BAD_EXPERT = 32
+LOGITS_F16, LOGITS_BF16, LOGITS_F32 = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -43,7 +46,7 @@ _vp = ctypes.c_void_p
 _i = ctypes.c_int
 _f = ctypes.c_float
 
-# (name, restype, argtypes) of every entry point in include/pa_decode.h
+# (name, restype, argtypes) of every entry point in include/pa_decode.h and include/pa_moe.h
 SIGNATURES = [
     ("pa_decode", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _vp]),
     ("pa_decode_partitioned", _i, [_vp] * 8 + [_i] * 7 + [_f, _i, _i, _i, _vp]),
@@ -57,6 +60,11 @@ SIGNATURES = [
     ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _i, _vp]),
     ("pa_prefill", _i, [_vp] * 7 + [_i] * 9 + [_f, _i, _vp]),
     ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
+    ("pa_topk_softmax", _i, [_vp] * 3 + [_i] * 5 + [_vp]),
+    ("pa_moe_sort_workspace_bytes", ctypes.c_size_t, [_i, _i]),
+    ("pa_moe_sort", _i, [_vp] * 4 + [_i, _i, _vp, ctypes.c_size_t, _vp]),
+    ("pa_moe_gather", _i, [_vp] * 3 + [_i] * 5 + [_vp]),
+    ("pa_moe_scatter_back", _i, [_vp] * 4 + [_i] * 4 + [_vp]),
     ("pa_selftest_wait_timeout", _i, [_vp, _i]),
     ("pa_device_status", _i, [_vp, ctypes.POINTER(_i)]),
     ("pa_status_string", ctypes.c_char_p, [_i]),
@@ -304,6 +312,86 @@ def prefill(query, key_cache, value_cache, block_tables, seq_lens, q_start, scal
             _i32(seq_lens, "seq_lens"), _i32(q_start, "q_start"), S, R, int(max_q_len), Hq,
             Hkv, D, bs, nb, mb, float(scale), _dtype_code(query), _stream(query))
     _check(st, "pa_prefill")
+    return out
+
+
+def topk_softmax(gating_logits, topk: int, renormalize: bool = False,
+                 weights: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None):
+    """MoE router (``pa_topk_softmax``): returns (weights fp32 [T,k], ids int32 [T,k])."""
+    T, E = gating_logits.shape
+    code = {torch.float16: LOGITS_F16, torch.bfloat16: LOGITS_BF16,
+            torch.float32: LOGITS_F32}.get(gating_logits.dtype)
+    if code is None:
+        raise TypeError("router logits must be float16, bfloat16 or float32")
+    dev = gating_logits.device
+    if weights is None:
+        weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().pa_topk_softmax(_f32(weights, "weights"), _i32(ids, "ids"),
+                                     _dev(gating_logits, "gating_logits"), T, E, int(topk),
+                                     int(bool(renormalize)), code, _stream(gating_logits))
+    _check(st, "pa_topk_softmax")
+    return weights, ids
+
+
+def moe_sort_workspace_bytes(num_pairs: int, num_experts: int) -> int:
+    return int(_load().pa_moe_sort_workspace_bytes(int(num_pairs), int(num_experts)))
+
+
+def moe_sort(expert_ids, num_experts: int, workspace: Optional[torch.Tensor] = None, out=None):
+    """Stable sort of the flat pairs by expert (``pa_moe_sort``): returns
+    (sorted_pairs [P], expert_offsets [E+1], pair_pos [P]), int32."""
+    flat = expert_ids.reshape(-1)
+    P = flat.numel()
+    dev = expert_ids.device
+    if out is None:
+        out = (torch.empty(P, dtype=torch.int32, device=dev),
+               torch.empty(num_experts + 1, dtype=torch.int32, device=dev),
+               torch.empty(P, dtype=torch.int32, device=dev))
+    sp, off, pos = out
+    need = moe_sort_workspace_bytes(P, num_experts)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().pa_moe_sort(_i32(sp, "sorted_pairs"), _i32(off, "expert_offsets"),
+                                 _i32(pos, "pair_pos"), _i32(flat, "expert_ids"), P,
+                                 int(num_experts), _dev(workspace, "workspace"),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream(expert_ids))
+    _check(st, "pa_moe_sort")
+    return sp, off, pos
+
+
+def moe_gather(hidden, sorted_pairs, topk: int, out: Optional[torch.Tensor] = None):
+    """Hidden rows in expert-sorted pair order (``pa_moe_gather``): [P, H]."""
+    T, H = hidden.shape
+    P = sorted_pairs.numel()
+    if out is None:
+        out = torch.empty((P, H), dtype=hidden.dtype, device=hidden.device)
+    with torch.cuda.device(hidden.device):
+        st = _load().pa_moe_gather(_dev(out, "sorted_hidden"), _dev(hidden, "hidden"),
+                                   _i32(sorted_pairs, "sorted_pairs"), P, int(topk), T, H,
+                                   _dtype_code(hidden), _stream(hidden))
+    _check(st, "pa_moe_gather")
+    return out
+
+
+def moe_scatter_back(expert_out, pair_pos, topk_weights, out: Optional[torch.Tensor] = None):
+    """Weighted scatter-back of the per-pair rows (``pa_moe_scatter_back``): [T, H]."""
+    P, H = expert_out.shape
+    T, K = topk_weights.shape
+    if P != T * K:
+        raise ValueError("expert_out must have num_tokens * topk rows")
+    if out is None:
+        out = torch.empty((T, H), dtype=expert_out.dtype, device=expert_out.device)
+    with torch.cuda.device(expert_out.device):
+        st = _load().pa_moe_scatter_back(_dev(out, "out"), _dev(expert_out, "expert_out"),
+                                         _i32(pair_pos, "pair_pos"),
+                                         _f32(topk_weights, "topk_weights"), T, K, H,
+                                         _dtype_code(expert_out), _stream(expert_out))
+    _check(st, "pa_moe_scatter_back")
     return out
 
 

@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libpadecode.so")
 
 SOURCES = ["pa_api.cu", "pa_aux.cu", "pa_inst_bf16.cu", "pa_inst_f16.cu", "pa_prefill.cu",
-           "pa_static.cu"]
+           "pa_moe.cu", "pa_static.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 
@@ -36,7 +36,7 @@ def _nvcc() -> str:
 def _inputs() -> list:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
              if f.endswith((".cu", ".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "pa_decode.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -12,6 +12,7 @@
 
 #include "pa_decode.h"
 #include "pa_launch.h"
+#include "pa_moe.h"
 
 #ifndef PA_TILE_PIECES
 #define PA_TILE_PIECES 1
@@ -642,6 +643,136 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
         dtype == PA_BF16 ? launch_prefill_tc<__nv_bfloat16>(head_dim, tq, tk, tv, p, grid, st)
                          : launch_prefill_tc<__half>(head_dim, tq, tk, tv, p, grid, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_topk_softmax(float *topk_weights, int32_t *topk_ids, const void *gating_logits,
+                    int num_tokens, int num_experts, int topk, int renormalize,
+                    pa_logits_t logits_dtype, void *stream) {
+    if (num_tokens < 0 || topk <= 0) return PA_ERR_INVALID_ARGUMENT;
+    if (logits_dtype != PA_LOGITS_F16 && logits_dtype != PA_LOGITS_BF16 &&
+        logits_dtype != PA_LOGITS_F32)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (num_experts != 32 && num_experts != 64 && num_experts != 128 && num_experts != 256 &&
+        num_experts != 512)
+        return PA_ERR_UNSUPPORTED;
+    if (topk > 32 || topk > num_experts) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!topk_weights || !topk_ids || !gating_logits) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(gating_logits, 16) || !aligned(topk_weights, 4) || !aligned(topk_ids, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    TopkParams p{};
+    p.logits = gating_logits;
+    p.weights = topk_weights;
+    p.ids = topk_ids;
+    p.num_tokens = num_tokens;
+    p.topk = topk;
+    p.renormalize = renormalize != 0;
+    return launch_topk_softmax(static_cast<int>(logits_dtype), num_experts, p,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+size_t pa_moe_sort_workspace_bytes(int num_pairs, int num_experts) {
+    if (num_pairs < 0 || num_experts <= 0 || num_experts > 1024) return 0;
+    return align256(static_cast<size_t>(moe_sort_chunks(num_pairs)) * num_experts *
+                    sizeof(int32_t)) + 256;
+}
+
+int pa_moe_sort(int32_t *sorted_pairs, int32_t *expert_offsets, int32_t *pair_pos,
+                const int32_t *expert_ids, int num_pairs, int num_experts, void *workspace,
+                size_t workspace_bytes, void *stream) {
+    if (num_pairs < 0 || num_experts <= 0) return PA_ERR_INVALID_ARGUMENT;
+    if (num_experts > 1024) return PA_ERR_UNSUPPORTED;
+    if (!expert_offsets) return PA_ERR_INVALID_ARGUMENT;
+    if (num_pairs > 0 && (!sorted_pairs || !pair_pos || !expert_ids))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(sorted_pairs, 4) || !aligned(expert_offsets, 4) || !aligned(pair_pos, 4) ||
+        !aligned(expert_ids, 4))
+        return PA_ERR_MISALIGNED;
+    if (!workspace) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256)) return PA_ERR_MISALIGNED;
+    if (workspace_bytes < pa_moe_sort_workspace_bytes(num_pairs, num_experts))
+        return PA_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    SortParams p{};
+    p.expert_ids = expert_ids;
+    p.sorted_pairs = sorted_pairs;
+    p.offsets = expert_offsets;
+    p.pair_pos = pair_pos;
+    p.hist = static_cast<int32_t *>(workspace);
+    p.status = di->status;
+    p.num_pairs = num_pairs;
+    p.num_experts = num_experts;
+    p.num_chunks = moe_sort_chunks(num_pairs);
+    if (num_pairs == 0) {   // offsets are all zero: the scan alone writes them
+        p.num_chunks = 0;
+    }
+    return launch_moe_sort(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                : PA_ERR_CUDA;
+}
+
+int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *sorted_pairs,
+                  int num_pairs, int topk, int num_tokens, int hidden_size, pa_dtype_t dtype,
+                  void *stream) {
+    if (num_pairs < 0 || topk <= 0 || num_tokens < 0 || hidden_size <= 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
+    if ((hidden_size * 2) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!sorted_hidden || !hidden || !sorted_pairs) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(sorted_hidden, 16) || !aligned(hidden, 16) || !aligned(sorted_pairs, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    MoeGatherParams p{};
+    p.out = sorted_hidden;
+    p.hidden = hidden;
+    p.sorted_pairs = sorted_pairs;
+    p.status = di->status;
+    p.num_pairs = num_pairs;
+    p.topk = topk;
+    p.num_tokens = num_tokens;
+    p.row_bytes = hidden_size * 2;
+    return launch_moe_gather(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                  : PA_ERR_CUDA;
+}
+
+int pa_moe_scatter_back(void *out, const void *expert_out, const int32_t *pair_pos,
+                        const float *topk_weights, int num_tokens, int topk, int hidden_size,
+                        pa_dtype_t dtype, void *stream) {
+    if (num_tokens < 0 || topk <= 0 || hidden_size <= 0) return PA_ERR_INVALID_ARGUMENT;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
+    if (topk > 32 || hidden_size % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_tokens) * topk > INT_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!out || !expert_out || !pair_pos || !topk_weights) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(out, 16) || !aligned(expert_out, 16) || !aligned(pair_pos, 4) ||
+        !aligned(topk_weights, 4))
+        return PA_ERR_MISALIGNED;
+    DevInfo *di = nullptr;
+    const int rc = device_info(&di);
+    if (rc != PA_OK) return rc;
+    MoeScatterParams p{};
+    p.out = out;
+    p.y = expert_out;
+    p.pair_pos = pair_pos;
+    p.weights = topk_weights;
+    p.status = di->status;
+    p.num_tokens = num_tokens;
+    p.topk = topk;
+    p.num_pairs = num_tokens * topk;
+    p.hidden_size = hidden_size;
+    return launch_moe_scatter(dtype == PA_BF16, p, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 int pa_selftest_wait_timeout(void *stream, int limit_us) {

@@ -1,7 +1,8 @@
 // pa_launch.h -- declarations of the kernel launchers.  The attention and
 // reduce launchers are templates explicitly instantiated per dtype in
 // pa_inst_bf16.cu / pa_inst_f16.cu, the prefill launcher in pa_prefill.cu;
-// the planner and gather launchers live in pa_aux.cu.
+// the planner and gather launchers live in pa_aux.cu, the MoE router and
+// regrouping launchers in pa_moe.cu.
 #pragma once
 
 #include <cuda.h>
@@ -28,5 +29,12 @@ cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_gather(int D, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const GatherParams &gp, dim3 grid, cudaStream_t st);
+
+cudaError_t launch_topk_softmax(int logits_type, int num_experts, const TopkParams &p,
+                                cudaStream_t st);
+int moe_sort_chunks(int num_pairs);
+cudaError_t launch_moe_sort(const SortParams &p, cudaStream_t st);
+cudaError_t launch_moe_gather(const MoeGatherParams &p, cudaStream_t st);
+cudaError_t launch_moe_scatter(bool bf16, const MoeScatterParams &p, cudaStream_t st);
 
 }  // namespace pa

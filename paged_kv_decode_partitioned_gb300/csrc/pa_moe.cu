@@ -1,0 +1,429 @@
+// pa_moe.cu -- MoE router and token regrouping kernels for GB300 (sm_103a).
+//
+// The operations (page: project_6 commit cd0d9e1, "qwen3_6_scripts", the MoE
+// prefill rewrite: 256 experts x top_k = 8, flatten the T x K token-expert
+// pairs, sort them by expert so each expert's tokens are contiguous, gather
+// the hidden rows in that order, scatter the expert outputs back with
+// index_add_; page: commit 490ff98, "Dockerfile": the topk_softmax router
+// kernel, which the pages rebuilt for a 64-wide warp):
+//   * topk_softmax: one 32-lane warp per token; each lane holds E/32
+//     consecutive logits in fp32 registers (a 16-byte load per lane for bf16
+//     at E = 256).  The softmax max and sum are warp reductions; the top-k
+//     are chosen on the logits themselves (softmax is monotonic), k rounds of
+//     a warp arg-max with ties to the lower expert id, so the chosen ids are
+//     exact whatever the rounding of the probabilities.
+//   * sort: a stable counting sort in three launches -- per-chunk expert
+//     histograms, one CTA turning them into each chunk's first position per
+//     expert, and a scatter in which each warp walks its share of the chunk in
+//     order, ranking equal experts inside a 32-pair step with __match_any_sync.
+//   * gather: one warp per sorted row, 16-byte loads, streaming stores (the
+//     regrouped rows are written once; the hidden rows, read K times, stay in
+//     L2).
+//   * scatter-back: index_add_ written as a gather-reduce -- one warp per
+//     token sums its K weighted rows in fp32 in slot order and rounds once, so
+//     the result is deterministic and needs no atomics.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <climits>
+
+#include "pa_launch.h"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+// VPL consecutive logits of one lane as fp32 (exact for every input type).
+template <typename TL, int VPL>
+__device__ __forceinline__ void load_logits(const TL *row, int lane, float (&x)[VPL]) {
+    const TL *src = row + lane * VPL;
+    constexpr int kBytes = VPL * static_cast<int>(sizeof(TL));
+    if constexpr (kBytes % 16 == 0) {
+        constexpr int kPer = 16 / static_cast<int>(sizeof(TL));
+#pragma unroll
+        for (int c = 0; c < VPL / kPer; ++c) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+            const TL *e = reinterpret_cast<const TL *>(&v);
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) x[c * kPer + i] = to_f32(e[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) x[i] = to_f32(src[i]);
+    }
+}
+
+}  // namespace
+
+template <typename TL, int VPL>
+__global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= p.num_tokens) return;
+    constexpr int E = VPL * 32;
+    float x[VPL];
+    load_logits<TL, VPL>(static_cast<const TL *>(p.logits) + static_cast<size_t>(t) * E, lane, x);
+    float m = x[0];
+#pragma unroll
+    for (int i = 1; i < VPL; ++i) m = fmaxf(m, x[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) z += expf(x[i] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+
+    uint32_t taken = 0;     // bit i: this lane's expert lane*VPL + i already chosen
+    int my_id = 0;          // lane r keeps the id and logit of choice r
+    float my_x = 0.f;
+    for (int r = 0; r < p.topk; ++r) {
+        float bv = 0.f;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (!(taken >> i & 1u) && (be == INT_MAX || x[i] > bv)) {
+                bv = x[i];
+                be = lane * VPL + i;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be / VPL == lane) taken |= 1u << (be % VPL);
+        if (lane == r) {
+            my_id = be;
+            my_x = bv;
+        }
+    }
+    float w = lane < p.topk ? expf(my_x - m) / z : 0.f;
+    if (p.renormalize) {
+        float s = w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        w = w / s;
+    }
+    if (lane < p.topk) {
+        p.weights[static_cast<size_t>(t) * p.topk + lane] = w;
+        p.ids[static_cast<size_t>(t) * p.topk + lane] = my_id;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stable counting sort of the flat pairs by expert id
+// ---------------------------------------------------------------------------
+constexpr int kSortThreads = 256;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortChunk = 2048;   // pairs per CTA (256 per warp)
+
+// hist[c][e] = pairs of chunk c with expert e
+__global__ void __launch_bounds__(kSortThreads) pa_moe_hist_kernel(const SortParams p) {
+    extern __shared__ int h[];
+    for (int e = threadIdx.x; e < p.num_experts; e += kSortThreads) h[e] = 0;
+    __syncthreads();
+    const int c0 = blockIdx.x * kSortChunk;
+    const int c1 = min(c0 + kSortChunk, p.num_pairs);
+    bool bad = false;
+    for (int i = c0 + threadIdx.x; i < c1; i += kSortThreads) {
+        const int e = __ldg(p.expert_ids + i);
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(p.num_experts))
+            atomicAdd(&h[e], 1);
+        else
+            bad = true;
+    }
+    if (bad) atomicOr(p.status, kBadExpert);
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.num_experts; e += kSortThreads)
+        p.hist[static_cast<size_t>(blockIdx.x) * p.num_experts + e] = h[e];
+}
+
+// One CTA: hist[c][e] becomes the first sorted position of chunk c's pairs of
+// expert e; offsets[e] the first position of expert e, offsets[E] the total.
+__global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
+    __shared__ int warp_sum[32];
+    const int e = threadIdx.x;
+    const int E = p.num_experts;
+    int tot = 0;
+    if (e < E)
+        for (int c = 0; c < p.num_chunks; ++c) tot += p.hist[static_cast<size_t>(c) * E + e];
+    // exclusive scan of tot over the experts (block scan, <= 1024 experts)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int s = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += v;
+        }
+        warp_sum[lane] = s;   // inclusive over warps
+    }
+    __syncthreads();
+    const int start = incl - tot + (warp > 0 ? warp_sum[warp - 1] : 0);
+    if (e < E) {
+        p.offsets[e] = start;
+        int run = start;
+        for (int c = 0; c < p.num_chunks; ++c) {
+            int *hc = p.hist + static_cast<size_t>(c) * E + e;
+            const int n = *hc;
+            *hc = run;
+            run += n;
+        }
+        if (e == E - 1) p.offsets[E] = run;
+    }
+}
+
+// Each warp places its 256 pairs in order: within a 32-pair step, pairs with
+// the same expert are ranked by lane (match_any + popc of the lower lanes).
+__global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortParams p) {
+    extern __shared__ int cnt[];   // [kSortWarps][E]: this warp's next position per expert
+    const int E = p.num_experts;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kSortWarps * E; i += kSortThreads) cnt[i] = 0;
+    __syncthreads();
+    constexpr int kSub = kSortChunk / kSortWarps;
+    const int w0 = blockIdx.x * kSortChunk + warp * kSub;
+    const int w1 = min(w0 + kSub, p.num_pairs);
+    int *mine = cnt + warp * E;
+    for (int i = w0 + lane; i < w1; i += 32) {
+        const int e = __ldg(p.expert_ids + i);
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&mine[e], 1);
+    }
+    __syncthreads();
+    // per-warp counts -> per-warp first positions
+    for (int e = threadIdx.x; e < E; e += kSortThreads) {
+        int run = p.hist[static_cast<size_t>(blockIdx.x) * E + e];
+        for (int w = 0; w < kSortWarps; ++w) {
+            const int n = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += n;
+        }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        int e = i < w1 ? __ldg(p.expert_ids + i) : -1;
+        const bool ok = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+        if (!ok) e = -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        if (ok) {
+            const int pos = mine[e] + __popc(same & lt);
+            p.sorted_pairs[pos] = i;
+            p.pair_pos[i] = pos;
+        } else if (i < w1) {
+            p.pair_pos[i] = -1;
+        }
+        __syncwarp();
+        if (ok && (same & lt) == 0) mine[e] += __popc(same);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Gather and scatter-back
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= p.num_pairs) return;
+    const int pair = __ldg(p.sorted_pairs + r);
+    const int t = pair / p.topk;
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
+                                           static_cast<size_t>(r) * p.row_bytes);
+    const int n16 = p.row_bytes / 16;
+    if (pair < 0 || t >= p.num_tokens) {   // not a valid pair: the row is zeroed
+        if (lane == 0) atomicOr(p.status, kBadExpert);
+        for (int c = lane; c < n16; c += 32) __stcs(dst + c, make_uint4(0, 0, 0, 0));
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.hidden) +
+                                                       static_cast<size_t>(t) * p.row_bytes);
+    int c = lane;
+    for (; c + 96 < n16; c += 128) {   // four 16-byte chunks in flight per lane
+        const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), d = __ldg(src + c + 64),
+                    e = __ldg(src + c + 96);
+        __stcs(dst + c, a);
+        __stcs(dst + c + 32, b);
+        __stcs(dst + c + 64, d);
+        __stcs(dst + c + 96, e);
+    }
+    for (; c < n16; c += 32) __stcs(dst + c, __ldg(src + c));
+}
+
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void unpack(const uint4 &v, float (&f)[8]) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __bfloat1622float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+        uint4 v;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        return v;
+    }
+};
+template <>
+struct Vec8<__half> {
+    static __device__ __forceinline__ void unpack(const uint4 &v, float (&f)[8]) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __half22float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+        uint4 v;
+        __half2 *h = reinterpret_cast<__half2 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        return v;
+    }
+};
+
+// out[t] = sum_k w[t][k] * y[pair_pos[t*K + k]], fp32 in slot order, one rounding.
+template <typename T>
+__global__ void __launch_bounds__(256) pa_moe_scatter_kernel(const MoeScatterParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= p.num_tokens) return;
+    const int K = p.topk;
+    int my_pos = 0;
+    float my_w = 0.f;
+    if (lane < K) {
+        my_pos = __ldg(p.pair_pos + static_cast<size_t>(t) * K + lane);
+        my_w = __ldg(p.weights + static_cast<size_t>(t) * K + lane);
+        if (static_cast<unsigned>(my_pos) >= static_cast<unsigned>(p.num_pairs)) {
+            atomicOr(p.status, kBadExpert);   // a pair that was never placed adds nothing
+            my_pos = -1;
+        }
+    }
+    const int n16 = p.hidden_size / 8;
+    const uint4 *y = static_cast<const uint4 *>(p.y);
+    uint4 *out = static_cast<uint4 *>(p.out) + static_cast<size_t>(t) * n16;
+    // the column loop is uniform over the warp: every lane takes part in the
+    // shuffles that broadcast the K (row, weight) pairs
+    for (int c0 = 0; c0 < n16; c0 += 64) {
+        const int c = c0 + lane;
+        const bool one = c < n16, two = c + 32 < n16;
+        float a0[8], a1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a0[i] = a1[i] = 0.f;
+        for (int k = 0; k < K; ++k) {
+            const int r = __shfl_sync(0xffffffffu, my_pos, k);
+            const float w = __shfl_sync(0xffffffffu, my_w, k);
+            if (r < 0) continue;
+            const uint4 *row = y + static_cast<size_t>(r) * n16;
+            float f[8];
+            if (one) {
+                Vec8<T>::unpack(__ldg(row + c), f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a0[i] = fmaf(w, f[i], a0[i]);
+            }
+            if (two) {
+                Vec8<T>::unpack(__ldg(row + c + 32), f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a1[i] = fmaf(w, f[i], a1[i]);
+            }
+        }
+        if (one) out[c] = Vec8<T>::pack(a0);
+        if (two) out[c + 32] = Vec8<T>::pack(a1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_topk_softmax(int logits_type, int num_experts, const TopkParams &p,
+                                cudaStream_t st) {
+    const dim3 grid((p.num_tokens + 7) / 8);
+#define PA_TOPK(TL, VPL) pa_topk_softmax_kernel<TL, VPL><<<grid, 256, 0, st>>>(p)
+#define PA_TOPK_E(TL)                                  \
+    switch (num_experts) {                             \
+        case 32: PA_TOPK(TL, 1); break;                \
+        case 64: PA_TOPK(TL, 2); break;                \
+        case 128: PA_TOPK(TL, 4); break;               \
+        case 256: PA_TOPK(TL, 8); break;               \
+        case 512: PA_TOPK(TL, 16); break;              \
+        default: return cudaErrorInvalidValue;         \
+    }
+    if (logits_type == 0) {
+        PA_TOPK_E(__half)
+    } else if (logits_type == 1) {
+        PA_TOPK_E(__nv_bfloat16)
+    } else if (logits_type == 2) {
+        PA_TOPK_E(float)
+    } else {
+        return cudaErrorInvalidValue;
+    }
+#undef PA_TOPK_E
+#undef PA_TOPK
+    return cudaGetLastError();
+}
+
+int moe_sort_chunks(int num_pairs) { return (num_pairs + kSortChunk - 1) / kSortChunk; }
+
+cudaError_t launch_moe_sort(const SortParams &p, cudaStream_t st) {
+    const int E = p.num_experts;
+    cudaError_t e;
+    if (p.num_chunks > 0) {
+        pa_moe_hist_kernel<<<p.num_chunks, kSortThreads, E * sizeof(int), st>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    pa_moe_scan_kernel<<<1, 1024, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.num_chunks == 0) return cudaSuccess;
+    const int smem = kSortWarps * E * static_cast<int>(sizeof(int));
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(pa_moe_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem);
+        if (e != cudaSuccess) return e;
+    }
+    pa_moe_place_kernel<<<p.num_chunks, kSortThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_gather(const MoeGatherParams &p, cudaStream_t st) {
+    pa_moe_gather_kernel<<<(p.num_pairs + 7) / 8, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_scatter(bool bf16, const MoeScatterParams &p, cudaStream_t st) {
+    const dim3 grid((p.num_tokens + 7) / 8);
+    if (bf16)
+        pa_moe_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+    else
+        pa_moe_scatter_kernel<__half><<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

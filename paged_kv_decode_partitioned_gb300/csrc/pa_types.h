@@ -15,7 +15,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s
 
 // Flags of the device status word (mirrors PA_DEV_* in pa_decode.h).
-enum : int { kBadBlock = 1, kLenClamped = 2, kWaitTimeout = 4, kTooManyParts = 8, kBadRows = 16 };
+enum : int {
+    kBadBlock = 1, kLenClamped = 2, kWaitTimeout = 4, kTooManyParts = 8, kBadRows = 16,
+    kBadExpert = 32
+};
 
 // Unit kinds.
 enum : int { kOutFinal = 0, kOutPartialDense = 1, kOutPartialCompact = 2 };
@@ -86,6 +89,40 @@ struct GatherParams {
     const int32_t *seq_lens;
     int *status;
     int num_kv_heads, block_size, max_blocks, num_blocks, max_len;
+};
+
+struct TopkParams {
+    const void *logits;         // [T][E] f16 / bf16 / f32
+    float *weights;             // [T][k]
+    int32_t *ids;               // [T][k]
+    int num_tokens, topk, renormalize;
+};
+
+struct SortParams {
+    const int32_t *expert_ids;  // [P] (the router's ids, flattened)
+    int32_t *sorted_pairs;      // [P]
+    int32_t *offsets;           // [E + 1]
+    int32_t *pair_pos;          // [P]
+    int32_t *hist;              // workspace [num_chunks][E]
+    int *status;
+    int num_pairs, num_experts, num_chunks;
+};
+
+struct MoeGatherParams {
+    void *out;                  // [P][row_bytes]
+    const void *hidden;         // [T][row_bytes]
+    const int32_t *sorted_pairs;
+    int *status;
+    int num_pairs, topk, num_tokens, row_bytes;
+};
+
+struct MoeScatterParams {
+    void *out;                  // [T][H]
+    const void *y;              // [P][H], sorted order
+    const int32_t *pair_pos;    // [P]
+    const float *weights;       // [T][K]
+    int *status;
+    int num_tokens, topk, num_pairs, hidden_size;
 };
 
 }  // namespace pa

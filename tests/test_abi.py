@@ -7,7 +7,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pa_decode.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("pa_decode.h", "pa_moe.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,7 +19,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
 
 
@@ -167,3 +167,29 @@ def _prefill(lib, **kw):
 ])
 def test_prefill_rejects_on_host(lib, kw, status):
     assert _prefill(lib, **kw) == status
+
+
+def test_moe_entry_points_reject_on_host(lib):
+    # router: unsupported expert count, topk above 32 or E, bad dtype, misaligned logits
+    assert lib.pa_topk_softmax(A, A, A, 16, 100, 8, 0, 1, None) == -2
+    assert lib.pa_topk_softmax(A, A, A, 16, 256, 33, 0, 1, None) == -2
+    assert lib.pa_topk_softmax(A, A, A, 16, 32, 33, 0, 1, None) == -2
+    assert lib.pa_topk_softmax(A, A, A, 16, 256, 8, 0, 5, None) == -1
+    assert lib.pa_topk_softmax(A, A, A + 4, 16, 256, 8, 0, 1, None) == -3
+    assert lib.pa_topk_softmax(A, A, A, 0, 256, 8, 0, 1, None) == 0
+    # sort: too many experts, missing workspace, workspace too small, misaligned
+    need = lib.pa_moe_sort_workspace_bytes(131072, 256)
+    assert need >= 64 * 256 * 4
+    assert lib.pa_moe_sort_workspace_bytes(10, 2000) == 0
+    assert lib.pa_moe_sort(A, A, A, A, 131072, 2000, A, need, None) == -2
+    assert lib.pa_moe_sort(A, A, A, A, 131072, 256, 0, need, None) == -1
+    assert lib.pa_moe_sort(A, A, A, A, 131072, 256, A, need - 1, None) == -4
+    assert lib.pa_moe_sort(A, A, A, A, 131072, 256, A + 16, need, None) == -3
+    # gather / scatter-back: row size, topk, alignment
+    assert lib.pa_moe_gather(A, A, A, 100, 8, 20, 12, 1, None) == -2
+    assert lib.pa_moe_gather(A + 8, A, A, 100, 8, 20, 2048, 1, None) == -3
+    assert lib.pa_moe_gather(A, A, A, 0, 8, 20, 2048, 1, None) == 0
+    assert lib.pa_moe_scatter_back(A, A, A, A, 16, 33, 2048, 1, None) == -2
+    assert lib.pa_moe_scatter_back(A, A, A, A, 16, 8, 2044, 1, None) == -2
+    assert lib.pa_moe_scatter_back(A, A, A, A, 16, 8, 2048, 3, None) == -1
+    assert lib.pa_moe_scatter_back(A, A, A, A, 0, 8, 2048, 1, None) == 0

@@ -293,3 +293,45 @@ def make_dense_prefill_case(*, ctx_lens: Sequence[int], q_lens: Sequence[int],
         qs.append(qs[-1] + int(n))
     pc = PrefillCase(case, q, torch.tensor(qs, dtype=torch.int32), [int(n) for n in q_lens])
     return pc, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# MoE routing workload (synthetic router logits and hidden states)
+# ---------------------------------------------------------------------------
+@dataclass
+class MoeCase:
+    """Router logits [T, E] and hidden states [T, H] of one MoE layer input."""
+
+    logits: torch.Tensor
+    hidden: torch.Tensor
+    topk: int
+
+    @property
+    def num_tokens(self) -> int:
+        return self.hidden.shape[0]
+
+    @property
+    def num_experts(self) -> int:
+        return self.logits.shape[1]
+
+    def to(self, device) -> "MoeCase":
+        return MoeCase(self.logits.to(device), self.hidden.to(device), self.topk)
+
+
+MOE_SEED = 20261300
+
+
+def make_moe_case(*, num_tokens: int = 16384, num_experts: int = 256, topk: int = 8,
+                  hidden_size: int = 2048, dtype=torch.bfloat16,
+                  logits_dtype=torch.bfloat16, device="cpu", seed: int = MOE_SEED) -> MoeCase:
+    """Seeded MoE inputs: router logits ~ N(0, 1) and hidden states ~ N(0, 1),
+    both drawn in fp32 on ``device`` and rounded to their dtypes.  The default
+    shape is the pages' MoE prefill batch: 16384 tokens, 256 experts, top-8;
+    hidden size 2048 (the pages do not state it)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    logits = torch.empty((num_tokens, num_experts), dtype=logits_dtype, device=dev)
+    hidden = torch.empty((num_tokens, hidden_size), dtype=dtype, device=dev)
+    _fill_randn(logits, gen)
+    _fill_randn(hidden, gen)
+    return MoeCase(logits, hidden, topk)
