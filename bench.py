@@ -19,8 +19,11 @@ user makes) with the per-step inputs copied from pinned host memory and the
 output read back, inside the timed region.  ``cpu_baseline`` times the fp64
 oracle on a bounded sample of the same workload on the host cores.
 
-``--impl reference`` times the oracle alone (the reference arm) on the same
-workload, metric and unit.  Multi-GPU (torchrun): every rank runs its own
+``--path prefill`` times the paged prefix-prefill kernel (TFLOP/s against
+the bf16 tensor peak) and ``--path moe`` the MoE router + sort-by-expert
+regroup + scatter-back (GB/s against the HBM peak); both print a line of the
+same shape.  ``--impl reference`` times the oracle alone (the reference arm)
+on the same workload, metric and unit.  Multi-GPU (torchrun): every rank runs its own
 replica of the workload (no collective on the data path); time is the max
 over ranks and the value is the total over ranks.
 """
@@ -43,6 +46,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV-read GB/s and % of GB300 HBM peak; decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "paged prefix-prefill attention: TFLOP/s on the bf16 tensor cores"
+MOE_METRIC = ("MoE router + sort-by-expert regroup + scatter-back: GB/s of algorithmic HBM "
+              "traffic; tokens/s")
+# prefix-prefill workloads: (context tokens, chunk tokens, sequences); 24 query /
+# 4 KV heads, head_dim 128, block 16, bf16 (the decode workloads' model shape)
+PREFILL_WORKLOADS = {
+    "chunk2048_ctx16384_x16": (16384, 2048, 16),
+    "full100k_x1": (0, 100000, 1),
+    "chunk512_ctx4096_x64": (4096, 512, 64),
+}
 
 
 def parse_args():
@@ -66,6 +80,12 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--check", action="store_true",
                     help="also compare sampled sequences of the output with the oracle")
+    ap.add_argument("--path", choices=["decode", "prefill", "moe"], default="decode",
+                    help="decode (default): the paged decode step; prefill: the paged "
+                         "prefix-prefill kernel; moe: router + sort-by-expert regroup + "
+                         "scatter-back")
+    ap.add_argument("--prefill-workload", choices=sorted(PREFILL_WORKLOADS),
+                    default="chunk2048_ctx16384_x16")
     return ap.parse_args()
 
 
@@ -87,12 +107,22 @@ def qo_bytes(case) -> int:
 def source_sha() -> str:
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_decode_partitioned_gb300", "csrc", "*")))
-    files.append(os.path.join(ROOT, "include", "pa_decode.h"))
+    files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def measured_bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s, one earlier GB300 measurement)"
 
 
 def measured_peaks():
@@ -105,16 +135,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def committed_traffic(wid: int, partition_size: int):
-    """DRAM bytes per attention-kernel launch from the committed ncu summary, or None
-    if the kernel sources changed since it was taken."""
+def committed_traffic(wid, partition_size=None):
+    """DRAM bytes per launch of a dominant kernel from the committed ncu summary
+    (key ``workload{wid}_P{P}`` for decode, else the key itself), or None if the
+    kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(f"workload{wid}_P{partition_size}")
+    key = f"workload{wid}_P{partition_size}" if partition_size is not None else wid
+    e = d.get(key)
     if not e or e.get("source_sha") != source_sha():
         return None
     return e.get("dram_bytes_per_launch")
@@ -332,9 +364,386 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# The next rows of the path: prefix prefill and the MoE regrouping
+# ---------------------------------------------------------------------------
+def prefill_flops(ctx_lens, q_lens, num_q_heads, head_dim):
+    """4 * d * Hq * (visible cache tokens summed over chunk rows): QK^T and PV."""
+    vis = 0
+    for c, n in zip(ctx_lens, q_lens):
+        vis += n * c + n * (n + 1) // 2
+    return 4.0 * head_dim * num_q_heads * vis
+
+
+def timed_steps(launches, K, warmup, flush_l2, stream):
+    """Run W (and at least 1 s of) warm-up steps, then K timed steps with CUDA
+    events around every launch; a spin kernel holds the stream while the host
+    enqueues, so no host gap falls inside a step.  Returns (per-step ms,
+    per-launch mean ms, wall-clock start, end)."""
+    import torch
+    t_soak, n = time.time(), 0
+    while n < warmup or time.time() - t_soak < 1.0:
+        flush_l2()
+        for _, fn in launches:
+            fn()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(4):
+        flush_l2()
+        for _, fn in launches:
+            fn()
+    host_step = (time.perf_counter() - t0) / 4
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+          for _ in range(K)]
+    torch.cuda._sleep(int(min(2.0, 1.5 * K * host_step + 0.005) * 2.2e9))
+    w0 = time.time()
+    for k in range(K):
+        flush_l2(k)
+        ev[k][0].record(stream)
+        for j, (_, fn) in enumerate(launches):
+            fn()
+            ev[k][j + 1].record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
+    launch_ms = {name: sum(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)) / K
+                 for j, (name, _) in enumerate(launches)}
+    return step_ms, launch_ms, w0, w1
+
+
+def timed_e2e(fn, K, flush_l2, stream):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for k in range(K):
+        flush_l2(k)
+        e0[k].record(stream)
+        fn()
+        e1[k].record(stream)
+    torch.cuda.synchronize()
+    return sum(e0[k].elapsed_time(e1[k]) for k in range(K))
+
+
+def make_prefill_inputs(name, device, rank=0):
+    import torch
+    from workloads import custom_workload, make_prefill_case
+    ctx, n, S = PREFILL_WORKLOADS[name]
+    w = custom_workload(num_q_heads=24, num_kv_heads=4, head_dim=128, block_size=16,
+                        dtype=torch.bfloat16, name=f"prefill_{name}")
+    return make_prefill_case(w, ctx_lens=[ctx] * S, q_lens=[n] * S, device=device,
+                             seed=20261400 + 1000 * rank), (ctx, n, S)
+
+
+def oracle_prefill_sample(pc, rows: int):
+    """The oracle's prefix prefill on the last ``rows`` chunk rows of sequence 0
+    (they see the most context): host copies of that sequence's blocks."""
+    import torch
+    import oracle
+    c = pc.case
+    L = c.seq_lens_list[0]
+    n = pc.q_lens[0]
+    rows = max(1, min(rows, n))
+    bs = c.key_cache.shape[1]
+    nb = -(-L // bs)
+    blocks = c.block_tables[0, :nb].long()
+    kc = c.key_cache.index_select(0, blocks).cpu()
+    vc = c.value_cache.index_select(0, blocks).cpu()
+    bt = torch.arange(nb, dtype=torch.int32)[None, :]
+    q = pc.query[n - rows:n].cpu()
+    qs = torch.tensor([0, rows], dtype=torch.int32)
+    sl = torch.tensor([L], dtype=torch.int32)
+    t = time.perf_counter()
+    oracle.prefill(q, kc, vc, bt, sl, qs, c.scale)
+    secs = time.perf_counter() - t
+    flops = 4.0 * c.workload.head_dim * c.workload.num_q_heads * sum(
+        L - rows + i + 1 for i in range(rows))
+    return secs, flops, rows
+
+
+def run_next_path(args, rank, world, local_rank):
+    """``--path prefill`` / ``--path moe``: one JSON line in the same contract."""
+    import torch
+    import torch.distributed as dist
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return run_next_reference(args, world)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from paged_kv_decode_partitioned_gb300 import build as pa_build
+    if rank == 0:
+        pa_build.build()
+    if world > 1:
+        dist.barrier()
+    pa_build.build()
+    import paged_kv_decode_partitioned_gb300 as pa
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device="cuda")
+    flush_sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def flush_l2(k=1):
+        flush_w.fill_(k & 0xFF)
+        torch.sum(flush_r, dim=0, out=flush_sink)
+
+    K = args.steps
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if args.path == "prefill":
+        pc, (ctx, n, S) = make_prefill_inputs(args.prefill_workload, "cuda", rank)
+        c = pc.case
+        w = c.workload
+        out = torch.empty_like(pc.query)
+
+        def run():
+            pa.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                       pc.q_start, c.scale, n, out=out)
+        launches = [("prefill", run)]
+        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream)
+        if pa.device_status() != 0:
+            raise SystemExit("device status flags raised")
+        flops = prefill_flops([ctx] * S, [n] * S, w.num_q_heads, w.head_dim)
+        (tot_ms,), (fl_all, tok_all) = across_ranks(world, "cuda", [sum(step_ms)],
+                                                    [flops, n * S])
+        ms = tot_ms / K
+        value = fl_all / (ms * 1e-3) / 1e12
+        peak, peak_src = measured_bf16_peak()
+        achieved = flops / (launch_ms["prefill"] * 1e-3) / 1e12
+        e2e = None
+        if not args.no_e2e:
+            hq = pc.query.cpu().pin_memory()
+            hqs = pc.q_start.cpu().pin_memory()
+            hsl = c.seq_lens.cpu().pin_memory()
+            hbt = c.block_tables.cpu().pin_memory()
+            hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+            h2d = (hq.numel() * 2 + hqs.numel() * 4 + hsl.numel() * 4 + hbt.numel() * 4)
+
+            def e2e_step():
+                pc.query.copy_(hq, non_blocking=True)
+                pc.q_start.copy_(hqs, non_blocking=True)
+                c.seq_lens.copy_(hsl, non_blocking=True)
+                c.block_tables.copy_(hbt, non_blocking=True)
+                run()
+                hout.copy_(out, non_blocking=True)
+            (e_ms,), _ = across_ranks(world, "cuda", [timed_e2e(e2e_step, K, flush_l2, stream)])
+            e2e = {"value": round(fl_all / (e_ms / K * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 2),
+                   "kv_cache": "resident in HBM; chunk query, tables and lengths copied in"}
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            secs, fl, rows = oracle_prefill_sample(pc, 8)
+            rows = max(1, min(n, int(rows * args.cpu_seconds / max(secs, 1e-3))))
+            secs, fl, rows = oracle_prefill_sample(pc, rows)
+            cpu = {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_threads(),
+                   "kind": "oracle",
+                   "sample": f"the last {rows} chunk rows of sequence 0 ({fl / 1e9:.1f} GFLOP), "
+                             f"{secs:.1f} s"}
+        name = f"prefill_{args.prefill_workload}_hq24_hkv4_d128_bs16_bf16"
+        line = {
+            "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": name, "global_batch": S * world, "context_tokens": ctx,
+                       "chunk_tokens": n,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed between steps (outside the events)"},
+            "prefill_tokens_per_s": round(tok_all / (ms * 1e-3), 1),
+            "roofline": {"bound": "tensor", "kernel": "pa_prefill_tc_kernel",
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": committed_traffic(f"prefill_{args.prefill_workload}"),
+                         "algorithmic_flops_per_launch": flops,
+                         "kernel_ms_per_launch": round(launch_ms["prefill"], 4),
+                         "peak_source": peak_src},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "launch_ms": {k: round(v, 4) for k, v in launch_ms.items()},
+            "gpu_launches": K, "clocks": None,
+        }
+    else:
+        from workloads import make_moe_case
+        case = make_moe_case(device="cuda", seed=20261500 + 1000 * rank)
+        T, E, K_, H = case.num_tokens, case.num_experts, case.topk, case.hidden.shape[1]
+        P = T * K_
+        w = torch.empty((T, K_), dtype=torch.float32, device="cuda")
+        ids = torch.empty((T, K_), dtype=torch.int32, device="cuda")
+        ws = torch.empty(pa.moe_sort_workspace_bytes(P, E), dtype=torch.uint8, device="cuda")
+        sp = torch.empty(P, dtype=torch.int32, device="cuda")
+        off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        pos = torch.empty(P, dtype=torch.int32, device="cuda")
+        y = torch.empty((P, H), dtype=case.hidden.dtype, device="cuda")
+        out = torch.empty_like(case.hidden)
+        launches = [
+            ("topk_softmax", lambda: pa.topk_softmax(case.logits, K_, True, weights=w, ids=ids)),
+            ("sort", lambda: pa.moe_sort(ids, E, workspace=ws, out=(sp, off, pos))),
+            ("gather", lambda: pa.moe_gather(case.hidden, sp, K_, out=y)),
+            ("scatter_back", lambda: pa.moe_scatter_back(y, pos, w, out=out)),
+        ]
+        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream)
+        if pa.device_status() != 0:
+            raise SystemExit("device status flags raised")
+        row = H * 2
+        alg = {"topk_softmax": T * E * 2 + T * K_ * 8,
+               "sort": 3 * P * 4 + 2 * P * 4,          # ids read by 3 launches; order + inverse
+               "gather": P * row + T * row,
+               "scatter_back": P * row + T * row + T * K_ * 8}
+        step_bytes = sum(alg.values())
+        (tot_ms,), (b_all, t_all) = across_ranks(world, "cuda", [sum(step_ms)], [step_bytes, T])
+        ms = tot_ms / K
+        value = b_all / (ms * 1e-3) / 1e9
+        peak, peak_src = measured_peaks()
+        dom = "gather"
+        achieved = alg[dom] / (launch_ms[dom] * 1e-3) / 1e9
+        e2e = None
+        if not args.no_e2e:
+            hl = case.logits.cpu().pin_memory()
+            hh = case.hidden.cpu().pin_memory()
+            hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+            def e2e_step():
+                case.logits.copy_(hl, non_blocking=True)
+                case.hidden.copy_(hh, non_blocking=True)
+                for _, fn in launches:
+                    fn()
+                hout.copy_(out, non_blocking=True)
+            (e_ms,), _ = across_ranks(world, "cuda", [timed_e2e(e2e_step, K, flush_l2, stream)])
+            e2e = {"value": round(b_all / (e_ms / K * 1e-3) / 1e9, 2), "unit": "GB/s",
+                   "h2d_bytes_per_step": int(hl.numel() * 2 + hh.numel() * 2),
+                   "d2h_bytes_per_step": int(hout.numel() * 2)}
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            cpu = oracle_moe_sample(case, args.cpu_seconds)
+        line = {
+            "metric": MOE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"moe_T{T}_E{E}_top{K_}_H{H}_bf16_identity_expert",
+                       "global_batch": T * world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed between steps (outside the events)",
+                       "expert": "identity (the expert GEMMs need trained weights; not built)"},
+            "tokens_per_s": round(t_all / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "kernel": "pa_moe_gather_kernel",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": committed_traffic("moe_gather"),
+                         "algorithmic_bytes_per_launch": alg[dom],
+                         "kernel_ms_per_launch": round(launch_ms[dom], 4),
+                         "peak_source": peak_src,
+                         "per_kernel_gbs": {k: round(alg[k] / (launch_ms[k] * 1e-3) / 1e9, 1)
+                                            for k in alg}},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "launch_ms": {k: round(v, 4) for k, v in launch_ms.items()},
+            "gpu_launches": K * 6,   # router 1, sort 3, gather 1, scatter-back 1
+            "clocks": None,
+        }
+    rows = sampler.stop()
+    if rank != 0:
+        return
+    line["clocks"] = ClockSampler.summary(rows, w0, w1)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def oracle_moe_sample(case, target_seconds):
+    """The oracle's router + sort + gather + scatter-back on the first tokens of
+    the batch, sized to about target_seconds on the host cores."""
+    import numpy as np
+    import oracle
+    oracle.build()
+
+    def chain(t):
+        logits = case.logits[:t].cpu()
+        hidden = case.hidden[:t].cpu()
+        s0 = time.perf_counter()
+        w, ids = oracle.topk_softmax(logits, case.topk, True)
+        sp, off, pos = oracle.moe_sort(ids, case.num_experts)
+        y = oracle.moe_gather(hidden, sp, case.topk)
+        import torch
+        oracle.moe_scatter(torch.from_numpy(y.view(np.int16)).view(torch.bfloat16), pos, w,
+                           case.topk)
+        return time.perf_counter() - s0
+
+    t = 256
+    secs = chain(t)
+    t = int(max(1, min(case.num_tokens, t * target_seconds / max(secs, 1e-3))))
+    secs = chain(t)
+    H = case.hidden.shape[1]
+    P = t * case.topk
+    byts = t * case.num_experts * 2 + 2 * (P * H * 2 + t * H * 2)
+    return {"value": round(byts / secs / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"the first {t} of {case.num_tokens} tokens, {secs:.1f} s"}
+
+
+def run_next_reference(args, world):
+    """``--impl reference`` for the prefill / MoE paths: the oracle on the host."""
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    steps = []
+    if args.path == "prefill":
+        pc, (ctx, n, S) = make_prefill_inputs(args.prefill_workload, dev)
+        per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+        secs, fl, rows = oracle_prefill_sample(pc, 4)
+        rows = max(1, min(n, int(rows * per_step / max(secs, 1e-3))))
+        for _ in range(args.warmup + args.steps):
+            secs, fl, rows = oracle_prefill_sample(pc, rows)
+            steps.append(secs)
+        steps = steps[args.warmup:]
+        mean = sum(steps) / len(steps)
+        value, unit = fl / mean / 1e12, "TFLOP/s"
+        sample = f"the last {rows} chunk rows of sequence 0 per step"
+        metric, wl = PREFILL_METRIC, f"prefill_{args.prefill_workload}_hq24_hkv4_d128_bs16_bf16"
+    else:
+        from workloads import make_moe_case
+        case = make_moe_case(device=dev, seed=20261500)
+        per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+        vals = []
+        for _ in range(args.warmup + args.steps):
+            c = oracle_moe_sample(case, per_step)
+            vals.append(c)
+        vals = vals[args.warmup:]
+        value = sum(v["value"] for v in vals) / len(vals)
+        unit, sample = "GB/s", vals[-1]["sample"]
+        mean = None
+        metric = MOE_METRIC
+        wl = f"moe_T{case.num_tokens}_E{case.num_experts}_top{case.topk}_H" \
+             f"{case.hidden.shape[1]}_bf16_identity_expert"
+    line = {
+        "impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 3) if mean else None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl, "parallelism": "host threads (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cpu_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
+    if args.path != "decode":
+        if args.impl == "ours" and (args.steps < 1 or args.warmup < 3):
+            raise SystemExit("need --steps >= 1 and --warmup >= 3")
+        run_next_path(args, rank, world, local_rank)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
