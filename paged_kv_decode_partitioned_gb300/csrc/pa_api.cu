@@ -630,7 +630,7 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     p.block_size = block_size;
     p.max_blocks = max_blocks_per_seq;
     p.num_blocks = num_blocks;
-    p.tokens_per_cta = kPrefillRows / group;
+    p.tokens_per_cta = prefill_rows_per_cta(head_dim) / group;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const dim3 grid((max_q_len + p.tokens_per_cta - 1) / p.tokens_per_cta, num_kv_heads,
                     num_seqs);

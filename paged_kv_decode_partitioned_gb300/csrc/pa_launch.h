@@ -25,6 +25,9 @@ cudaError_t launch_prefill_tc(int D, const CUtensorMap &tmQ, const CUtensorMap &
                               const CUtensorMap &tmV, const PrefillParams &p, dim3 grid,
                               cudaStream_t st);
 
+// Query rows (chunk token x group head) one prefill CTA covers at head_dim D.
+int prefill_rows_per_cta(int D);
+
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_gather(int D, const CUtensorMap &tmK, const CUtensorMap &tmV,

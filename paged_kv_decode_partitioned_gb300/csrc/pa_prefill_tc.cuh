@@ -8,27 +8,32 @@
 // chunk row i of sequence s (n chunk tokens, L cached tokens) sits at
 // position p = L - n + i and attends to cache tokens 0..p.  The pages' tile
 // loop (matmul, softmax, matmul per key tile with the running max and sum of
-// the online softmax) is what one CTA runs below.
+// the online softmax) is what each Q tile of a CTA runs below.
 //
-// One CTA = 128 query rows of one (sequence, KV head): row = chunk token x
-// query head of the GQA group, so every row of the CTA uses every K/V tile
-// it loads.  Warp roles (192 threads):
+// One CTA = NQ Q tiles of 128 query rows of one (sequence, KV head): row =
+// chunk token x query head of the GQA group, so every row of the CTA uses
+// every K/V tile it loads, and with two Q tiles each loaded K/V byte feeds
+// 256 rows.  Warp roles (64 + 128 NQ threads):
 //   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
-//              x the CTA's chunk tokens), then N-token K and V tiles of the
-//              context through NS shared-memory stages, walking the block
-//              table through a lane-distributed window of 16-token box ids;
-//   warp 1     tensor-memory owner and MMA issuer (one thread): S_j = Q K_j^T
-//              into one of two S buffers in tensor memory and
-//              O += P_j V_j with P read from tensor memory (the S buffer it
-//              was written over) and O accumulating in tensor memory, each
-//              issued as soon as its inputs are ready; tcgen05.commit
-//              completes the mbarriers that free K and V stages separately;
-//   warps 2-5  softmax (one thread per row, the row's tensor-memory lane):
-//              S row -> causal mask -> scale -> running max -> exp2 -> P (bf16
-//              or f16) written back into tensor memory; O is rescaled in
-//              tensor memory only when a row's max grows by more than 2^8
-//              (exponents stay below 2^8 in between and the final division by
-//              the running sum is exact either way); finally O / l -> out.
+//              x the CTA's chunk tokens), then 64-token K and V tiles of the
+//              context through NS shared-memory stages; each lane looks up the
+//              block of one (16-row box, 64-element piece) and issues its
+//              copy, so a tile's copies go out in parallel.  Each CTA starts
+//              its walk at its own tile and wraps around;
+//   warp 1     tensor-memory owner and MMA issuer (one thread): for each Q
+//              tile, S_j = Q K_j^T into one of two S buffers in tensor memory
+//              and O += P_j V_j with P read from tensor memory (the S buffer
+//              it was written over) and O accumulating in tensor memory; it
+//              polls its barriers and issues whichever MMA is ready, so the
+//              two tiles' MMAs fill the gaps of each other's softmax; a K
+//              (V) stage is released once every Q tile's QK (PV) has used it;
+//   warps 2..  one softmax warpgroup per Q tile, one thread per query row
+//              (its tensor-memory lane): S row -> causal mask -> scale ->
+//              running max -> exp2 -> P (bf16 or f16) written back into tensor
+//              memory; O is rescaled in tensor memory only when a row's max
+//              grows by more than 2^8 (exponents stay below 2^8 in between and
+//              the final division by the running sum is exact either way);
+//              finally O / l -> out.
 // Every mbarrier wait is bounded; a role that gives up raises
 // PA_DEV_WAIT_TIMEOUT and leaves its loop, in-flight copies and MMAs are
 // waited for (bounded) and tensor memory is freed before the CTA exits.
@@ -39,40 +44,47 @@
 
 namespace pa {
 
-// Tile plan per head_dim.  d64 / d128: 64-token K/V tiles and a 256-column
-// tensor-memory footprint, so two CTAs share an SM and one CTA's softmax
-// overlaps the other's MMAs.  d256: one CTA per SM.
-#ifndef PA_PREFILL_TC_N
-#define PA_PREFILL_TC_N 64
+// Back-off of the MMA thread's polling loop when nothing is ready (0: spin).
+#ifndef PA_PREFILL_MMA_SLEEP_NS
+#define PA_PREFILL_MMA_SLEEP_NS 0
 #endif
+
+// Tile plan per head_dim.  A tcgen05.mma with M = 128 and K = 16 costs about
+// 80 cycles whatever N <= 128 is (measured on GB300: N = 64 reaches 38 % of
+// the tensor peak, N = 128 80 %, N = 256 all of it), so the MMAs are kept
+// wide: head_dim 64 / 128 run 128-token K/V tiles and two Q tiles per CTA, each
+// with one S buffer in tensor memory (the two tiles take turns on the tensor
+// pipe); head_dim 256 (its O alone takes 256 columns) runs one Q tile with two
+// S buffers of 64 tokens.
 template <int D>
 struct PrefillTcCfg {
-    static constexpr int kRows = kPrefillRows;                   // 128 query rows (MMA M)
-    static constexpr int kN = D <= 128 ? PA_PREFILL_TC_N : 64;   // cache tokens per tile
-    static constexpr int kCtasPerSm = (D <= 128 && kN == 64) ? 2 : 1;
-    static constexpr int kStages = kCtasPerSm == 2 ? (D <= 64 ? 4 : 2)
-                                                   : (D <= 64 ? 6 : (D <= 128 ? 3 : 2));
+    static constexpr int kQTiles = D <= 128 ? 2 : 1;
+    static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
+    static constexpr int kN = D <= 128 ? 128 : 64;                // cache tokens per tile
+    static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
+    static constexpr int kStages = D <= 64 ? 6 : 2;
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
+    static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
     static constexpr int kKvPiece = kN * 128;                    // bytes of one K (V) piece
     static constexpr int kQBytes = kPieces * kQPiece;
     static constexpr int kTileBytes = kPieces * kKvPiece;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
-    // barriers: q_full, o_full, vtail, mma_done, k_full[NS], v_full[NS],
-    // k_empty[NS], v_empty[NS], s_full[2], p_full[2], s_free[2]; then the
-    // tensor-memory slot
-    static constexpr int kNumBars = 4 + 4 * kStages + 6;
+    // barriers: q_full, vtail, mma_done, k_full[NS], v_full[NS], k_empty[NS],
+    // v_empty[NS]; per Q tile s_full[2], p_full[2], s_free[2], o_full (the
+    // first kSBufs of each pair in use); then the tensor-memory slot
+    static constexpr int kTileBars = 7;
+    static constexpr int kNumBars = 3 + 4 * kStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
     static constexpr int kLaunchBytes = kSlotOffset + 16 + 1024;
-    static constexpr int kThreads = 192;
-    // tensor memory: S0 [0, N), S1 [N, 2N), O [2N, 2N + D), rounded up to a power of two
-    static constexpr int kOCol = 2 * kN;
-    static constexpr int kTmemCols = kOCol + D <= 256 ? 256 : 512;
-    static_assert(kLaunchBytes * kCtasPerSm <= 228 * 1024 - 1024 * kCtasPerSm,
-                  "shared memory plan too large");
-    static_assert(kOCol + D <= kTmemCols && kTmemCols * kCtasPerSm <= 512,
-                  "tensor memory plan too large");
+    static constexpr int kThreads = 64 + 128 * kQTiles;
+    // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
+    static constexpr int kOCol = kSBufs * kN;
+    static constexpr int kTileCols = kSBufs * kN + D;
+    static constexpr int kTmemCols = 512;
+    static_assert(kLaunchBytes <= 227 * 1024, "shared memory plan too large");
+    static_assert(kTileCols * kQTiles <= kTmemCols, "tensor memory plan too large");
 };
 
 template <typename T> struct TcType;
@@ -119,12 +131,12 @@ __device__ __forceinline__ bool mbar_wait_cycles(uint32_t bar, uint32_t parity) 
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
+__global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     using C = PrefillTcCfg<D>;
-    constexpr int N = C::kN, NS = C::kStages;
+    constexpr int N = C::kN, NS = C::kStages, NQ = C::kQTiles, SB = C::kSBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -132,10 +144,10 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
     const uint32_t q_smem = base;
     const uint32_t stage0 = base + C::kQBytes;
     const uint32_t bars = base + C::kBarOffset;
-    const uint32_t q_full = bars, o_full = bars + 8, vtail = bars + 16, mma_done = bars + 24;
-    const uint32_t k_full = bars + 32, v_full = k_full + NS * 8;
+    const uint32_t q_full = bars, vtail = bars + 8, mma_done = bars + 16;
+    const uint32_t k_full = bars + 24, v_full = k_full + NS * 8;
     const uint32_t k_empty = v_full + NS * 8, v_empty = k_empty + NS * 8;
-    const uint32_t s_full = v_empty + NS * 8, p_full = s_full + 16, s_free = p_full + 16;
+    const uint32_t tile_bars = v_empty + NS * 8;   // + t * 56: s_full, p_full, s_free, o_full
     const uint32_t slot = base + C::kSlotOffset;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -163,13 +175,18 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
     const int pos_first = L - n + tok0;   // position of the CTA's first chunk token
     const int kv_end = pos_first + ntok;  // cache tokens any row of the CTA sees
     const int ntiles = (kv_end + N - 1) / N;
+    // The CTAs of one (sequence, KV head) start their walk over the context
+    // at different tiles: run in lockstep from tile 0 they would all ask the
+    // same L2 lines at once.  The online softmax does not depend on the order.
+    const int rot = static_cast<int>((static_cast<unsigned>(qt) * 37u) % static_cast<unsigned>(ntiles));
+    const int rows_used = g * ntok;
+    const int nq = NQ > 1 && rows_used > 128 ? 2 : 1;   // Q tiles with any row to compute
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmQ);
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
         mbar_init(q_full, 1);
-        mbar_init(o_full, 1);
         mbar_init(vtail, 1);
         mbar_init(mma_done, 1);
         for (int i = 0; i < NS; ++i) {
@@ -178,10 +195,14 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
             mbar_init(k_empty + i * 8, 1);
             mbar_init(v_empty + i * 8, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full + i * 8, 1);
-            mbar_init(p_full + i * 8, 4);   // one arrive per softmax warp
-            mbar_init(s_free + i * 8, 1);
+        for (int t = 0; t < NQ; ++t) {
+            const uint32_t tb = tile_bars + t * 56;
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(tb + i * 8, 1);          // s_full
+                mbar_init(tb + 16 + i * 8, 4);     // p_full: one arrive per softmax warp
+                mbar_init(tb + 32 + i * 8, 1);     // s_free
+            }
+            mbar_init(tb + 48, 1);                 // o_full
         }
         fence_mbar_init();
     }
@@ -196,14 +217,19 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kBoxes = N / kTile;   // 16-token boxes per tile
-        auto fetch = [&](int bx) -> int {
-            if (bx >= nbox) return 0;
+        constexpr int kOps = kBoxes * C::kPieces;   // copies per K (or V) tile
+        static_assert(kOps <= 32, "one copy per lane");
+        const int op_box = (lane % kOps) / C::kPieces, op_piece = (lane % kOps) % C::kPieces;
+        // block of this lane's box of tile jt (0 when the lane has no copy)
+        auto box_block = [&](int jt) -> int {
+            const int bx = jt * kBoxes + op_box;
+            if (lane >= kOps || bx >= nbox) return 0;
             const int b = __ldg(bt_row + (bx * kTile) / p.block_size);
             if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
                 atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
             return b;
         };
-        // Q rows the box does not cover (128 % group) are never loaded: zero
+        // Q rows the box does not cover (kRows % group) are never loaded: zero
         // them so those rows stay finite (and never force an O rescale).
         const int qrows = g * p.tokens_per_cta;
         if (qrows < C::kRows) {
@@ -220,29 +246,22 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
             for (int c = 0; c < C::kPieces; ++c)
                 tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
         }
-        int win_cur = fetch(lane), win_next = fetch(32 + lane), win_base = 0;
+        int jt_next = rot, phys_next = box_block(rot);
         int issued = 0;
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
             const int st = j % NS;
+            const int jt = jt_next, op_phys = phys_next;
+            jt_next = jt + 1 == ntiles ? 0 : jt + 1;
+            if (j + 1 < ntiles) phys_next = box_block(jt_next);   // next tile's table entries
             const uint32_t kdst = stage0 + st * C::kStageBytes, vdst = kdst + C::kTileBytes;
-            const bool last = j == ntiles - 1;
+            const bool last = jt == ntiles - 1;   // the context's tail tile
             const uint32_t vbar = last ? vtail : v_full + st * 8;
-            int phys[kBoxes];
             int boxes = 0;
 #pragma unroll
-            for (int k = 0; k < kBoxes; ++k) {
-                const int bx = j * kBoxes + k;
-                if (bx - win_base >= 32) {   // slide the block-table window
-                    win_cur = win_next;
-                    win_base += 32;
-                    win_next = fetch(win_base + 32 + lane);
-                }
-                phys[k] = __shfl_sync(0xffffffffu, win_cur, bx - win_base);
-                boxes += bx < nbox;
-            }
+            for (int k = 0; k < kBoxes; ++k) boxes += jt * kBoxes + k < nbox;
             const uint32_t bytes = static_cast<uint32_t>(boxes * C::kPieces * 2048);
-            // K of tile j once QK of tile j - NS is done, V once its PV is done
+            // K of tile j once every QK of tile j - NS is done, V once every PV is
             if (j >= NS) {
                 const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NS) - 1) & 1u);
                 if (!__all_sync(0xffffffffu, w)) {
@@ -250,18 +269,14 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
                     break;
                 }
             }
-            if (lane == 0) {
-                mbar_expect_tx(k_full + st * 8, bytes);
-#pragma unroll
-                for (int k = 0; k < kBoxes; ++k)
-                    if (j * kBoxes + k < nbox) {
-                        const int row = ((j * kBoxes + k) * kTile) % p.block_size;
-#pragma unroll
-                        for (int c = 0; c < C::kPieces; ++c)
-                            tma_load_5d(kdst + c * C::kKvPiece + k * 2048, &tmK, k_full + st * 8,
-                                        0, c, kvh, row, phys[k]);
-                    }
-            }
+            // one copy per lane: a single thread issuing them back to back is
+            // bound by the issue latency of each copy, not by the TMA engine
+            if (lane == 0) mbar_expect_tx(k_full + st * 8, bytes);
+            __syncwarp();
+            if (lane < kOps && jt * kBoxes + op_box < nbox)
+                tma_load_5d(kdst + op_piece * C::kKvPiece + op_box * 2048, &tmK, k_full + st * 8,
+                            0, op_piece, kvh, ((jt * kBoxes + op_box) * kTile) % p.block_size,
+                            op_phys);
             if (j >= NS) {
                 const bool w = mbar_wait_cycles(v_empty + st * 8, ((j / NS) - 1) & 1u);
                 if (!__all_sync(0xffffffffu, w)) {
@@ -271,18 +286,11 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
                     break;
                 }
             }
-            if (lane == 0) {
-                mbar_expect_tx(vbar, bytes);
-#pragma unroll
-                for (int k = 0; k < kBoxes; ++k)
-                    if (j * kBoxes + k < nbox) {
-                        const int row = ((j * kBoxes + k) * kTile) % p.block_size;
-#pragma unroll
-                        for (int c = 0; c < C::kPieces; ++c)
-                            tma_load_5d(vdst + c * C::kKvPiece + k * 2048, &tmV, vbar, 0, c, kvh,
-                                        row, phys[k]);
-                    }
-            }
+            if (lane == 0) mbar_expect_tx(vbar, bytes);
+            __syncwarp();
+            if (lane < kOps && jt * kBoxes + op_box < nbox)
+                tma_load_5d(vdst + op_piece * C::kKvPiece + op_box * 2048, &tmV, vbar, 0, op_piece,
+                            kvh, ((jt * kBoxes + op_box) * kTile) % p.block_size, op_phys);
             issued = j + 1;
             if (last) {
                 // V rows at or past kv_end hold cache data past the context (or
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
                     ok = false;
                     break;
                 }
-                const int first_row = kv_end - j * N;
+                const int first_row = kv_end - jt * N;
                 const int nchunks = (N - first_row) * 8;   // 16-byte chunks per piece
                 for (int c = 0; c < C::kPieces; ++c)
                     for (int e = lane; e < nchunks; e += 32)
@@ -307,59 +315,80 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
         if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
         // copies still landing must land before the CTA exits
         (void)mbar_wait_cycles(q_full, 0);
+        const int j_tail = ntiles - 1 - rot;   // use order of the tail tile
         for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
             (void)mbar_wait_cycles(k_full + (j % NS) * 8, (j / NS) & 1u);
-            if (j != ntiles - 1)
-                (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
+            if (j != j_tail) (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
         }
-        if (issued == ntiles) (void)mbar_wait_cycles(vtail, 0);
+        if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
             constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
             bool ok = mbar_wait_cycles(q_full, 0);
-            // Issue whichever of QK (next tile) and PV (oldest tile with P ready)
-            // can go: a late K tile must not hold back the PV that frees a stage.
-            int qk = 0, pv = 0;
+            int qk[NQ], pv[NQ];
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) qk[t] = pv[t] = 0;
             bool idle = false;
             long long idle_since = 0;
-            while (ok && pv < ntiles) {
-                bool progress = false;
-                if (pv < qk && mbar_test(p_full + (pv & 1) * 8, (pv >> 1) & 1u) &&
-                    mbar_test(v_full + (pv % NS) * 8, (pv / NS) & 1u)) {
-                    tc05::fence_after_sync();
-                    const int bb = pv & 1;
-                    const uint32_t vst = stage0 + (pv % NS) * C::kStageBytes + C::kTileBytes;
+            while (ok) {
+                bool busy = false, progress = false;
 #pragma unroll
-                    for (int kt = 0; kt < N / 16; ++kt)
-                        tc05::mma_ts(tmem + C::kOCol, tmem + bb * N + kt * 8,
-                                     tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
-                                     idesc_pv, (pv > 0 || kt > 0) ? 1u : 0u);
-                    tc05::commit(s_free + bb * 8);
-                    tc05::commit(v_empty + (pv % NS) * 8);
-                    ++pv;
-                    progress = true;
-                }
-                // S buffer qk & 1 is free once PV of tile qk - 2 has completed
-                if (qk < ntiles && qk <= pv + 1 &&
-                    mbar_test(k_full + (qk % NS) * 8, (qk / NS) & 1u) &&
-                    (qk < 2 || mbar_test(s_free + (qk & 1) * 8, ((qk - 2) >> 1) & 1u))) {
-                    tc05::fence_after_sync();
-                    const uint32_t kst = stage0 + (qk % NS) * C::kStageBytes;
+                for (int t = 0; t < NQ; ++t) {
+                    if (t >= nq) break;
+                    busy |= pv[t] < ntiles;
+                    const uint32_t tb = tile_bars + t * 56;
+                    const uint32_t tcol = tmem + t * C::kTileCols;
+                    // PV of the oldest tile whose P is ready
+                    int j = pv[t];
+                    if (j < qk[t] && mbar_test(tb + 16 + (j % SB) * 8, (j / SB) & 1u) &&
+                        mbar_test(v_full + (j % NS) * 8, (j / NS) & 1u)) {
+                        tc05::fence_after_sync();
+                        const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        tc05::mma_ss(tmem + (qk & 1) * N,
-                                     tc05::sw128_desc(q_smem + (kk >> 2) * C::kQPiece + (kk & 3) * 32,
-                                                      16, 1024),
-                                     tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32,
-                                                      16, 1024),
-                                     idesc_qk, kk > 0 ? 1u : 0u);
-                    tc05::commit(s_full + (qk & 1) * 8);
-                    tc05::commit(k_empty + (qk % NS) * 8);
-                    ++qk;
-                    progress = true;
+                        for (int kt = 0; kt < N / 16; ++kt)
+                            tc05::mma_ts(tcol + C::kOCol, tcol + (j % SB) * N + kt * 8,
+                                         tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
+                                         idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
+                        tc05::commit(tb + 32 + (j % SB) * 8);   // s_free
+                        bool last_user = true;   // the V stage is free once every tile used it
+#pragma unroll
+                        for (int u = 0; u < NQ; ++u)
+                            if (u != t && u < nq && pv[u] <= j) last_user = false;
+                        if (last_user) tc05::commit(v_empty + (j % NS) * 8);
+                        if (j == ntiles - 1) tc05::commit(tb + 48);   // o_full
+                        ++pv[t];
+                        progress = true;
+                    }
+                    // QK of the next tile; S buffer j % SB is free once PV of j - SB is done
+                    j = qk[t];
+                    if (j < ntiles && j <= pv[t] + SB - 1 &&
+                        mbar_test(k_full + (j % NS) * 8, (j / NS) & 1u) &&
+                        (j < SB || mbar_test(tb + 32 + (j % SB) * 8, ((j - SB) / SB) & 1u))) {
+                        tc05::fence_after_sync();
+                        const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
+                        const uint32_t qst = q_smem + t * C::kQTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            tc05::mma_ss(
+                                tcol + (j % SB) * N,
+                                tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16,
+                                                 1024),
+                                tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16,
+                                                 1024),
+                                idesc_qk, kk > 0 ? 1u : 0u);
+                        tc05::commit(tb + (j % SB) * 8);   // s_full
+                        bool last_user = true;
+#pragma unroll
+                        for (int u = 0; u < NQ; ++u)
+                            if (u != t && u < nq && qk[u] <= j) last_user = false;
+                        if (last_user) tc05::commit(k_empty + (j % NS) * 8);
+                        ++qk[t];
+                        progress = true;
+                    }
                 }
+                if (!busy) break;
                 if (progress) {
                     idle = false;
                 } else if (!idle) {
@@ -367,11 +396,10 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
                     idle_since = clock64();
                 } else if (clock64() - idle_since > 1000000000ll) {
                     ok = false;
-                } else {
-                    __nanosleep(20);
+                } else if (PA_PREFILL_MMA_SLEEP_NS > 0) {
+                    __nanosleep(PA_PREFILL_MMA_SLEEP_NS);
                 }
             }
-            if (ok) tc05::commit(o_full);
             if (!ok) atomicOr(p.status, kWaitTimeout);
             // every MMA issued has completed before tensor memory is freed
             tc05::commit(mma_done);
@@ -380,116 +408,130 @@ __global__ void __launch_bounds__(192, PrefillTcCfg<D>::kCtasPerSm)
         __syncwarp();
     } else {
         // ------------------------------ softmax ------------------------------
-        const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
-        const int r = quarter * 32 + lane;
-        const int rows_used = g * ntok;
-        const bool valid = r < rows_used;
-        const int tq = valid ? r / g : ntok - 1, hq = valid ? r % g : 0;
-        const int pos = pos_first + tq;   // last cache token this row sees
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const float sl2 = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            const int b = j & 1;
-            const bool w = mbar_wait_cycles(s_full + b * 8, (j >> 1) & 1u);
-            if (!__all_sync(0xffffffffu, w)) {
-                ok = false;
-                break;
-            }
-            tc05::fence_after_sync();
-            const uint32_t sb = tmem + lane_base + b * N;
-            float x[N];
-            {
-                uint32_t rr[N];
-                if constexpr (N == 128) tc05::ld128(sb, rr);
-                else tc05::ld64(sb, rr);
-#pragma unroll
-                for (int c = 0; c < N; ++c) x[c] = __uint_as_float(rr[c]);
-            }
-            const int lim = pos - j * N;   // columns c <= lim are visible
-            float mx[8];   // eight independent max chains
-            if (lim >= N - 1) {
-#pragma unroll
-                for (int c = 0; c < N; ++c) {
-                    x[c] *= sl2;
-                    mx[c & 7] = c < 8 ? x[c] : fmaxf(mx[c & 7], x[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < N; ++c) {
-                    x[c] = c <= lim ? x[c] * sl2 : -INFINITY;
-                    mx[c & 7] = c < 8 ? x[c] : fmaxf(mx[c & 7], x[c]);
-                }
-            }
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (j == 0) {
-                m = mt;   // column 0 (cache token 0) is visible to every row
-            } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled
-                const bool w2 = mbar_wait_cycles(s_free + ((j - 1) & 1) * 8, ((j - 1) >> 1) & 1u);
-                if (!__all_sync(0xffffffffu, w2)) {
+        const int t = (warp - 2) >> 2;   // the Q tile of this warpgroup
+        if (t < nq) {
+            const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
+            const int r = t * 128 + quarter * 32 + lane;
+            const bool valid = r < rows_used;
+            const int tq = valid ? r / g : ntok - 1, hq = valid ? r % g : 0;
+            const int pos = pos_first + tq;   // last cache token this row sees
+            const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+            const uint32_t tcol = tmem + lane_base + t * C::kTileCols;
+            const uint32_t tb = tile_bars + t * 56;
+            const float sl2 = p.scale_log2;
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < ntiles; ++j) {
+                const int b = j % SB;
+                const bool w = mbar_wait_cycles(tb + b * 8, (j / SB) & 1u);
+                if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
                     break;
                 }
                 tc05::fence_after_sync();
-                const float mn = fmaxf(m, mt);
-                const float alpha = ex2(m - mn);
-                m = mn;
-                l *= alpha;
+                const uint32_t sb = tcol + b * N;
+                const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
+                const int lim = pos - jt * N;   // columns c <= lim are visible
+                // pass 1: the row max over the tile, 32 columns at a time
+                float mt = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < N / 32; ++h) {
+                    uint32_t rr[32];
+                    tc05::ld32(sb + h * 32, rr);
+                    float mx[8];   // eight independent max chains
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float v = h * 32 + c <= lim ? __uint_as_float(rr[c]) : -INFINITY;
+                        mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
+                    }
+                    mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
+                }
+                mt *= sl2;   // log2 domain (scale > 0)
+                if (j == 0) {
+                    m = mt;   // -inf when every column of the first tile is past the row
+                } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
+                    // O must hold P_{j-1} V_{j-1} before it is rescaled
+                    const bool w2 =
+                        mbar_wait_cycles(tb + 32 + ((j - 1) % SB) * 8, ((j - 1) / SB) & 1u);
+                    if (!__all_sync(0xffffffffu, w2)) {
+                        ok = false;
+                        break;
+                    }
+                    tc05::fence_after_sync();
+                    const float mn = fmaxf(m, mt);
+                    const float alpha = m == mn ? 1.f : ex2(m - mn);   // 0 when m was -inf
+                    m = mn;
+                    l *= alpha;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t rr[32];
+                        tc05::ld32(tcol + C::kOCol + c0, rr);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        tc05::st32(tcol + C::kOCol + c0, rr);
+                    }
+                }
+                // pass 2: P = exp2(scale * s - m) per 32-column chunk, written over
+                // the first N / 2 columns of S (chunk h's S has been read by then)
+                const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
+                float sm[8];   // eight independent sum chains
+#pragma unroll
+                for (int h = 0; h < N / 32; ++h) {
+                    uint32_t rr[32];
+                    tc05::ld32(sb + h * 32, rr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = h * 32 + 2 * i;
+                        const float e0 = c <= lim ? ex2(__uint_as_float(rr[2 * i]) * sl2 - mu) : 0.f;
+                        const float e1 =
+                            c + 1 <= lim ? ex2(__uint_as_float(rr[2 * i + 1]) * sl2 - mu) : 0.f;
+                        sm[i & 7] = (h == 0 && i < 8) ? e0 + e1 : sm[i & 7] + (e0 + e1);
+                        pk[i] = Mma<T>::pack(e0, e1);
+                    }
+                    tc05::st16(sb + h * 16, pk);
+                }
+                l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                tc05::wait_st();
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(tb + 16 + b * 8);   // p_full
+            }
+            if (ok) {
+                const bool w = mbar_wait_cycles(tb + 48, 0);   // o_full
+                ok = __all_sync(0xffffffffu, w);
+            }
+            if (ok) {
+                tc05::fence_after_sync();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                T *orow = static_cast<T *>(p.out) +
+                          (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) *
+                              D;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t rr[32];
-                    tc05::ld32(tmem + lane_base + C::kOCol + c0, rr);
+                    tc05::ld32(tcol + C::kOCol + c0, rr);
+                    if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                    tc05::st32(tmem + lane_base + C::kOCol + c0, rr);
-                }
-            }
-            float sm[8];   // eight independent sum chains
-            uint32_t pk[N / 2];
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                const float e0 = ex2(x[2 * i] - m), e1 = ex2(x[2 * i + 1] - m);
-                sm[i & 7] = i < 8 ? e0 + e1 : sm[i & 7] + (e0 + e1);
-                pk[i] = Mma<T>::pack(e0, e1);
-            }
-            if constexpr (N == 128) tc05::st64(sb, pk);   // P over the first N/2 columns of S
-            else tc05::st32(sb, pk);
-            l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-            tc05::wait_st();
-            tc05::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cta(p_full + b * 8);
-        }
-        if (ok) {
-            const bool w = mbar_wait_cycles(o_full, 0);
-            ok = __all_sync(0xffffffffu, w);
-        }
-        if (ok) {
-            tc05::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            T *orow = static_cast<T *>(p.out) +
-                      (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) * D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t rr[32];
-                tc05::ld32(tmem + lane_base + C::kOCol + c0, rr);
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 v;
-                        v.x = Mma<T>::pack(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
-                        v.y = Mma<T>::pack(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
-                        v.z = Mma<T>::pack(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
-                        v.w = Mma<T>::pack(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + c0 + i) = v;
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 v;
+                            v.x = Mma<T>::pack(__uint_as_float(rr[i]) * inv,
+                                               __uint_as_float(rr[i + 1]) * inv);
+                            v.y = Mma<T>::pack(__uint_as_float(rr[i + 2]) * inv,
+                                               __uint_as_float(rr[i + 3]) * inv);
+                            v.z = Mma<T>::pack(__uint_as_float(rr[i + 4]) * inv,
+                                               __uint_as_float(rr[i + 5]) * inv);
+                            v.w = Mma<T>::pack(__uint_as_float(rr[i + 6]) * inv,
+                                               __uint_as_float(rr[i + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(orow + c0 + i) = v;
+                        }
                     }
                 }
+            } else if (lane == 0) {
+                atomicOr(p.status, kWaitTimeout);
             }
-        } else if (lane == 0) {
-            atomicOr(p.status, kWaitTimeout);
         }
     }
     tc05::fence_before_sync();

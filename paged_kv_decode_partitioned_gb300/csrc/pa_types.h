@@ -9,7 +9,7 @@ namespace pa {
 
 constexpr int kTile = 16;       // tokens per pipeline tile (the MMA M of S^T)
 constexpr int kHeadsPad = 8;    // query heads per KV head, padded to the MMA N
-constexpr int kPrefillRows = 128;   // query rows (chunk token x group head) per prefill CTA
+constexpr int kPrefillRows = 128;   // largest GQA group the prefill kernel takes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s
@@ -78,7 +78,7 @@ struct PrefillParams {
     const int32_t *q_start;     // [S + 1] first chunk row of each sequence
     int *status;
     int num_seqs, num_rows, num_q_heads, num_kv_heads, group, block_size, max_blocks, num_blocks;
-    int tokens_per_cta;         // chunk tokens per CTA (128 query rows / group)
+    int tokens_per_cta;         // chunk tokens per CTA (query rows per CTA / group)
     float scale_log2;           // scale * log2(e)
 };
 
