@@ -130,6 +130,61 @@ __device__ __forceinline__ bool mbar_wait_cycles(uint32_t bar, uint32_t parity) 
     }
 }
 
+// Row max of one S tile in tensor memory (raw logits, columns c <= lim only
+// when MASK), read in 32-column chunks with the next chunk's load in flight
+// while the current one is reduced.
+template <int N, bool MASK>
+__device__ __forceinline__ float tile_row_max(uint32_t sb, int lim) {
+    uint32_t rr[2][32];
+    float mt = -INFINITY;
+    tc05::ld32_async(sb, rr[0]);
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+        tc05::wait_ld(rr[h & 1]);
+        if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
+        float mx[8];   // eight independent max chains
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float v = __uint_as_float(rr[h & 1][c]);
+            const float u = (!MASK || h * 32 + c <= lim) ? v : -INFINITY;
+            mx[c & 7] = c < 8 ? u : fmaxf(mx[c & 7], u);
+        }
+        mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
+    }
+    return mt;
+}
+
+// P = exp2(s * sl2 - mu) of one S tile (0 past lim when MASK), written as
+// 16-bit pairs over the first N / 2 columns of the tile (chunk h's S has been
+// read before its P lands on columns [16h, 16h + 16)); returns the row sum.
+template <typename T, int N, bool MASK>
+__device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, float mu) {
+    uint32_t rr[2][32];
+    float sm[8];   // eight independent sum chains
+    tc05::ld32_async(sb, rr[0]);
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+        tc05::wait_ld(rr[h & 1]);
+        if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = h * 32 + 2 * i;
+            float e0 = ex2(__uint_as_float(rr[h & 1][2 * i]) * sl2 - mu);
+            float e1 = ex2(__uint_as_float(rr[h & 1][2 * i + 1]) * sl2 - mu);
+            if (MASK) {
+                e0 = c <= lim ? e0 : 0.f;
+                e1 = c + 1 <= lim ? e1 : 0.f;
+            }
+            sm[i & 7] = (h == 0 && i < 8) ? e0 + e1 : sm[i & 7] + (e0 + e1);
+            pk[i] = Mma<T>::pack(e0, e1);
+        }
+        tc05::st16(sb + h * 16, pk);
+    }
+    return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -432,21 +487,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 const uint32_t sb = tcol + b * N;
                 const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
                 const int lim = pos - jt * N;   // columns c <= lim are visible
-                // pass 1: the row max over the tile, 32 columns at a time
-                float mt = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < N / 32; ++h) {
-                    uint32_t rr[32];
-                    tc05::ld32(sb + h * 32, rr);
-                    float mx[8];   // eight independent max chains
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float v = h * 32 + c <= lim ? __uint_as_float(rr[c]) : -INFINITY;
-                        mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
-                    }
-                    mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
-                }
+                // pass 1: the row max; tiles inside every row's window skip the mask
+                const bool full = __all_sync(0xffffffffu, lim >= N - 1);
+                float mt = full ? tile_row_max<N, false>(sb, lim) : tile_row_max<N, true>(sb, lim);
                 mt *= sl2;   // log2 domain (scale > 0)
                 if (j == 0) {
                     m = mt;   // -inf when every column of the first tile is past the row
@@ -473,27 +516,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                         tc05::st32(tcol + C::kOCol + c0, rr);
                     }
                 }
-                // pass 2: P = exp2(scale * s - m) per 32-column chunk, written over
-                // the first N / 2 columns of S (chunk h's S has been read by then)
+                // pass 2: P and its row sum
                 const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
-                float sm[8];   // eight independent sum chains
-#pragma unroll
-                for (int h = 0; h < N / 32; ++h) {
-                    uint32_t rr[32];
-                    tc05::ld32(sb + h * 32, rr);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c = h * 32 + 2 * i;
-                        const float e0 = c <= lim ? ex2(__uint_as_float(rr[2 * i]) * sl2 - mu) : 0.f;
-                        const float e1 =
-                            c + 1 <= lim ? ex2(__uint_as_float(rr[2 * i + 1]) * sl2 - mu) : 0.f;
-                        sm[i & 7] = (h == 0 && i < 8) ? e0 + e1 : sm[i & 7] + (e0 + e1);
-                        pk[i] = Mma<T>::pack(e0, e1);
-                    }
-                    tc05::st16(sb + h * 16, pk);
-                }
-                l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                l += full ? tile_row_p<T, N, false>(sb, lim, sl2, mu)
+                          : tile_row_p<T, N, true>(sb, lim, sl2, mu);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
