@@ -80,6 +80,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--check", action="store_true",
                     help="also compare sampled sequences of the output with the oracle")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0,
+                    help="minimum wall time of the warm-up (0 under a profiler, so the number "
+                         "of launches before the timed steps is exactly known)")
     ap.add_argument("--path", choices=["decode", "prefill", "moe"], default="decode",
                     help="decode (default): the paged decode step; prefill: the paged "
                          "prefix-prefill kernel; moe: router + sort-by-expert regroup + "
@@ -104,13 +107,23 @@ def qo_bytes(case) -> int:
     return 2 * case.num_seqs * w.num_q_heads * w.head_dim * 2
 
 
-def source_sha() -> str:
+# Sources each committed traffic figure depends on (a figure is dropped when
+# any of them changes).
+KERNEL_SOURCES = {
+    "decode": ["pa_kernels.cuh", "pa_launch.cuh", "pa_launch.h", "pa_types.h", "pa_inst_bf16.cu",
+               "pa_inst_f16.cu", "pa_aux.cu", "pa_api.cu", "../../include/pa_decode.h"],
+    "prefill": ["pa_prefill_tc.cuh", "pa_tc05.cuh", "pa_prefill.cu", "pa_kernels.cuh",
+                "pa_launch.cuh", "pa_types.h", "pa_api.cu", "../../include/pa_decode.h"],
+    "moe": ["pa_moe.cu", "pa_types.h", "pa_api.cu", "../../include/pa_moe.h"],
+}
+
+
+def source_sha(path: str = "decode") -> str:
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_decode_partitioned_gb300", "csrc", "*")))
-    files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    csrc = os.path.join(ROOT, "paged_kv_decode_partitioned_gb300", "csrc")
+    for name in KERNEL_SOURCES[path]:
+        with open(os.path.normpath(os.path.join(csrc, name)), "rb") as fh:
+            h.update(os.path.basename(name).encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -146,8 +159,9 @@ def committed_traffic(wid, partition_size=None):
     except (OSError, ValueError):
         return None
     key = f"workload{wid}_P{partition_size}" if partition_size is not None else wid
+    path = "decode" if partition_size is not None else str(wid).split("_")[0]
     e = d.get(key)
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(path if path in KERNEL_SOURCES else "decode"):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -375,14 +389,14 @@ def prefill_flops(ctx_lens, q_lens, num_q_heads, head_dim):
     return 4.0 * head_dim * num_q_heads * vis
 
 
-def timed_steps(launches, K, warmup, flush_l2, stream):
+def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0):
     """Run W (and at least 1 s of) warm-up steps, then K timed steps with CUDA
     events around every launch; a spin kernel holds the stream while the host
     enqueues, so no host gap falls inside a step.  Returns (per-step ms,
     per-launch mean ms, wall-clock start, end)."""
     import torch
     t_soak, n = time.time(), 0
-    while n < warmup or time.time() - t_soak < 1.0:
+    while n < warmup or time.time() - t_soak < warmup_seconds:
         flush_l2()
         for _, fn in launches:
             fn()
@@ -510,7 +524,8 @@ def run_next_path(args, rank, world, local_rank):
             pa.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
                        pc.q_start, c.scale, n, out=out)
         launches = [("prefill", run)]
-        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream)
+        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream,
+                                                 args.warmup_seconds)
         if pa.device_status() != 0:
             raise SystemExit("device status flags raised")
         flops = prefill_flops([ctx] * S, [n] * S, w.num_q_heads, w.head_dim)
@@ -590,7 +605,8 @@ def run_next_path(args, rank, world, local_rank):
             ("gather", lambda: pa.moe_gather(case.hidden, sp, K_, out=y)),
             ("scatter_back", lambda: pa.moe_scatter_back(y, pos, w, out=out)),
         ]
-        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream)
+        step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream,
+                                                 args.warmup_seconds)
         if pa.device_status() != 0:
             raise SystemExit("device status flags raised")
         row = H * 2
@@ -798,7 +814,7 @@ def main():
     # W warm-up steps, continued for at least 1 s so the clock sampler sees
     # the same load before the timed region starts.
     t_soak, n = time.time(), 0
-    while n < args.warmup or time.time() - t_soak < 1.0:
+    while n < args.warmup or time.time() - t_soak < args.warmup_seconds:
         flush_l2()
         step()
         n += 1

@@ -10,15 +10,16 @@
 //     consecutive logits in fp32 registers (a 16-byte load per lane for bf16
 //     at E = 256).  The softmax max and sum are warp reductions; the top-k
 //     are chosen on the logits themselves (softmax is monotonic), k rounds of
-//     a warp arg-max with ties to the lower expert id, so the chosen ids are
-//     exact whatever the rounding of the probabilities.
+//     a warp arg-max (two redux.sync reductions: the largest order-preserving
+//     key, then the lowest expert id holding it), so the chosen ids are exact
+//     whatever the rounding of the probabilities.
 //   * sort: a stable counting sort in three launches -- per-chunk expert
 //     histograms, one CTA turning them into each chunk's first position per
 //     expert, and a scatter in which each warp walks its share of the chunk in
 //     order, ranking equal experts inside a 32-pair step with __match_any_sync.
-//   * gather: one warp per sorted row, 16-byte loads, streaming stores (the
-//     regrouped rows are written once; the hidden rows, read K times, stay in
-//     L2).
+//   * gather: one warp per sorted row, 16-byte loads with an L2 evict-last
+//     policy and streaming stores (the regrouped rows are written once; the
+//     hidden rows, read K times at scattered moments, stay in L2).
 //   * scatter-back: index_add_ written as a gather-reduce -- one warp per
 //     token sums its K weighted rows in fp32 in slot order and rounds once, so
 //     the result is deterministic and needs no atomics.
@@ -59,6 +60,19 @@ __device__ __forceinline__ void load_logits(const TL *row, int lane, float (&x)[
     }
 }
 
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key; -0 and +0 share one key as they compare equal; every float maps to a
+// key >= 1, so 0 can mean "none").
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t u = __float_as_uint(x == 0.f ? 0.f : x);
+    const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return k == 0u ? 1u : k;
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 }  // namespace
 
 template <typename TL, int VPL>
@@ -80,31 +94,34 @@ __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
 
-    uint32_t taken = 0;     // bit i: this lane's expert lane*VPL + i already chosen
+    // Each round: the lane's best remaining logit as an order-preserving
+    // unsigned key (0 = nothing left), the warp's largest key by one redux, then
+    // the lowest expert id holding that key by a second one.
+    uint32_t key[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) key[i] = order_key(x[i]);
     int my_id = 0;          // lane r keeps the id and logit of choice r
     float my_x = 0.f;
     for (int r = 0; r < p.topk; ++r) {
-        float bv = 0.f;
-        int be = INT_MAX;
+        uint32_t bk = 0;
+        int bi = 0;
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
-            if (!(taken >> i & 1u) && (be == INT_MAX || x[i] > bv)) {
-                bv = x[i];
-                be = lane * VPL + i;
+            if (key[i] > bk) {   // strict: the lowest index wins a tie inside the lane
+                bk = key[i];
+                bi = i;
             }
+        const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t e = __reduce_min_sync(
+            0xffffffffu, bk == top ? static_cast<uint32_t>(lane * VPL + bi) : 0xffffffffu);
+        if (static_cast<int>(e) / VPL == lane) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
-            }
+            for (int i = 0; i < VPL; ++i)
+                if (i == static_cast<int>(e) % VPL) key[i] = 0;
         }
-        if (be / VPL == lane) taken |= 1u << (be % VPL);
         if (lane == r) {
-            my_id = be;
-            my_x = bv;
+            my_id = static_cast<int>(e);
+            my_x = key_value(top);
         }
     }
     float w = lane < p.topk ? expf(my_x - m) / z : 0.f;
@@ -241,6 +258,17 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortPa
 // ---------------------------------------------------------------------------
 // Gather and scatter-back
 // ---------------------------------------------------------------------------
+// 16-byte load that asks L2 to keep the line (evict-last policy): a hidden
+// row is read again for each of its K experts, spread over the whole launch,
+// while the written rows stream past it.
+__device__ __forceinline__ uint4 ld_keep(const uint4 *ptr, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(policy));
+    return v;
+}
+
 __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
@@ -257,16 +285,18 @@ __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParam
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.hidden) +
                                                        static_cast<size_t>(t) * p.row_bytes);
+    uint64_t keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
     int c = lane;
     for (; c + 96 < n16; c += 128) {   // four 16-byte chunks in flight per lane
-        const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), d = __ldg(src + c + 64),
-                    e = __ldg(src + c + 96);
+        const uint4 a = ld_keep(src + c, keep), b = ld_keep(src + c + 32, keep),
+                    d = ld_keep(src + c + 64, keep), e = ld_keep(src + c + 96, keep);
         __stcs(dst + c, a);
         __stcs(dst + c + 32, b);
         __stcs(dst + c + 64, d);
         __stcs(dst + c + 96, e);
     }
-    for (; c < n16; c += 32) __stcs(dst + c, __ldg(src + c));
+    for (; c < n16; c += 32) __stcs(dst + c, ld_keep(src + c, keep));
 }
 
 template <typename T>

@@ -66,12 +66,14 @@ def test_topk_ties_and_extremes(pa):
     x[2, 7] = 3e4                              # tie at the top
     x[3, :] = -1e30
     x[3, 200] = 0.0
+    x[3, 100] = -0.0                           # equal to +0: the lower id comes first
     for renorm in (False, True):
         w, ids = pa.topk_softmax(x.cuda(), 8, renorm)
         w_ref, ids_ref = oracle.topk_softmax(x.numpy(), 8, renorm)
         _check_router(w, ids, w_ref, ids_ref, f"ties renorm={renorm}")
     assert list(ids[0].cpu()) == list(range(8))
     assert list(ids[2].cpu()[:2]) == [7, 100]
+    assert list(ids[3].cpu()[:2]) == [100, 200]
 
 
 def _routing(T, E, K, seed):
