@@ -602,7 +602,7 @@ def run_next_path(args, rank, world, local_rank):
         launches = [
             ("topk_softmax", lambda: pa.topk_softmax(case.logits, K_, True, weights=w, ids=ids)),
             ("sort", lambda: pa.moe_sort(ids, E, workspace=ws, out=(sp, off, pos))),
-            ("gather", lambda: pa.moe_gather(case.hidden, sp, K_, out=y)),
+            ("gather", lambda: pa.moe_gather(case.hidden, pos, K_, out=y)),
             ("scatter_back", lambda: pa.moe_scatter_back(y, pos, w, out=out)),
         ]
         step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream,

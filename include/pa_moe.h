@@ -75,14 +75,20 @@ PA_API int pa_moe_sort(int32_t *sorted_pairs, int32_t *expert_offsets, int32_t *
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * pa_moe_gather -- sorted_hidden[r][:] = hidden[sorted_pairs[r] / topk][:]
- * (bit copies), so each expert's rows are contiguous.  hidden [num_tokens]
- * [hidden_size], sorted_hidden [num_pairs][hidden_size], both 16-byte
- * aligned; hidden_size * 2 bytes a multiple of 16.  A row whose pair index
- * is out of range is zeroed and flagged.  One launch.
+ * pa_moe_gather -- the hidden rows in expert-sorted order, so each expert's
+ * rows are contiguous: sorted_hidden[r][:] = hidden[t][:] for the pair
+ * p = t * topk + k placed at r = pair_pos[p] (bit copies; the same rows as
+ * sorted_hidden[r] = hidden[sorted_pairs[r] / topk]).  It runs token-major:
+ * each hidden row is read once and written to its topk positions.
+ * hidden [num_tokens][hidden_size], sorted_hidden [num_rows][hidden_size]
+ * (num_rows = the rows the output holds, num_tokens * topk when every pair is
+ * placed), both 16-byte aligned; hidden_size * 2 bytes a multiple of 16;
+ * topk <= 32.  pair_pos as written by pa_moe_sort: a pair at -1 (not placed)
+ * is skipped; a position outside [0, num_rows) is skipped and flagged.  One
+ * launch.
  */
-PA_API int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *sorted_pairs,
-                         int num_pairs, int topk, int num_tokens, int hidden_size,
+PA_API int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *pair_pos,
+                         int num_tokens, int topk, int num_rows, int hidden_size,
                          pa_dtype_t dtype, void *stream);
 
 /*

@@ -364,15 +364,17 @@ def moe_sort(expert_ids, num_experts: int, workspace: Optional[torch.Tensor] = N
     return sp, off, pos
 
 
-def moe_gather(hidden, sorted_pairs, topk: int, out: Optional[torch.Tensor] = None):
-    """Hidden rows in expert-sorted pair order (``pa_moe_gather``): [P, H]."""
+def moe_gather(hidden, pair_pos, topk: int, out: Optional[torch.Tensor] = None):
+    """Hidden rows in expert-sorted order (``pa_moe_gather``): row ``pair_pos[p]`` of
+    the result is ``hidden[p // topk]``; returns [T * topk, H]."""
     T, H = hidden.shape
-    P = sorted_pairs.numel()
+    if pair_pos.numel() != T * topk:
+        raise ValueError("pair_pos must have num_tokens * topk entries")
     if out is None:
-        out = torch.empty((P, H), dtype=hidden.dtype, device=hidden.device)
+        out = torch.empty((T * topk, H), dtype=hidden.dtype, device=hidden.device)
     with torch.cuda.device(hidden.device):
         st = _load().pa_moe_gather(_dev(out, "sorted_hidden"), _dev(hidden, "hidden"),
-                                   _i32(sorted_pairs, "sorted_pairs"), P, int(topk), T, H,
+                                   _i32(pair_pos, "pair_pos"), T, int(topk), out.shape[0], H,
                                    _dtype_code(hidden), _stream(hidden))
     _check(st, "pa_moe_gather")
     return out

@@ -717,16 +717,17 @@ int pa_moe_sort(int32_t *sorted_pairs, int32_t *expert_offsets, int32_t *pair_po
                                                                                 : PA_ERR_CUDA;
 }
 
-int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *sorted_pairs,
-                  int num_pairs, int topk, int num_tokens, int hidden_size, pa_dtype_t dtype,
+int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *pair_pos,
+                  int num_tokens, int topk, int num_rows, int hidden_size, pa_dtype_t dtype,
                   void *stream) {
-    if (num_pairs < 0 || topk <= 0 || num_tokens < 0 || hidden_size <= 0)
+    if (num_tokens < 0 || topk <= 0 || num_rows < 0 || hidden_size <= 0)
         return PA_ERR_INVALID_ARGUMENT;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
-    if ((hidden_size * 2) % 16 != 0) return PA_ERR_UNSUPPORTED;
-    if (num_pairs == 0) return PA_OK;
-    if (!sorted_hidden || !hidden || !sorted_pairs) return PA_ERR_INVALID_ARGUMENT;
-    if (!aligned(sorted_hidden, 16) || !aligned(hidden, 16) || !aligned(sorted_pairs, 4))
+    if ((hidden_size * 2) % 16 != 0 || topk > 32) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_tokens) * topk > INT_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!sorted_hidden || !hidden || !pair_pos) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(sorted_hidden, 16) || !aligned(hidden, 16) || !aligned(pair_pos, 4))
         return PA_ERR_MISALIGNED;
     DevInfo *di = nullptr;
     const int rc = device_info(&di);
@@ -734,9 +735,9 @@ int pa_moe_gather(void *sorted_hidden, const void *hidden, const int32_t *sorted
     MoeGatherParams p{};
     p.out = sorted_hidden;
     p.hidden = hidden;
-    p.sorted_pairs = sorted_pairs;
+    p.pair_pos = pair_pos;
     p.status = di->status;
-    p.num_pairs = num_pairs;
+    p.num_rows = num_rows;
     p.topk = topk;
     p.num_tokens = num_tokens;
     p.row_bytes = hidden_size * 2;

@@ -17,9 +17,10 @@
 //     histograms, one CTA turning them into each chunk's first position per
 //     expert, and a scatter in which each warp walks its share of the chunk in
 //     order, ranking equal experts inside a 32-pair step with __match_any_sync.
-//   * gather: one warp per sorted row, 16-byte loads with an L2 evict-last
-//     policy and streaming stores (the regrouped rows are written once; the
-//     hidden rows, read K times at scattered moments, stay in L2).
+//   * gather: token-major -- one warp reads a token's hidden row once and
+//     writes it to the sorted positions of the token's K pairs (streaming
+//     stores), so every hidden byte crosses DRAM once and every regrouped
+//     byte is written once.
 //   * scatter-back: index_add_ written as a gather-reduce -- one warp per
 //     token sums its K weighted rows in fp32 in slot order and rounds once, so
 //     the result is deterministic and needs no atomics.
@@ -258,45 +259,45 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortPa
 // ---------------------------------------------------------------------------
 // Gather and scatter-back
 // ---------------------------------------------------------------------------
-// 16-byte load that asks L2 to keep the line (evict-last policy): a hidden
-// row is read again for each of its K experts, spread over the whole launch,
-// while the written rows stream past it.
-__device__ __forceinline__ uint4 ld_keep(const uint4 *ptr, uint64_t policy) {
-    uint4 v;
-    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(policy));
-    return v;
-}
-
+// sorted_hidden[pair_pos[p]] = hidden[p / K], token-major: one warp reads its
+// token's row once (16-byte loads, up to 8 per lane in flight) and writes it
+// to the K sorted positions of the token's pairs with streaming stores, so
+// every hidden byte crosses DRAM once.
 __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= p.num_pairs) return;
-    const int pair = __ldg(p.sorted_pairs + r);
-    const int t = pair / p.topk;
-    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
-                                           static_cast<size_t>(r) * p.row_bytes);
-    const int n16 = p.row_bytes / 16;
-    if (pair < 0 || t >= p.num_tokens) {   // not a valid pair: the row is zeroed
-        if (lane == 0) atomicOr(p.status, kBadExpert);
-        for (int c = lane; c < n16; c += 32) __stcs(dst + c, make_uint4(0, 0, 0, 0));
-        return;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= p.num_tokens) return;
+    const int K = p.topk;
+    int my_pos = -1;   // lane k: sorted position of pair (t, k)
+    if (lane < K) {
+        my_pos = __ldg(p.pair_pos + static_cast<size_t>(t) * K + lane);
+        if (my_pos != -1 && static_cast<unsigned>(my_pos) >= static_cast<unsigned>(p.num_rows)) {
+            atomicOr(p.status, kBadExpert);   // a position outside the output: not written
+            my_pos = -1;
+        }
     }
+    const int n16 = p.row_bytes / 16;
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.hidden) +
                                                        static_cast<size_t>(t) * p.row_bytes);
-    uint64_t keep;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-    int c = lane;
-    for (; c + 96 < n16; c += 128) {   // four 16-byte chunks in flight per lane
-        const uint4 a = ld_keep(src + c, keep), b = ld_keep(src + c + 32, keep),
-                    d = ld_keep(src + c + 64, keep), e = ld_keep(src + c + 96, keep);
-        __stcs(dst + c, a);
-        __stcs(dst + c + 32, b);
-        __stcs(dst + c + 64, d);
-        __stcs(dst + c + 96, e);
+    uint4 *out = static_cast<uint4 *>(p.out);
+    for (int c0 = 0; c0 < n16; c0 += 256) {   // 8 chunks of 16 bytes per lane per round
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + i * 32 + lane;
+            if (c < n16) v[i] = __ldcs(src + c);
+        }
+        for (int k = 0; k < K; ++k) {
+            const int r = __shfl_sync(0xffffffffu, my_pos, k);
+            if (r < 0) continue;   // a pair that was not placed (flagged by the sort)
+            uint4 *dst = out + static_cast<size_t>(r) * n16;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = c0 + i * 32 + lane;
+                if (c < n16) __stcs(dst + c, v[i]);
+            }
+        }
     }
-    for (; c < n16; c += 32) __stcs(dst + c, ld_keep(src + c, keep));
 }
 
 template <typename T>
@@ -443,7 +444,7 @@ cudaError_t launch_moe_sort(const SortParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_moe_gather(const MoeGatherParams &p, cudaStream_t st) {
-    pa_moe_gather_kernel<<<(p.num_pairs + 7) / 8, 256, 0, st>>>(p);
+    pa_moe_gather_kernel<<<(p.num_tokens + 7) / 8, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -109,11 +109,11 @@ struct SortParams {
 };
 
 struct MoeGatherParams {
-    void *out;                  // [P][row_bytes]
+    void *out;                  // [num_rows][row_bytes]
     const void *hidden;         // [T][row_bytes]
-    const int32_t *sorted_pairs;
+    const int32_t *pair_pos;    // [T * topk] sorted position of each pair, -1: not placed
     int *status;
-    int num_pairs, topk, num_tokens, row_bytes;
+    int num_rows, topk, num_tokens, row_bytes;
 };
 
 struct MoeScatterParams {

@@ -186,9 +186,11 @@ def test_moe_entry_points_reject_on_host(lib):
     assert lib.pa_moe_sort(A, A, A, A, 131072, 256, A, need - 1, None) == -4
     assert lib.pa_moe_sort(A, A, A, A, 131072, 256, A + 16, need, None) == -3
     # gather / scatter-back: row size, topk, alignment
-    assert lib.pa_moe_gather(A, A, A, 100, 8, 20, 12, 1, None) == -2
-    assert lib.pa_moe_gather(A + 8, A, A, 100, 8, 20, 2048, 1, None) == -3
-    assert lib.pa_moe_gather(A, A, A, 0, 8, 20, 2048, 1, None) == 0
+    assert lib.pa_moe_gather(A, A, A, 100, 8, 800, 12, 1, None) == -2
+    assert lib.pa_moe_gather(A, A, A, 100, 33, 3300, 2048, 1, None) == -2
+    assert lib.pa_moe_gather(A + 8, A, A, 100, 8, 800, 2048, 1, None) == -3
+    assert lib.pa_moe_gather(A, A, A + 2, 100, 8, 800, 2048, 1, None) == -3
+    assert lib.pa_moe_gather(A, A, A, 0, 8, 0, 2048, 1, None) == 0
     assert lib.pa_moe_scatter_back(A, A, A, A, 16, 33, 2048, 1, None) == -2
     assert lib.pa_moe_scatter_back(A, A, A, A, 16, 8, 2044, 1, None) == -2
     assert lib.pa_moe_scatter_back(A, A, A, A, 16, 8, 2048, 3, None) == -1

@@ -130,7 +130,7 @@ def test_moe_gather_bit_exact_and_scatter_matches_oracle(pa, H, dt):
     dev = case.to("cuda")
     w, ids = pa.topk_softmax(dev.logits, K, True)
     sp, off, pos = pa.moe_sort(ids, E)
-    y = pa.moe_gather(dev.hidden, sp, K)
+    y = pa.moe_gather(dev.hidden, pos, K)
     # the reference chain runs on the oracle alone
     w_ref, ids_ref = oracle.topk_softmax(case.logits, K, True)
     rsp, roff, rpos = oracle.moe_sort(ids_ref, E)
@@ -151,7 +151,7 @@ def test_identity_expert_round_trip(pa):
     dev = case.to("cuda")
     w, ids = pa.topk_softmax(dev.logits, 8, True)
     sp, off, pos = pa.moe_sort(ids, 256)
-    out = pa.moe_scatter_back(pa.moe_gather(dev.hidden, sp, 8), pos, w)
+    out = pa.moe_scatter_back(pa.moe_gather(dev.hidden, pos, 8), pos, w)
     h = to_f64(case.hidden)
     err = np.abs(to_f64(out) - h)
     assert (err <= 2 ** -7 * np.abs(h) + 1e-30).all(), err.max()   # at most 1 bf16 ulp
@@ -168,7 +168,7 @@ def test_full_moe_batch(pa):
     rsp, roff, rpos = oracle.moe_sort(ids_ref, 256)
     assert (sp.cpu().numpy() == rsp).all() and (off.cpu().numpy() == roff).all()
     assert (pos.cpu().numpy() == rpos).all()
-    y = pa.moe_gather(dev.hidden, sp, 8)
+    y = pa.moe_gather(dev.hidden, pos, 8)
     rows = torch.randint(0, y.shape[0], (512,), generator=torch.Generator().manual_seed(1))
     y_ref = oracle.moe_gather(case.hidden, rsp[rows.numpy()], 8)
     assert (y[rows.cuda()].cpu().view(torch.int16).numpy().view(np.uint16) == y_ref).all()
@@ -182,3 +182,24 @@ def test_full_moe_batch(pa):
                              np.arange(pairs.size, dtype=np.int32), w_ref[toks], 8)
     assert_out_close(out[torch.from_numpy(toks).cuda()], ref, "full batch scatter-back")
     assert pa.device_status() == 0
+
+
+def test_moe_gather_skips_pairs_that_were_not_placed(pa):
+    """Pairs at -1 (an out-of-range expert id in the sort) write nothing; the
+    other rows are still the oracle's."""
+    T, E, K, H = 64, 16, 4, 64
+    ids = _routing(T, E, K, 4600).reshape(-1)
+    ids[5] = E            # out of range: not placed
+    hidden = torch.randn((T, H), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    sp, off, pos = pa.moe_sort(ids.cuda(), E)
+    assert pa.device_status() & pa.DEV_BAD_EXPERT
+    y = torch.full((T * K, H), 7.0, dtype=torch.bfloat16, device="cuda")
+    pa.moe_gather(hidden.cuda(), pos, K, out=y)
+    placed = int(off[-1])
+    keep = np.ones(T * K, dtype=bool)
+    keep[5] = False
+    valid = np.nonzero(keep)[0]
+    rsp, _, _ = oracle.moe_sort(ids[keep], E)
+    y_ref = oracle.moe_gather(hidden, valid[rsp].astype(np.int32), K)
+    assert (y[:placed].cpu().view(torch.int16).numpy().view(np.uint16) == y_ref).all()
+    assert bool((y[placed:] == 7.0).all())
