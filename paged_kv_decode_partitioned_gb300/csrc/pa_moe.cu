@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float z = 0.f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) z += expf(x[i] - m);
+    for (int i = 0; i < VPL; ++i) z += __expf(x[i] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
 
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p
             my_x = key_value(top);
         }
     }
-    float w = lane < p.topk ? expf(my_x - m) / z : 0.f;
+    float w = lane < p.topk ? __expf(my_x - m) / z : 0.f;
     if (p.renormalize) {
         float s = w;
 #pragma unroll
@@ -173,8 +173,10 @@ __global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
     const int e = threadIdx.x;
     const int E = p.num_experts;
     int tot = 0;
-    if (e < E)
-        for (int c = 0; c < p.num_chunks; ++c) tot += p.hist[static_cast<size_t>(c) * E + e];
+    if (e < E) {
+#pragma unroll 16
+        for (int c = 0; c < p.num_chunks; ++c) tot += __ldg(p.hist + static_cast<size_t>(c) * E + e);
+    }
     // exclusive scan of tot over the experts (block scan, <= 1024 experts)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = tot;
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
     if (e < E) {
         p.offsets[e] = start;
         int run = start;
+#pragma unroll 16
         for (int c = 0; c < p.num_chunks; ++c) {
             int *hc = p.hist + static_cast<size_t>(c) * E + e;
             const int n = *hc;
