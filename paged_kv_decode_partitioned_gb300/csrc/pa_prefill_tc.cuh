@@ -13,7 +13,7 @@
 // One CTA = NQ Q tiles of 128 query rows of one (sequence, KV head): row =
 // chunk token x query head of the GQA group, so every row of the CTA uses
 // every K/V tile it loads, and with two Q tiles each loaded K/V byte feeds
-// 256 rows.  Warp roles (64 + 128 NQ threads):
+// 256 rows.  Warp roles (64 + 256 NQ threads):
 //   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
 //              x the CTA's chunk tokens), then 64-token K and V tiles of the
 //              context through NS shared-memory stages; each lane looks up the
@@ -27,13 +27,15 @@
 //              polls its barriers and issues whichever MMA is ready, so the
 //              two tiles' MMAs fill the gaps of each other's softmax; a K
 //              (V) stage is released once every Q tile's QK (PV) has used it;
-//   warps 2..  one softmax warpgroup per Q tile, one thread per query row
-//              (its tensor-memory lane): S row -> causal mask -> scale ->
-//              running max -> exp2 -> P (bf16 or f16) written back into tensor
-//              memory; O is rescaled in tensor memory only when a row's max
-//              grows by more than 2^8 (exponents stay below 2^8 in between and
-//              the final division by the running sum is exact either way);
-//              finally O / l -> out.
+//   warps 2..  two softmax warpgroups per Q tile, each taking half of the S
+//              columns of every row (a thread per row and half, on the row's
+//              tensor-memory lane): S -> causal mask -> scale -> the half's
+//              row max, swapped with the other half's through shared memory
+//              -> exp2 -> P (bf16 or f16) written back over the half's own S
+//              columns; O is rescaled in tensor memory (each half its own O
+//              columns) only when a row's max grows by more than 2^8 (exponents
+//              stay below 2^8 in between and the final division by the running
+//              sum is exact either way); finally O / l -> out.
 // Every mbarrier wait is bounded; a role that gives up raises
 // PA_DEV_WAIT_TIMEOUT and leaves its loop, in-flight copies and MMAs are
 // waited for (bounded) and tensor memory is freed before the CTA exits.
@@ -62,7 +64,7 @@ struct PrefillTcCfg {
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
     static constexpr int kN = D <= 128 ? 128 : 64;                // cache tokens per tile
     static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
-    static constexpr int kStages = D <= 64 ? 6 : 2;
+    static constexpr int kStages = D <= 64 ? 5 : 2;
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
     static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
@@ -77,8 +79,16 @@ struct PrefillTcCfg {
     static constexpr int kTileBars = 7;
     static constexpr int kNumBars = 3 + 4 * kStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
-    static constexpr int kLaunchBytes = kSlotOffset + 16 + 1024;
-    static constexpr int kThreads = 64 + 128 * kQTiles;
+    // each Q tile's softmax runs in two warpgroups, one per half of the S
+    // columns; they swap row maxima (two buffers by tile parity) and, at the
+    // end, row sums through shared memory, synchronised by mbarriers
+    // (xbar[2] and xend per Q tile, one arrive per warp)
+    static constexpr int kHalfCols = kN / 2;
+    static constexpr int kXBarOffset = kSlotOffset + 16;
+    static constexpr int kXOffset = kXBarOffset + kQTiles * 3 * 8 + 8;
+    static constexpr int kXBytes = kQTiles * 3 * 2 * 128 * 4;   // [tile][max0, max1, sum][half][row]
+    static constexpr int kLaunchBytes = kXOffset + kXBytes + 1024;
+    static constexpr int kThreads = 64 + 256 * kQTiles;
     // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
     static constexpr int kOCol = kSBufs * kN;
     static constexpr int kTileCols = kSBufs * kN + D;
@@ -254,10 +264,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             const uint32_t tb = tile_bars + t * 56;
             for (int i = 0; i < 2; ++i) {
                 mbar_init(tb + i * 8, 1);          // s_full
-                mbar_init(tb + 16 + i * 8, 4);     // p_full: one arrive per softmax warp
+                mbar_init(tb + 16 + i * 8, 8);     // p_full: one arrive per softmax warp
                 mbar_init(tb + 32 + i * 8, 1);     // s_free
             }
             mbar_init(tb + 48, 1);                 // o_full
+            for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
         }
         fence_mbar_init();
     }
@@ -403,7 +414,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                         const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
                         for (int kt = 0; kt < N / 16; ++kt)
-                            tc05::mma_ts(tcol + C::kOCol, tcol + (j % SB) * N + kt * 8,
+                            // tokens [16 kt, 16 kt + 16) lie in half (16 kt) / (N / 2),
+                            // whose P occupies the first half of its own S columns
+                            tc05::mma_ts(tcol + C::kOCol,
+                                         tcol + (j % SB) * N +
+                                             ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
                                          tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
                                          idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
                         tc05::commit(tb + 32 + (j % SB) * 8);   // s_free
@@ -463,18 +478,24 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------ softmax ------------------------------
-        const int t = (warp - 2) >> 2;   // the Q tile of this warpgroup
+        constexpr int HC = C::kHalfCols;
+        const int idx = warp - 2;
+        const int t = idx >> 3;          // the Q tile of this warp
+        const int hf = (idx >> 2) & 1;   // the half of the S columns it handles
         if (t < nq) {
             const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
-            const int r = t * 128 + quarter * 32 + lane;
+            const int rl = quarter * 32 + lane;   // row within the Q tile
+            const int r = t * 128 + rl;
             const bool valid = r < rows_used;
             const int tq = valid ? r / g : ntok - 1, hq = valid ? r % g : 0;
             const int pos = pos_first + tq;   // last cache token this row sees
             const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
             const uint32_t tcol = tmem + lane_base + t * C::kTileCols;
             const uint32_t tb = tile_bars + t * 56;
+            const uint32_t xbar = base + C::kXBarOffset + t * 3 * 8;   // max exchange x2, sums
+            float *xch = reinterpret_cast<float *>(smem + C::kXOffset) + t * 3 * 256;
             const float sl2 = p.scale_log2;
-            float m = -INFINITY, l = 0.f;
+            float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
             bool ok = true;
             for (int j = 0; j < ntiles; ++j) {
                 const int b = j % SB;
@@ -484,17 +505,26 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     break;
                 }
                 tc05::fence_after_sync();
-                const uint32_t sb = tcol + b * N;
+                const uint32_t sb = tcol + b * N + hf * HC;   // this half's S columns
                 const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
-                const int lim = pos - jt * N;   // columns c <= lim are visible
-                // pass 1: the row max; tiles inside every row's window skip the mask
-                const bool full = __all_sync(0xffffffffu, lim >= N - 1);
-                float mt = full ? tile_row_max<N, false>(sb, lim) : tile_row_max<N, true>(sb, lim);
+                const int lim = pos - jt * N - hf * HC;   // own columns c <= lim are visible
+                // pass 1: this half's row max, swapped with the other half's
+                const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
+                const float pm = full ? tile_row_max<HC, false>(sb, lim) : tile_row_max<HC, true>(sb, lim);
+                xch[(j & 1) * 256 + hf * 128 + rl] = pm;
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
+                if (!__all_sync(0xffffffffu, mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
+                    ok = false;
+                    break;
+                }
+                float mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                 mt *= sl2;   // log2 domain (scale > 0)
                 if (j == 0) {
                     m = mt;   // -inf when every column of the first tile is past the row
                 } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
-                    // O must hold P_{j-1} V_{j-1} before it is rescaled
+                    // O must hold P_{j-1} V_{j-1} before it is rescaled (both halves
+                    // see the same maxima, so both take this branch for a row)
                     const bool w2 =
                         mbar_wait_cycles(tb + 32 + ((j - 1) % SB) * 8, ((j - 1) / SB) & 1u);
                     if (!__all_sync(0xffffffffu, w2)) {
@@ -507,23 +537,31 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     m = mn;
                     l *= alpha;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {   // this half's O columns
                         uint32_t rr[32];
-                        tc05::ld32(tcol + C::kOCol + c0, rr);
+                        const uint32_t oc = tcol + C::kOCol + hf * (D / 2) + c0;
+                        tc05::ld32(oc, rr);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                        tc05::st32(tcol + C::kOCol + c0, rr);
+                        tc05::st32(oc, rr);
                     }
                 }
-                // pass 2: P and its row sum
+                // pass 2: P of this half over the first half of its own S columns
                 const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
-                l += full ? tile_row_p<T, N, false>(sb, lim, sl2, mu)
-                          : tile_row_p<T, N, true>(sb, lim, sl2, mu);
+                l += full ? tile_row_p<T, HC, false>(sb, lim, sl2, mu)
+                          : tile_row_p<T, HC, true>(sb, lim, sl2, mu);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(tb + 16 + b * 8);   // p_full
+            }
+            if (ok) {   // the row sum is the two halves' shares
+                xch[2 * 256 + hf * 128 + rl] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(xbar + 16);
+                ok = __all_sync(0xffffffffu, mbar_wait_cycles(xbar + 16, 0));
+                if (ok) l += xch[2 * 256 + (1 - hf) * 128 + rl];
             }
             if (ok) {
                 const bool w = mbar_wait_cycles(tb + 48, 0);   // o_full
@@ -534,11 +572,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 T *orow = static_cast<T *>(p.out) +
                           (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) *
-                              D;
+                              D + hf * (D / 2);
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {   // this half's output columns
                     uint32_t rr[32];
-                    tc05::ld32(tcol + C::kOCol + c0, rr);
+                    tc05::ld32(tcol + C::kOCol + hf * (D / 2) + c0, rr);
                     if (valid) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) {
