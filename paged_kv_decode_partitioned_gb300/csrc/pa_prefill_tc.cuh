@@ -431,11 +431,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                         ++pv[t];
                         progress = true;
                     }
-                    // QK of the next tile; S buffer j % SB is free once PV of j - SB is done
+                    // QK of the next tile into S buffer j % SB, whose P the PV of
+                    // j - SB reads: that PV only has to be issued, not finished,
+                    // since this thread's MMAs run on the tensor pipe in issue
+                    // order (the QK's writes come after the PV's operand reads)
                     j = qk[t];
                     if (j < ntiles && j <= pv[t] + SB - 1 &&
-                        mbar_test(k_full + (j % NS) * 8, (j / NS) & 1u) &&
-                        (j < SB || mbar_test(tb + 32 + (j % SB) * 8, ((j - SB) / SB) & 1u))) {
+                        mbar_test(k_full + (j % NS) * 8, (j / NS) & 1u)) {
                         tc05::fence_after_sync();
                         const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
                         const uint32_t qst = q_smem + t * C::kQTileBytes;

@@ -206,3 +206,31 @@ def test_max_q_len_too_small_raises_flag(pa):
                c.scale, 16, out=out)
     assert pa.device_status() & pa.DEV_LEN_CLAMPED
     assert_out_close(out[:16], _oracle(host)[:16], "rows covered by max_q_len")
+
+
+@pytest.mark.parametrize("name", ["chunk2048_ctx16384_x16", "full100k_x1"])
+def test_bench_prefill_workloads_sampled(pa, name):
+    """The bench's prefill workloads at full size, in the bench's launch, checked on
+    sampled rows (first, last and random rows of a few sequences) against the oracle."""
+    import bench
+    pc, (ctx, n, S) = bench.make_prefill_inputs(name, "cuda")
+    c = pc.case
+    out = pa.prefill(pc.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                     pc.q_start, c.scale, n)
+    assert pa.device_status() == 0
+    g = torch.Generator().manual_seed(17)
+    seqs = sorted({0, S - 1} | set(torch.randint(0, S, (2,), generator=g).tolist()))
+    for s in seqs:
+        L = c.seq_lens_list[s]
+        nblk = -(-L // c.key_cache.shape[1])
+        blocks = c.block_tables[s, :nblk].long()
+        kc = c.key_cache.index_select(0, blocks).cpu()
+        vc = c.value_cache.index_select(0, blocks).cpu()
+        bt = torch.arange(nblk, dtype=torch.int32)[None, :]
+        rows = sorted({0, n - 1} | set(torch.randint(0, n, (3,), generator=g).tolist()))
+        for i in rows:
+            r = s * n + i
+            p = L - n + i
+            ref = oracle.attention(pc.query[r:r + 1].cpu(), kc, vc, bt,
+                                   torch.tensor([p + 1], dtype=torch.int32), c.scale)
+            assert_out_close(out[r:r + 1], ref, f"{name}: row {i} of sequence {s}")
