@@ -406,10 +406,17 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     busy |= pv[t] < ntiles;
                     const uint32_t tb = tile_bars + t * 56;
                     const uint32_t tcol = tmem + t * C::kTileCols;
+                    // The tile's three barrier tests go out together, so their
+                    // shared-memory latencies overlap (this thread alone feeds the
+                    // tensor pipe: time spent here is time the pipe may idle).  A
+                    // test of an index past the loop's end is ignored.
+                    const int jp = pv[t], jq = qk[t];
+                    const bool p_ok = mbar_test(tb + 16 + (jp % SB) * 8, (jp / SB) & 1u);
+                    const bool v_ok = mbar_test(v_full + (jp % NS) * 8, (jp / NS) & 1u);
+                    const bool k_ok = mbar_test(k_full + (jq % NS) * 8, (jq / NS) & 1u);
                     // PV of the oldest tile whose P is ready
-                    int j = pv[t];
-                    if (j < qk[t] && mbar_test(tb + 16 + (j % SB) * 8, (j / SB) & 1u) &&
-                        mbar_test(v_full + (j % NS) * 8, (j / NS) & 1u)) {
+                    int j = jp;
+                    if (j < jq && p_ok && v_ok) {
                         tc05::fence_after_sync();
                         const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
@@ -435,9 +442,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     // j - SB reads: that PV only has to be issued, not finished,
                     // since this thread's MMAs run on the tensor pipe in issue
                     // order (the QK's writes come after the PV's operand reads)
-                    j = qk[t];
-                    if (j < ntiles && j <= pv[t] + SB - 1 &&
-                        mbar_test(k_full + (j % NS) * 8, (j / NS) & 1u)) {
+                    j = jq;
+                    if (j < ntiles && j <= pv[t] + SB - 1 && k_ok) {
                         tc05::fence_after_sync();
                         const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
                         const uint32_t qst = q_smem + t * C::kQTileBytes;
