@@ -428,7 +428,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                                              ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
                                          tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
                                          idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
-                        tc05::commit(tb + 32 + (j % SB) * 8);   // s_free
+                        // s_free: with one S buffer the commit of the QK issued next
+                        // (S_{j+1}) tracks this PV as well, so none is needed
+                        if (SB > 1) tc05::commit(tb + 32 + (j % SB) * 8);
                         bool last_user = true;   // the V stage is free once every tile used it
 #pragma unroll
                         for (int u = 0; u < NQ; ++u)
@@ -532,14 +534,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     m = mt;   // -inf when every column of the first tile is past the row
                 } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
                     // O must hold P_{j-1} V_{j-1} before it is rescaled (both halves
-                    // see the same maxima, so both take this branch for a row)
-                    const bool w2 =
-                        mbar_wait_cycles(tb + 32 + ((j - 1) % SB) * 8, ((j - 1) / SB) & 1u);
-                    if (!__all_sync(0xffffffffu, w2)) {
-                        ok = false;
-                        break;
+                    // see the same maxima, so both take this branch for a row).  With
+                    // one S buffer, PV_{j-1} went out before QK_j from the same thread,
+                    // so the S_j commit waited for above has already seen it finish.
+                    if (SB > 1) {
+                        const bool w2 =
+                            mbar_wait_cycles(tb + 32 + ((j - 1) % SB) * 8, ((j - 1) / SB) & 1u);
+                        if (!__all_sync(0xffffffffu, w2)) {
+                            ok = false;
+                            break;
+                        }
+                        tc05::fence_after_sync();
                     }
-                    tc05::fence_after_sync();
                     const float mn = fmaxf(m, mt);
                     const float alpha = m == mn ? 1.f : ex2(m - mn);   // 0 when m was -inf
                     m = mn;
