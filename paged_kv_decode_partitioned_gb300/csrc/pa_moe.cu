@@ -74,13 +74,114 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// 16-bit logits (bf16, f16): the same order-preserving map on the raw bits
+// (-0 and +0 share a key), and its inverse.
+__device__ __forceinline__ uint32_t order_key16(uint32_t h) {
+    h = h == 0x8000u ? 0u : h;
+    return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+}
+__device__ __forceinline__ uint32_t key16_bits(uint32_t k) {
+    return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+}
+__device__ __forceinline__ float bits16_f32(uint32_t h, __nv_bfloat16) { return __uint_as_float(h << 16); }
+__device__ __forceinline__ float bits16_f32(uint32_t h, __half) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// VPL consecutive 16-bit logits of one lane as raw bits.
+template <int VPL>
+__device__ __forceinline__ void load_bits16(const uint16_t *row, int lane, uint32_t (&h)[VPL]) {
+    const uint16_t *src = row + lane * VPL;
+    if constexpr (VPL % 8 == 0) {
+#pragma unroll
+        for (int c = 0; c < VPL / 8; ++c) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[c * 8 + 2 * i] = w[i] & 0xffffu;
+                h[c * 8 + 2 * i + 1] = w[i] >> 16;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) h[i] = __ldg(src + i);
+    }
+}
+
+// Descending bitonic sort of n (a power of two) keys in registers.
+template <int n>
+__device__ __forceinline__ void sort_desc(uint32_t (&v)[n]) {
+#pragma unroll
+    for (int k = 2; k <= n; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint32_t a = v[i], b = v[l];
+                    const bool desc = (i & k) == 0;
+                    v[i] = desc ? max(a, b) : min(a, b);
+                    v[l] = desc ? min(a, b) : max(a, b);
+                }
+            }
+}
+
 }  // namespace
+
+// Router for 16-bit logits.  A logit's order key takes 16 bits, so key and
+// expert id pack into one u32, (key << 16) | (0xffff - id): the largest packed
+// value is the largest logit and, among equal logits, the lowest id.  Each lane
+// sorts its packed values once; a round is then one warp max of the lanes'
+// heads, and the lane whose head won moves to its next value.  The row max of
+// the softmax is the first round's winner, and with renormalisation the sum
+// over all experts cancels, so only the top-k exponentials are taken.
+template <typename TL, int VPL>
+__device__ __forceinline__ void topk_softmax_16(const TopkParams &p, int t, int lane) {
+    constexpr int E = VPL * 32;
+    uint32_t h[VPL], v[VPL];
+    load_bits16<VPL>(static_cast<const uint16_t *>(p.logits) + static_cast<size_t>(t) * E, lane, h);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        v[i] = (order_key16(h[i]) << 16) | (0xffffu - static_cast<uint32_t>(lane * VPL + i));
+    if constexpr (VPL > 1) sort_desc<VPL>(v);
+    uint32_t mine = 0u, first = 0u;   // lane r keeps the winner of round r
+    for (int r = 0; r < p.topk; ++r) {
+        const uint32_t top = __reduce_max_sync(0xffffffffu, v[0]);
+        if (r == 0) first = top;
+        if (lane == r) mine = top;
+        const bool own = v[0] == top;   // packed values are unique
+#pragma unroll
+        for (int i = 0; i + 1 < VPL; ++i) v[i] = own ? v[i + 1] : v[i];
+        v[VPL - 1] = own ? 0u : v[VPL - 1];
+    }
+    const float m = bits16_f32(key16_bits(first >> 16), TL());
+    float w = lane < p.topk ? __expf(bits16_f32(key16_bits(mine >> 16), TL()) - m) : 0.f;
+    float s = 0.f;   // the normaliser: the top-k's exponentials, or every expert's
+    if (p.renormalize) {
+        s = w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) s += __expf(bits16_f32(h[i], TL()) - m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane < p.topk) {
+        p.weights[static_cast<size_t>(t) * p.topk + lane] = w / s;
+        p.ids[static_cast<size_t>(t) * p.topk + lane] = static_cast<int>(0xffffu - (mine & 0xffffu));
+    }
+}
 
 template <typename TL, int VPL>
 __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.num_tokens) return;
+    if constexpr (sizeof(TL) == 2) {
+        topk_softmax_16<TL, VPL>(p, t, lane);
+        return;
+    }
     constexpr int E = VPL * 32;
     float x[VPL];
     load_logits<TL, VPL>(static_cast<const TL *>(p.logits) + static_cast<size_t>(t) * E, lane, x);

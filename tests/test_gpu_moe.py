@@ -76,6 +76,34 @@ def test_topk_ties_and_extremes(pa):
     assert list(ids[3].cpu()[:2]) == [100, 200]
 
 
+@pytest.mark.parametrize("ldt", [torch.bfloat16, torch.float16])
+def test_topk_ties_and_extremes_16bit(pa, ldt):
+    """The 16-bit router: all-equal rows, pairs of equal logits, a tie at the
+    top, -0 against +0, the largest finite and most negative values, and a row
+    whose top-k spans all 32 lanes' first choices."""
+    big = 3.0e38 if ldt == torch.bfloat16 else 65504.0
+    x = torch.zeros((6, 256), dtype=torch.float32)
+    x[1, :] = torch.arange(256) // 2
+    x[2, 100] = 30.0
+    x[2, 7] = 30.0
+    x[3, :] = -big
+    x[3, 200] = 0.0
+    x[3, 100] = -0.0
+    x[4, :] = -5.0
+    x[4, 255] = big
+    x[5, :] = -(torch.arange(256) % 8).float()   # every lane's first logit is 0
+    xl = x.to(ldt)
+    for renorm in (False, True):
+        w, ids = pa.topk_softmax(xl.cuda(), 8, renorm)
+        w_ref, ids_ref = oracle.topk_softmax(xl, 8, renorm)
+        _check_router(w, ids, w_ref, ids_ref, f"16-bit ties renorm={renorm}")
+    assert list(ids[0].cpu()) == list(range(8))
+    assert list(ids[2].cpu()[:2]) == [7, 100]
+    assert list(ids[3].cpu()[:2]) == [100, 200]
+    assert list(ids[5].cpu()) == [8 * i for i in range(8)]
+    assert pa.device_status() == 0
+
+
 def _routing(T, E, K, seed):
     g = torch.Generator().manual_seed(seed)
     return torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)]).to(torch.int32)
