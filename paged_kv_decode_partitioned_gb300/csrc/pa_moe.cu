@@ -404,6 +404,9 @@ __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParam
     }
 }
 
+// 16-byte columns (8 elements) of a scatter-back work unit: 1 KB of a row
+constexpr int kScatterBlock = 64;
+
 template <typename T>
 struct Vec8;
 template <>
@@ -449,8 +452,15 @@ struct Vec8<__half> {
 template <typename T>
 __global__ void __launch_bounds__(256) pa_moe_scatter_kernel(const MoeScatterParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= p.num_tokens) return;
+    // one warp per (token, 1 KB block of columns): a warp per whole token gave
+    // 1.7 waves of warps at 16384 tokens, whose partial last wave left the
+    // DRAM under-used for a sixth of the launch
+    const int n16 = p.hidden_size / 8;
+    const int nblk = (n16 + kScatterBlock - 1) / kScatterBlock;
+    const long long u = static_cast<long long>(blockIdx.x) * 8 + warp;
+    if (u >= static_cast<long long>(p.num_tokens) * nblk) return;
+    const int t = static_cast<int>(u / nblk);
+    const int cb = static_cast<int>(u % nblk) * kScatterBlock;
     const int K = p.topk;
     int my_pos = 0;
     float my_w = 0.f;
@@ -462,14 +472,14 @@ __global__ void __launch_bounds__(256) pa_moe_scatter_kernel(const MoeScatterPar
             my_pos = -1;
         }
     }
-    const int n16 = p.hidden_size / 8;
     const uint4 *y = static_cast<const uint4 *>(p.y);
     uint4 *out = static_cast<uint4 *>(p.out) + static_cast<size_t>(t) * n16;
     // the column loop is uniform over the warp: every lane takes part in the
     // shuffles that broadcast the K (row, weight) pairs
-    for (int c0 = 0; c0 < n16; c0 += 64) {
+    const int cend = min(cb + kScatterBlock, n16);
+    for (int c0 = cb; c0 < cend; c0 += 64) {
         const int c = c0 + lane;
-        const bool one = c < n16, two = c + 32 < n16;
+        const bool one = c < cend, two = c + 32 < cend;
         float a0[8], a1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) a0[i] = a1[i] = 0.f;
@@ -553,7 +563,11 @@ cudaError_t launch_moe_gather(const MoeGatherParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_moe_scatter(bool bf16, const MoeScatterParams &p, cudaStream_t st) {
-    const dim3 grid((p.num_tokens + 7) / 8);
+    const long long nblk = (p.hidden_size / 8 + kScatterBlock - 1) / kScatterBlock;
+    const long long units = static_cast<long long>(p.num_tokens) * nblk;
+    if (units == 0) return cudaSuccess;
+    if ((units + 7) / 8 > INT_MAX) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>((units + 7) / 8));
     if (bf16)
         pa_moe_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
     else
