@@ -270,46 +270,78 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_hist_kernel(const SortPar
 // One CTA: hist[c][e] becomes the first sorted position of chunk c's pairs of
 // expert e; offsets[e] the first position of expert e, offsets[E] the total.
 __global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
+    __shared__ int part[1024];    // [group][expert] chunk sums
+    __shared__ int first[1024];   // [expert] first sorted position
     __shared__ int warp_sum[32];
-    const int e = threadIdx.x;
-    const int E = p.num_experts;
-    int tot = 0;
-    if (e < E) {
-#pragma unroll 16
-        for (int c = 0; c < p.num_chunks; ++c) tot += __ldg(p.hist + static_cast<size_t>(c) * E + e);
+    // thread = (chunk group g, expert e): the chunks are split over the
+    // 1024 / E groups, so every thread walks only its share of the columns
+    const int E = p.num_experts, C = p.num_chunks;
+    const int G = 1024 / E;
+    const int g = threadIdx.x / E, e = threadIdx.x - g * E;
+    const bool act = g < G;
+    const int per = (C + G - 1) / G;
+    const int c_begin = act ? min(g * per, C) : 0, c_end = act ? min(c_begin + per, C) : 0;
+    constexpr int kBatch = 16;   // loads issued together, ahead of any use
+    int sum = 0;
+    for (int c0 = c_begin; c0 < c_end; c0 += kBatch) {
+        int v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            v[i] = c0 + i < c_end ? p.hist[static_cast<size_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) sum += v[i];
     }
-    // exclusive scan of tot over the experts (block scan, <= 1024 experts)
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    int pre = 0, tot = 0;   // this group's offset within expert e, and e's total
+    if (act) {
+        for (int q = 0; q < G; ++q) {
+            const int x = part[q * E + e];
+            pre += q < g ? x : 0;
+            tot += x;
+        }
+    }
+    // exclusive scan of the totals over the experts (threads 0 .. E-1)
+    const int val = g == 0 ? tot : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = tot;
+    int incl = val;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
     }
     if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int s = warp_sum[lane];
+        int w = warp_sum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += v;
+            const int x = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += x;
         }
-        warp_sum[lane] = s;   // inclusive over warps
+        warp_sum[lane] = w;   // inclusive over warps
     }
     __syncthreads();
-    const int start = incl - tot + (warp > 0 ? warp_sum[warp - 1] : 0);
-    if (e < E) {
+    if (g == 0) {
+        const int start = incl - val + (warp > 0 ? warp_sum[warp - 1] : 0);
+        first[e] = start;
         p.offsets[e] = start;
-        int run = start;
-#pragma unroll 16
-        for (int c = 0; c < p.num_chunks; ++c) {
-            int *hc = p.hist + static_cast<size_t>(c) * E + e;
-            const int n = *hc;
-            *hc = run;
-            run += n;
+        if (e == E - 1) p.offsets[E] = start + tot;
+    }
+    __syncthreads();
+    if (act) {   // hist[c][e] becomes the first position of chunk c's pairs of e
+        int run = first[e] + pre;
+        for (int c0 = c_begin; c0 < c_end; c0 += kBatch) {
+            int v[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                v[i] = c0 + i < c_end ? p.hist[static_cast<size_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (c0 + i < c_end) p.hist[static_cast<size_t>(c0 + i) * E + e] = run;
+                run += v[i];
+            }
         }
-        if (e == E - 1) p.offsets[E] = run;
     }
 }
 
