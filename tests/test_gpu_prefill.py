@@ -234,3 +234,49 @@ def test_bench_prefill_workloads_sampled(pa, name):
             ref = oracle.attention(pc.query[r:r + 1].cpu(), kc, vc, bt,
                                    torch.tensor([p + 1], dtype=torch.int32), c.scale)
             assert_out_close(out[r:r + 1], ref, f"{name}: row {i} of sequence {s}")
+
+
+def _ramped_keys(pc, rate_log2, seed, spike=None):
+    """Rewrite the case so a row's running max grows along the context: every
+    query of KV head h is a * u_h and the key at position t is b * t * u_h (u_h a
+    unit vector) plus small noise, with a * b chosen so the logit rises by
+    ``rate_log2`` (log2 units) every 128 positions.  ``spike`` = (position,
+    log2 logit) puts one much larger key at that position."""
+    c = pc.case
+    w = c.workload
+    D, Hkv, g = w.head_dim, w.num_kv_heads, w.num_q_heads // w.num_kv_heads
+    gen = torch.Generator().manual_seed(seed)
+    u = torch.randn((Hkv, D), generator=gen, dtype=torch.float64)
+    u /= u.norm(dim=1, keepdim=True)
+    sl2 = c.scale * 1.4426950408889634
+    a = 4.0
+    b = rate_log2 / (128.0 * sl2 * a)
+    q = (a * u).repeat_interleave(g, dim=0)                      # [Hq, D]
+    pc.query.copy_((q[None] + 0.01 * torch.randn((pc.query.shape[0], w.num_q_heads, D),
+                                                 generator=gen, dtype=torch.float64)).to(w.dtype))
+    bs = c.key_cache.shape[1]
+    for s, L in enumerate(c.seq_lens_list):
+        t = torch.arange(L, dtype=torch.float64)
+        k = b * t[:, None, None] * u[None] + 0.01 * torch.randn((L, Hkv, D), generator=gen,
+                                                              dtype=torch.float64)
+        if spike is not None and spike[0] < L:
+            k[spike[0]] = (spike[1] / (sl2 * a)) * u
+        blocks = c.block_tables[s, (torch.arange(L) // bs)].long()
+        c.key_cache[blocks, torch.arange(L) % bs] = k.to(w.dtype)
+
+
+@pytest.mark.parametrize("D,rate,spike", [
+    (128, 12.0, None), (128, 5.0, None), (64, 12.0, None), (256, 12.0, None),
+    (128, 0.5, (1200, 60.0)), (256, 0.5, (700, 60.0)),
+])
+def test_prefill_running_max_rescales(pa, D, rate, spike):
+    """The O rescale path: the row max grows by more than 2^8 from one K/V tile to
+    the next (rate 12 per 128 positions: a rescale at every tile the walk meets in
+    increasing order; rate 5: every second one), or once by a large spike in the
+    middle of the context.  Every row is checked against the oracle."""
+    w = _workload(24, 4, D, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[1700, 900], q_lens=[300, 77], seed=3500 + D)
+    _ramped_keys(host, rate, seed=3600 + D, spike=spike)
+    out = _run(pa, host.to("cuda"))
+    assert pa.device_status() == 0
+    assert_out_close(out, _oracle(host), f"rescaled prefill D={D} rate={rate} spike={spike}")
