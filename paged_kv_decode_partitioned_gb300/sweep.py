@@ -115,7 +115,7 @@ def run(reps: int = 20, seqs=SEQS, lens=LENS, parts=PARTS, hq=24, hkv=4, d=128, 
 def markdown(rows, parts=PARTS):
     head = "| seqs | seq_len | single ms | " + " | ".join(f"P={P} ms" for P in parts) + \
         " | best | best GB/s | auto ms (threshold) | auto GB/s |"
-    sep = "|" + "---|" * (6 + len(parts))
+    sep = "|" + "---|" * (7 + len(parts))
     lines = [head, sep]
     for r in rows:
         lines.append(f"| {r['num_seqs']} | {r['seq_len']} | {r['single']} | " +
