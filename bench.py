@@ -390,10 +390,13 @@ def prefill_flops(ctx_lens, q_lens, num_q_heads, head_dim):
 
 
 def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0):
-    """Run W (and at least 1 s of) warm-up steps, then K timed steps with CUDA
-    events around every launch; a spin kernel holds the stream while the host
-    enqueues, so no host gap falls inside a step.  Returns (per-step ms,
-    per-launch mean ms, wall-clock start, end)."""
+    """Run W (and at least 1 s of) warm-up steps, then K timed steps, each
+    bracketed by its own two CUDA events; a spin kernel holds the stream while
+    the host enqueues, so no host gap falls inside a step.  Per-launch times
+    come from a second pass of K steps with an event after every launch (an
+    event between two launches costs the step ~1 us, so the timed steps carry
+    none).  Returns (per-step ms, per-launch mean ms, wall-clock start, end of
+    the timed steps)."""
     import torch
     t_soak, n = time.time(), 0
     while n < warmup or time.time() - t_soak < warmup_seconds:
@@ -411,20 +414,32 @@ def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0):
             fn()
     host_step = (time.perf_counter() - t0) / 4
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
-          for _ in range(K)]
-    torch.cuda._sleep(int(min(2.0, 1.5 * K * host_step + 0.005) * 2.2e9))
+    hold = int(min(2.0, 1.5 * K * host_step + 0.005) * 2.2e9)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda._sleep(hold)
     w0 = time.time()
     for k in range(K):
         flush_l2(k)
         ev[k][0].record(stream)
-        for j, (_, fn) in enumerate(launches):
+        for _, fn in launches:
             fn()
-            ev[k][j + 1].record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
-    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
-    launch_ms = {name: sum(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)) / K
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    if len(launches) == 1:
+        return step_ms, {launches[0][0]: sum(step_ms) / K}, w0, w1
+    lev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+           for _ in range(K)]
+    torch.cuda._sleep(hold)
+    for k in range(K):
+        flush_l2(k)
+        lev[k][0].record(stream)
+        for j, (_, fn) in enumerate(launches):
+            fn()
+            lev[k][j + 1].record(stream)
+    torch.cuda.synchronize()
+    launch_ms = {name: sum(lev[k][j].elapsed_time(lev[k][j + 1]) for k in range(K)) / K
                  for j, (name, _) in enumerate(launches)}
     return step_ms, launch_ms, w0, w1
 
@@ -825,8 +840,7 @@ def main():
         raise SystemExit("device status flags raised during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
-          for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     # Host cost of enqueuing one step (flush + launches + events), measured
     # while the GPU is busy, sizes the stream hold below.
     t0 = time.perf_counter()
@@ -846,24 +860,41 @@ def main():
 
     hold_stream(K)
     t_wall0 = time.time()
-    for k in range(K):
+    for k in range(K):   # the timed steps: each step's own two events only
         flush_l2(k)
         ev[k][0].record(stream)
-        for j, (_, fn) in enumerate(launches):
+        for _, fn in launches:
             fn()
-            ev[k][j + 1].record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
     rows = sampler.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
 
+    # Per-launch times from a second pass with an event after every launch (an
+    # event between two launches costs the step ~1 us, so the timed steps carry
+    # none); with one launch per step the timed steps give it directly.
     names = [name for name, _ in launches]
     attn_idx = names.index("attention")
-    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(K)]
-    attn_ms = [ev[k][attn_idx].elapsed_time(ev[k][attn_idx + 1]) for k in range(K)]
-    # mean event time of each launch of the step (includes the gap before it)
-    launch_ms = {n: round(sum(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)) / K, 4)
-                 for j, n in enumerate(names)}
+    if len(launches) == 1:
+        attn_ms = step_ms
+        launch_ms = {names[0]: round(sum(step_ms) / K, 4)}
+    else:
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+               for _ in range(K)]
+        hold_stream(K)
+        for k in range(K):
+            flush_l2(k)
+            lev[k][0].record(stream)
+            for j, (_, fn) in enumerate(launches):
+                fn()
+                lev[k][j + 1].record(stream)
+        torch.cuda.synchronize()
+        attn_ms = [lev[k][attn_idx].elapsed_time(lev[k][attn_idx + 1]) for k in range(K)]
+        # mean event time of each launch of the step (includes the gap before it)
+        launch_ms = {n: round(sum(lev[k][j].elapsed_time(lev[k][j + 1]) for k in range(K)) / K, 4)
+                     for j, n in enumerate(names)}
     kvb = kv_bytes(case)
     (total_ms,), (kvb_all, seqs_all) = across_ranks(world, "cuda", [sum(step_ms)],
                                                     [kvb, case.num_seqs])
