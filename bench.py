@@ -389,20 +389,40 @@ def prefill_flops(ctx_lens, q_lens, num_q_heads, head_dim):
     return 4.0 * head_dim * num_q_heads * vis
 
 
-def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0):
+def graph_of(launches, stream):
+    """The step's launches captured once into a CUDA graph (warmed up first on a
+    side stream, as capture requires); returns its replay function."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _, fn in launches:
+            fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _, fn in launches:
+            fn()
+    torch.cuda.synchronize()
+    return g.replay
+
+
+def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0, step_fn=None):
     """Run W (and at least 1 s of) warm-up steps, then K timed steps, each
     bracketed by its own two CUDA events; a spin kernel holds the stream while
     the host enqueues, so no host gap falls inside a step.  Per-launch times
     come from a second pass of K steps with an event after every launch (an
     event between two launches costs the step ~1 us, so the timed steps carry
-    none).  Returns (per-step ms, per-launch mean ms, wall-clock start, end of
-    the timed steps)."""
+    none).  ``step_fn`` (a CUDA-graph replay of the launches) runs the step in
+    the warm-up and the timed steps when given.  Returns (per-step ms,
+    per-launch mean ms, wall-clock start, end of the timed steps)."""
     import torch
+    run_step = step_fn if step_fn is not None else (lambda: [fn() for _, fn in launches])
     t_soak, n = time.time(), 0
     while n < warmup or time.time() - t_soak < warmup_seconds:
         flush_l2()
-        for _, fn in launches:
-            fn()
+        run_step()
         n += 1
         if n % 16 == 0:
             torch.cuda.synchronize()
@@ -421,8 +441,7 @@ def timed_steps(launches, K, warmup, flush_l2, stream, warmup_seconds=1.0):
     for k in range(K):
         flush_l2(k)
         ev[k][0].record(stream)
-        for _, fn in launches:
-            fn()
+        run_step()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -620,8 +639,10 @@ def run_next_path(args, rank, world, local_rank):
             ("gather", lambda: pa.moe_gather(case.hidden, pos, K_, out=y)),
             ("scatter_back", lambda: pa.moe_scatter_back(y, pos, w, out=out)),
         ]
+        # the step's six kernels replay as one CUDA graph (no launch gaps from the host)
+        replay = graph_of(launches, stream)
         step_ms, launch_ms, w0, w1 = timed_steps(launches, K, args.warmup, flush_l2, stream,
-                                                 args.warmup_seconds)
+                                                 args.warmup_seconds, step_fn=replay)
         if pa.device_status() != 0:
             raise SystemExit("device status flags raised")
         row = H * 2
@@ -664,6 +685,7 @@ def run_next_path(args, rank, world, local_rank):
                        "global_batch": T * world,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed between steps (outside the events)",
+                       "launch": "the step's 6 kernels replayed as one CUDA graph",
                        "expert": "identity (the expert GEMMs need trained weights; not built)"},
             "tokens_per_s": round(t_all / (ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "kernel": "pa_moe_gather_kernel",
