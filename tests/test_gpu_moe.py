@@ -231,3 +231,47 @@ def test_moe_gather_skips_pairs_that_were_not_placed(pa):
     y_ref = oracle.moe_gather(hidden, valid[rsp].astype(np.int32), K)
     assert (y[:placed].cpu().view(torch.int16).numpy().view(np.uint16) == y_ref).all()
     assert bool((y[placed:] == 7.0).all())
+
+
+def test_moe_chain_replays_in_a_cuda_graph(pa):
+    """The whole chain (router, sort, gather, scatter-back) captured once into a
+    CUDA graph and replayed on new inputs gives bit for bit what direct calls give
+    (the bench times the step this way)."""
+    T, E, K, H = 2048, 256, 8, 512
+    a = make_moe_case(num_tokens=T, num_experts=E, topk=K, hidden_size=H, seed=4700).to("cuda")
+    b = make_moe_case(num_tokens=T, num_experts=E, topk=K, hidden_size=H, seed=4701).to("cuda")
+    logits, hidden = a.logits.clone(), a.hidden.clone()
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    ws = torch.empty(pa.moe_sort_workspace_bytes(T * K, E), dtype=torch.uint8, device="cuda")
+    sp = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    y = torch.empty((T * K, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(hidden)
+
+    def chain():
+        pa.topk_softmax(logits, K, True, weights=w, ids=ids)
+        pa.moe_sort(ids, E, workspace=ws, out=(sp, off, pos))
+        pa.moe_gather(hidden, pos, K, out=y)
+        pa.moe_scatter_back(y, pos, w, out=out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        chain()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for case in (b, a):   # replay on new inputs, then on the first ones again
+        logits.copy_(case.logits)
+        hidden.copy_(case.hidden)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (w, ids, sp, off, pos, out)]
+        chain()
+        torch.cuda.synchronize()
+        for x, r in zip(got, (w, ids, sp, off, pos, out)):
+            assert torch.equal(x, r)
+    assert pa.device_status() == 0
