@@ -7,12 +7,14 @@
 // index_add_; page: commit 490ff98, "Dockerfile": the topk_softmax router
 // kernel, which the pages rebuilt for a 64-wide warp):
 //   * topk_softmax: one 32-lane warp per token; each lane holds E/32
-//     consecutive logits in fp32 registers (a 16-byte load per lane for bf16
-//     at E = 256).  The softmax max and sum are warp reductions; the top-k
-//     are chosen on the logits themselves (softmax is monotonic), k rounds of
-//     a warp arg-max (two redux.sync reductions: the largest order-preserving
-//     key, then the lowest expert id holding it), so the chosen ids are exact
-//     whatever the rounding of the probabilities.
+//     consecutive logits (a 16-byte load per lane for bf16 at E = 256).  The
+//     top-k are chosen on the logits themselves (softmax is monotonic), k
+//     rounds of a warp arg-max on order-preserving keys, so the chosen ids are
+//     exact whatever the rounding of the probabilities: for 16-bit logits the
+//     key and the expert id pack into one u32 (one redux.sync per round on
+//     per-lane sorted values), for fp32 two reductions per round (largest key,
+//     then lowest id holding it).  The softmax max is the first winner (16-bit)
+//     or a warp reduction (fp32); the normaliser is a warp sum.
 //   * sort: a stable counting sort in three launches -- per-chunk expert
 //     histograms, one CTA turning them into each chunk's first position per
 //     expert, and a scatter in which each warp walks its share of the chunk in
@@ -22,8 +24,9 @@
 //     stores), so every hidden byte crosses DRAM once and every regrouped
 //     byte is written once.
 //   * scatter-back: index_add_ written as a gather-reduce -- one warp per
-//     token sums its K weighted rows in fp32 in slot order and rounds once, so
-//     the result is deterministic and needs no atomics.
+//     (token, 1 KB block of the row) sums the token's K weighted rows in fp32
+//     in slot order and rounds once, so the result is deterministic and needs
+//     no atomics.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
