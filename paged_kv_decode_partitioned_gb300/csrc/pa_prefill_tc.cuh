@@ -15,8 +15,8 @@
 // every K/V tile it loads, and with two Q tiles each loaded K/V byte feeds
 // 256 rows.  Warp roles (64 + 256 NQ threads):
 //   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
-//              x the CTA's chunk tokens), then 128-token K and V tiles of the
-//              context through NS shared-memory stages; each lane looks up the
+//              x the CTA's chunk tokens), then K and V tiles of the context
+//              (128 tokens, 192 at head_dim 64) through NS shared-memory stages; each lane looks up the
 //              block of one (16-row box, 64-element piece) and issues its
 //              copy, so a tile's copies go out in parallel.  Each CTA starts
 //              its walk at its own tile and wraps around;
@@ -54,9 +54,11 @@ namespace pa {
 // Tile plan per head_dim.  A tcgen05.mma with M = 128 and K = 16 costs about
 // 80 cycles whatever N <= 128 is (measured on GB300: N = 64 reaches 38 % of
 // the tensor peak, N = 128 80 %, N = 256 all of it), so the MMAs are kept
-// wide: every head_dim runs 128-token K/V tiles.  head_dim 64 / 128 run two Q
-// tiles per CTA, each with one S buffer in tensor memory (the two tiles take
-// turns on the tensor pipe); head_dim 256 (its O alone takes 256 columns) runs
+// wide: 128-token K/V tiles, 192 at head_dim 64 (its O is only 64 columns, so
+// two Q tiles of S + O still fit 512 columns, and each MMA group does 1.5x the
+// work for the same issue overhead: 736 -> 825 TFLOP/s).  head_dim 64 / 128 run
+// two Q tiles per CTA, each with one S buffer in tensor memory (the two tiles
+// take turns on the tensor pipe); head_dim 256 (its O alone takes 256 columns) runs
 // one Q tile with two S buffers, and its 128 KB K+V tile leaves room for one
 // shared-memory stage next to the 64 KB Q tile (64-token tiles with two
 // stages ran QK at N = 64: 737 against 911 TFLOP/s).
@@ -64,9 +66,9 @@ template <int D>
 struct PrefillTcCfg {
     static constexpr int kQTiles = D <= 128 ? 2 : 1;
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
-    static constexpr int kN = 128;                                // cache tokens per tile
+    static constexpr int kN = D <= 64 ? 192 : 128;                // cache tokens per tile
     static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
-    static constexpr int kStages = D <= 64 ? 5 : (D <= 128 ? 2 : 1);
+    static constexpr int kStages = D <= 64 ? 3 : (D <= 128 ? 2 : 1);
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
     static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
