@@ -121,6 +121,18 @@ def test_moe_sort_is_bit_exact(pa, T, E, K):
     assert pa.device_status() == 0
 
 
+def test_moe_sort_large(pa):
+    """3.2 M pairs (1563 chunks of 2048, more than the GPU holds at once): the
+    sort stays bit-exact against the oracle."""
+    g = torch.Generator().manual_seed(4150)
+    ids = torch.randint(0, 64, (400000 * 8,), generator=g, dtype=torch.int32)
+    sp, off, pos = pa.moe_sort(ids.cuda(), 64)
+    rsp, roff, rpos = oracle.moe_sort(ids, 64)
+    assert (sp.cpu().numpy() == rsp).all() and (off.cpu().numpy() == roff).all()
+    assert (pos.cpu().numpy() == rpos).all()
+    assert pa.device_status() == 0
+
+
 def test_moe_sort_skewed_routing(pa):
     """Every pair on one expert, then on two alternating experts: the sort keeps
     the flat order (stability) across chunks of the kernel."""
