@@ -10,19 +10,20 @@ pass, longer ones split into 512-token partitions), the one workload whose
 step runs every stage of the path.  ``--workload N`` selects another.
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
-and a device synchronise; every step is timed with CUDA events on the stream
-the kernels are launched on, with a 2x-L2 buffer write between steps (the
-KV inputs are also far larger than L2).  The attention kernel alone is timed
-the same way (events between its launch and its neighbours') for the
-roofline.  ``e2e`` repeats the step through ``pa_decode_auto`` (the one call a
+and a device synchronise; every step is timed with two CUDA events on the
+stream the kernels are launched on, with a 2x-L2 buffer write then read
+between steps, outside the events (the KV inputs are also far larger than
+L2).  Per-launch times, and the attention kernel's time for the roofline,
+come from a second pass of K steps with an event after every launch (an
+event between two launches would add ~1 us to a timed step).  ``e2e`` repeats the step through ``pa_decode_auto`` (the one call a
 user makes) with the per-step inputs copied from pinned host memory and the
 output read back, inside the timed region.  ``cpu_baseline`` times the fp64
 oracle on a bounded sample of the same workload on the host cores.
 
 ``--path prefill`` times the paged prefix-prefill kernel (TFLOP/s against
 the bf16 tensor peak) and ``--path moe`` the MoE router + sort-by-expert
-regroup + scatter-back (GB/s against the HBM peak); both print a line of the
-same shape.  ``--impl reference`` times the oracle alone (the reference arm)
+regroup + scatter-back (GB/s against the HBM peak; the step's six kernels
+replay as one CUDA graph); both print a line of the same shape.  ``--impl reference`` times the oracle alone (the reference arm)
 on the same workload, metric and unit.  Multi-GPU (torchrun): every rank runs its own
 replica of the workload (no collective on the data path); time is the max
 over ranks and the value is the total over ranks.
