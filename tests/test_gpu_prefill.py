@@ -29,6 +29,11 @@ SHAPES = [
     ([3000, 47], [1, 1], 24, 8, 128, 16, torch.float16),
     ([0, 300], [100, 45], 16, 2, 256, 16, torch.bfloat16),
     ([129, 64], [64, 1], 8, 8, 256, 32, torch.float16),
+    # blocks that 128- and 192-token K/V tiles straddle
+    ([300, 1000], [77, 200], 16, 4, 64, 48, torch.bfloat16),
+    ([500, 130], [250, 9], 32, 4, 64, 128, torch.float16),
+    ([700], [60], 16, 2, 256, 80, torch.bfloat16),
+    ([1100, 40], [130, 31], 24, 4, 128, 112, torch.bfloat16),
 ]
 IDS = [f"d{s[4]}_g{s[2] // s[3]}_bs{s[5]}_{str(s[6])[6:]}" for s in SHAPES]
 
