@@ -238,7 +238,7 @@ def test_long_sequence_single_pass_cluster_split(pa):
     assert pa.device_status() == 0
 
 
-@pytest.mark.parametrize("bs", [64, 256])
+@pytest.mark.parametrize("bs", [48, 64, 80, 256])
 def test_large_block_sizes(pa, bs):
     w = custom_workload(num_q_heads=16, num_kv_heads=2, head_dim=128, block_size=bs,
                         dtype=torch.float16)
