@@ -33,12 +33,21 @@
 #include <stdint.h>
 
 #include <climits>
+#include <utility>
 
 #include "pa_launch.h"
 
 namespace pa {
 
 namespace {
+
+// Programmatic dependent launch: the kernels of the MoE chain are launched so
+// that the next one may start while the previous one drains.  Each kernel
+// waits, before its first global access, for the previous grid in the stream
+// to complete with its memory visible (a no-op when launched without the
+// attribute), and lets the next grid launch once its own work is issued.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -178,11 +187,13 @@ __device__ __forceinline__ void topk_softmax_16(const TopkParams &p, int t, int 
 
 template <typename TL, int VPL>
 __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p) {
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.num_tokens) return;
     if constexpr (sizeof(TL) == 2) {
         topk_softmax_16<TL, VPL>(p, t, lane);
+        pdl_trigger();
         return;
     }
     constexpr int E = VPL * 32;
@@ -240,6 +251,7 @@ __global__ void __launch_bounds__(256) pa_topk_softmax_kernel(const TopkParams p
         p.weights[static_cast<size_t>(t) * p.topk + lane] = w;
         p.ids[static_cast<size_t>(t) * p.topk + lane] = my_id;
     }
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // ---------------------------------------------------------------------------
@@ -251,6 +263,7 @@ constexpr int kSortChunk = 2048;   // pairs per CTA (256 per warp)
 
 // hist[c][e] = pairs of chunk c with expert e
 __global__ void __launch_bounds__(kSortThreads) pa_moe_hist_kernel(const SortParams p) {
+    pdl_wait();
     extern __shared__ int h[];
     for (int e = threadIdx.x; e < p.num_experts; e += kSortThreads) h[e] = 0;
     __syncthreads();
@@ -268,11 +281,13 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_hist_kernel(const SortPar
     __syncthreads();
     for (int e = threadIdx.x; e < p.num_experts; e += kSortThreads)
         p.hist[static_cast<size_t>(blockIdx.x) * p.num_experts + e] = h[e];
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // One CTA: hist[c][e] becomes the first sorted position of chunk c's pairs of
 // expert e; offsets[e] the first position of expert e, offsets[E] the total.
 __global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
+    pdl_wait();
     __shared__ int part[1024];    // [group][expert] chunk sums
     __shared__ int first[1024];   // [expert] first sorted position
     __shared__ int warp_sum[32];
@@ -346,11 +361,13 @@ __global__ void __launch_bounds__(1024) pa_moe_scan_kernel(const SortParams p) {
             }
         }
     }
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // Each warp places its 256 pairs in order: within a 32-pair step, pairs with
 // the same expert are ranked by lane (match_any + popc of the lower lanes).
 __global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortParams p) {
+    pdl_wait();
     extern __shared__ int cnt[];   // [kSortWarps][E]: this warp's next position per expert
     const int E = p.num_experts;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,6 +410,7 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortPa
         if (ok && (same & lt) == 0) mine[e] += __popc(same);
         __syncwarp();
     }
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // ---------------------------------------------------------------------------
@@ -403,6 +421,7 @@ __global__ void __launch_bounds__(kSortThreads) pa_moe_place_kernel(const SortPa
 // to the K sorted positions of the token's pairs with streaming stores, so
 // every hidden byte crosses DRAM once.
 __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParams p) {
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.num_tokens) return;
@@ -437,6 +456,7 @@ __global__ void __launch_bounds__(256) pa_moe_gather_kernel(const MoeGatherParam
             }
         }
     }
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // 16-byte columns (8 elements) of a scatter-back work unit: 1 KB of a row
@@ -486,6 +506,7 @@ struct Vec8<__half> {
 // out[t] = sum_k w[t][k] * y[pair_pos[t*K + k]], fp32 in slot order, one rounding.
 template <typename T>
 __global__ void __launch_bounds__(256) pa_moe_scatter_kernel(const MoeScatterParams p) {
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // one warp per (token, 1 KB block of columns): a warp per whole token gave
     // 1.7 waves of warps at 16384 tokens, whose partial last wave left the
@@ -538,15 +559,35 @@ __global__ void __launch_bounds__(256) pa_moe_scatter_kernel(const MoeScatterPar
         if (one) out[c] = Vec8<T>::pack(a0);
         if (two) out[c + 32] = Vec8<T>::pack(a1);
     }
+    pdl_trigger();   // the next kernel in the stream may launch
 }
 
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+// A launch with programmatic stream serialisation: the kernel may start while
+// the previous one in the stream drains; its pdl_wait() orders its accesses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_topk_softmax(int logits_type, int num_experts, const TopkParams &p,
                                 cudaStream_t st) {
     const dim3 grid((p.num_tokens + 7) / 8);
-#define PA_TOPK(TL, VPL) pa_topk_softmax_kernel<TL, VPL><<<grid, 256, 0, st>>>(p)
+    cudaError_t e = cudaSuccess;
+#define PA_TOPK(TL, VPL) e = launch_pdl(pa_topk_softmax_kernel<TL, VPL>, grid, dim3(256), 0, st, p)
 #define PA_TOPK_E(TL)                                  \
     switch (num_experts) {                             \
         case 32: PA_TOPK(TL, 1); break;                \
@@ -567,7 +608,7 @@ cudaError_t launch_topk_softmax(int logits_type, int num_experts, const TopkPara
     }
 #undef PA_TOPK_E
 #undef PA_TOPK
-    return cudaGetLastError();
+    return e;
 }
 
 int moe_sort_chunks(int num_pairs) { return (num_pairs + kSortChunk - 1) / kSortChunk; }
@@ -576,11 +617,11 @@ cudaError_t launch_moe_sort(const SortParams &p, cudaStream_t st) {
     const int E = p.num_experts;
     cudaError_t e;
     if (p.num_chunks > 0) {
-        pa_moe_hist_kernel<<<p.num_chunks, kSortThreads, E * sizeof(int), st>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(pa_moe_hist_kernel, dim3(p.num_chunks), dim3(kSortThreads),
+                       E * sizeof(int), st, p);
+        if (e != cudaSuccess) return e;
     }
-    pa_moe_scan_kernel<<<1, 1024, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(pa_moe_scan_kernel, dim3(1), dim3(1024), 0, st, p)) != cudaSuccess) return e;
     if (p.num_chunks == 0) return cudaSuccess;
     const int smem = kSortWarps * E * static_cast<int>(sizeof(int));
     if (smem > 48 * 1024) {
@@ -588,13 +629,11 @@ cudaError_t launch_moe_sort(const SortParams &p, cudaStream_t st) {
                                  smem);
         if (e != cudaSuccess) return e;
     }
-    pa_moe_place_kernel<<<p.num_chunks, kSortThreads, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(pa_moe_place_kernel, dim3(p.num_chunks), dim3(kSortThreads), smem, st, p);
 }
 
 cudaError_t launch_moe_gather(const MoeGatherParams &p, cudaStream_t st) {
-    pa_moe_gather_kernel<<<(p.num_tokens + 7) / 8, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(pa_moe_gather_kernel, dim3((p.num_tokens + 7) / 8), dim3(256), 0, st, p);
 }
 
 cudaError_t launch_moe_scatter(bool bf16, const MoeScatterParams &p, cudaStream_t st) {
@@ -603,11 +642,8 @@ cudaError_t launch_moe_scatter(bool bf16, const MoeScatterParams &p, cudaStream_
     if (units == 0) return cudaSuccess;
     if ((units + 7) / 8 > INT_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>((units + 7) / 8));
-    if (bf16)
-        pa_moe_scatter_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
-    else
-        pa_moe_scatter_kernel<__half><<<grid, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return bf16 ? launch_pdl(pa_moe_scatter_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, p)
+                : launch_pdl(pa_moe_scatter_kernel<__half>, grid, dim3(256), 0, st, p);
 }
 
 }  // namespace pa
