@@ -66,13 +66,17 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--workload", type=int, default=4,
+                    help="decode workload id: 1-5 (the five configurations), 6 (the mixed "
+                         "batch with GQA 16), 7 (the mixed batch with block size 8)")
     ap.add_argument("--partition-size", type=int, default=None,
-                    help="override the workload's (first) partition size")
+                    help="override the workload's (first) partition size (auto mode: 0 lets "
+                         "the library's heuristic choose)")
     ap.add_argument("--mode", choices=["single", "partitioned", "auto"], default=None,
                     help="override the workload's decode mode")
     ap.add_argument("--single-pass-max-len", type=int, default=None,
-                    help="override the workload's single-pass limit (auto mode)")
+                    help="override the workload's single-pass limit (auto mode; -1 lets the "
+                         "library's heuristic choose)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="reduced batch of the same workload rule (for profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -299,6 +303,29 @@ def time_oracle(case, sample):
     return time.perf_counter() - t
 
 
+def one_core_oracle():
+    """The oracle on one host core: workload 1 whole, and workload 3 cut to one
+    of its 100,000-token sequences (GB/s of K+V and seconds of each)."""
+    import torch
+    import oracle
+    from workloads import WORKLOADS, make_case
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    res = {}
+    oracle.set_num_threads(1)
+    try:
+        for key, wid, kw in (("workload1", 1, {}), ("workload3_one_seq", 3,
+                                                    {"lengths": [100000]})):
+            case = make_case(WORKLOADS[wid], device=dev, seed=rank_seed(wid, 0), **kw)
+            ids = list(range(case.num_seqs))
+            secs = time_oracle(case, ids)
+            res[key] = {"value": round(kv_bytes(case) / secs / 1e9, 4), "unit": "GB/s",
+                        "seconds": round(secs, 4), "tokens": case.total_tokens}
+            del case
+    finally:
+        oracle.set_num_threads(cpu_threads())
+    return res
+
+
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -314,8 +341,8 @@ def rank_seed(wid: int, rank: int) -> int:
 
 
 def make_inputs(wid, device, num_seqs=None, rank=0):
-    from workloads import WORKLOADS, make_case
-    return make_case(WORKLOADS[wid], device=device, num_seqs=num_seqs, seed=rank_seed(wid, rank))
+    from workloads import make_case, workload
+    return make_case(workload(wid), device=device, num_seqs=num_seqs, seed=rank_seed(wid, rank))
 
 
 def across_ranks(world: int, device, max_vals=(), sum_vals=()):
@@ -827,12 +854,12 @@ def main():
 
     case = make_inputs(args.workload, "cuda", args.num_seqs, rank)
     w = case.workload
-    P = args.partition_size or w.partition_sizes[0]
+    P = w.partition_sizes[0] if args.partition_size is None else args.partition_size
     mode = args.mode or w.mode
     thr = w.single_pass_max_len if args.single_pass_max_len is None else args.single_pass_max_len
     step = DecodeStep(mode, case.query, case.key_cache, case.value_cache, case.block_tables,
                       case.seq_lens, w.scale, max_seq_len=case.max_seq_len, partition_size=P,
-                      single_pass_max_len=thr)
+                      single_pass_max_len=thr, max_total_tokens=case.total_tokens)
     launches = step.launches()
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
@@ -986,7 +1013,8 @@ def main():
         cpu = {"value": round(skv / secs / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(),
                "kind": "oracle",
                "sample": f"{len(sample)} of {case.num_seqs} sequences ({tok} tokens) of the "
-                         f"same workload, {secs:.1f} s"}
+                         f"same workload, {secs:.1f} s",
+               "one_core": one_core_oracle()}
 
     if rank != 0:
         return
@@ -1001,8 +1029,10 @@ def main():
                    f"{w.name} (reduced to {case.num_seqs} sequences)",
                    "global_batch": int(seqs_all),
                    "seq_len": case.max_seq_len, "total_tokens": case.total_tokens,
-                   "mode": mode, "partition_size": P,
-                   "single_pass_max_len": thr,
+                   "mode": mode, "partition_size": step.resolved[1] if mode == "auto" else P,
+                   "single_pass_max_len": step.resolved[0] if mode == "auto" else thr,
+                   "launch_form": ("single", "dense", "worklist")[step.form]
+                   if mode == "auto" else mode,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between steps (outside the events): {flush_w.numel() >> 20} "
                          f"MiB written, then {flush_r.numel() * 4 >> 20} MiB read; "

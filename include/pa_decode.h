@@ -26,9 +26,12 @@
  *   - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
  *   - dtype selects IEEE binary16 (PA_F16) or bfloat16 (PA_BF16) for query,
  *     caches and out.  Accumulation is fp32.  Partials are fp32.
- *   - Supported shapes: head_dim in {64, 128, 256}; block_size a multiple of
- *     16; num_q_heads / num_kv_heads between 1 and 8.  Other shapes return
- *     PA_ERR_UNSUPPORTED.
+ *   - Supported shapes (decode entry points): head_dim in {64, 128, 256};
+ *     block_size 8 or a multiple of 16; GQA group num_q_heads / num_kv_heads
+ *     between 1 and 128.  A group of up to 16 heads (8 at head_dim 256) is
+ *     served by one unit per KV head, which reads each K/V page once; a larger
+ *     group is split into head groups of 16 (8) that each read the KV head's
+ *     pages.  Other shapes return PA_ERR_UNSUPPORTED.
  *   - Alignment: caches, query, out and partial buffers 16-byte aligned
  *     (PA_ERR_MISALIGNED otherwise).
  *   - block_tables contents and seq_lens values are read on the device only.
@@ -135,6 +138,21 @@ PA_API int pa_partition_reduce(void *out, const float *tmp_out, const float *exp
                         pa_dtype_t dtype, void *stream);
 
 /*
+ * pa_partition_workspace_bytes -- bytes of the phase-1 partials of
+ * pa_decode_partitioned (V2 description, phase 1: a partial output, its
+ * exp-sum and its maximum logit kept per partition) for num_seqs sequences,
+ * num_q_heads query heads, head_dim and max_num_partitions slots, laid out in
+ * one buffer as three 256-byte-aligned regions in this order:
+ *   tmp_out    fp32 [num_seqs][num_q_heads][max_num_partitions][head_dim]
+ *   exp_sums   fp32 [num_seqs][num_q_heads][max_num_partitions]
+ *   max_logits fp32 [num_seqs][num_q_heads][max_num_partitions]
+ * Region i starts at the end of region i-1 rounded up to 256 bytes.  Returns
+ * 0 on bad arguments (a negative or zero size, or more than 2^40 elements).
+ */
+PA_API size_t pa_partition_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                           int max_num_partitions);
+
+/*
  * pa_default_single_pass_max_len -- the launch heuristic's threshold.
  * Sequences longer than the returned length are partitioned by
  * pa_decode_auto.  It is 8192, the forward_decode heuristic's boundary
@@ -149,13 +167,66 @@ PA_API int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int pa
                                    int num_sms);
 
 /*
+ * pa_default_partition_size -- the launch heuristic's partition size (the
+ * pages use 512 in one file and 256 in another).  Returns the smallest of
+ * 256, 512 and 1024 tokens for which the batch's partition units
+ * num_seqs * num_kv_heads * ceil(max_seq_len / P) fit in one wave of resident
+ * attention CTAs (num_sms x CTAs per SM), else 1024; rounded up to a multiple
+ * of block_size.  Measured on GB300: one wave of long partitions beats two
+ * waves of short ones, and at more than a wave the longer partitions write
+ * fewer partials.  num_sms <= 0 queries the current device.  Returns 0 on bad
+ * arguments.
+ */
+PA_API int pa_default_partition_size(int num_seqs, int num_kv_heads, int block_size,
+                                     int head_dim, int max_seq_len, int num_sms);
+
+/* Launch forms of pa_decode_auto (pa_auto_resolve). */
+enum {
+    PA_AUTO_SINGLE_PASS = 0,   /* max_seq_len <= threshold: the pa_decode grid, one launch */
+    PA_AUTO_DENSE = 1,         /* few sequences, all split: pa_decode_partitioned's grid and
+                                  pa_partition_reduce, partials in the workspace; two launches */
+    PA_AUTO_WORKLIST = 2       /* planner + work-list attention + reduce; three launches */
+};
+
+/*
+ * pa_auto_resolve -- what pa_decode_auto does for these host values, without
+ * launching anything: the single-pass threshold (single_pass_max_len < 0
+ * selects pa_default_single_pass_max_len, raised to max_seq_len when the
+ * batch has at least one (sequence, KV head) unit per SM and the caller's
+ * token bound max_total_tokens is at least 9/10 of num_seqs * max_seq_len:
+ * nearly equal lengths, which one pass balances without partials), the
+ * partition size (partition_size <= 0 selects pa_default_partition_size) and
+ * the launch form:
+ *   PA_AUTO_SINGLE_PASS when max_seq_len <= threshold;
+ *   PA_AUTO_DENSE when threshold <= partition size (every sequence longer
+ *     than one partition is split) and num_seqs * num_kv_heads < num_sms;
+ *   PA_AUTO_WORKLIST otherwise.
+ * Any output pointer may be NULL.  num_sms <= 0 queries the current device.
+ * Returns PA_OK, PA_ERR_INVALID_ARGUMENT or PA_ERR_UNSUPPORTED (a partition
+ * size that is not a multiple of block_size).
+ */
+PA_API int pa_auto_resolve(int num_seqs, int num_kv_heads, int head_dim, int block_size,
+                           int max_seq_len, long long max_total_tokens, int single_pass_max_len,
+                           int partition_size, int num_sms, int *out_single_pass_max_len,
+                           int *out_partition_size, int *out_form);
+
+/*
  * pa_auto_workspace_bytes -- device workspace pa_decode_auto needs (bytes),
- * for at most `max_seq_len` tokens per sequence.  Returns 0 on bad
- * arguments.  single_pass_max_len < 0 selects the heuristic above.
+ * for at most `max_seq_len` tokens per sequence and, when
+ * max_total_tokens > 0, at most that many tokens over the whole batch
+ * (0 or less: no bound beyond num_seqs * max_seq_len).  With the bound the
+ * work-list form keeps at most floor((T + S_p (P - 1)) / P) partition slots,
+ * S_p = min(num_seqs, T / (threshold + 1)) (the sequences that can be longer
+ * than the threshold), instead of num_seqs * ceil(max_seq_len / P).
+ * single_pass_max_len < 0 and partition_size <= 0 select the heuristics
+ * above (resolved on the current device, as pa_decode_auto resolves them).
+ * Returns 0 on bad arguments; 256 when the single-pass form needs no
+ * workspace.
  */
 PA_API size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
-                               int head_dim, int max_seq_len, int single_pass_max_len,
-                               int partition_size);
+                                      int head_dim, int block_size, int max_seq_len,
+                                      long long max_total_tokens, int single_pass_max_len,
+                                      int partition_size);
 
 /*
  * pa_decode_auto -- the whole decode step with a per-sequence choice of path
@@ -163,48 +234,52 @@ PA_API size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_
  * seq_len <= single_pass_max_len is computed in one pass and written to out
  * directly; a longer one is split into ceil(L/partition_size) partitions whose
  * partials (kept in `workspace`) are merged by the log-sum-exp reduce.  The
- * device builds the work list from seq_lens, so the host needs only the upper
- * bound `max_seq_len` (every seq_len must be <= it; a longer one raises
- * PA_DEV_TOO_MANY_PARTITIONS).  single_pass_max_len < 0 selects
- * pa_default_single_pass_max_len.  workspace: device memory of at least
+ * device reads seq_lens itself, so the host needs only the upper bounds
+ * `max_seq_len` (every seq_len must be <= it) and `max_total_tokens` (the sum
+ * of seq_lens must be <= it when it is > 0); a batch beyond either bound
+ * raises PA_DEV_TOO_MANY_PARTITIONS and the partitions past the bound are
+ * dropped from the output.  single_pass_max_len < 0 and partition_size <= 0
+ * select the launch heuristic (pa_auto_resolve gives the values and the
+ * launch form it picks).  workspace: device memory of at least
  * pa_auto_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller;
- * its contents need no initialisation and are scratch after the call.
- * Launches three kernels (plan, attention, reduce) on `stream`; when
- * max_seq_len <= the single-pass limit it launches the single-pass grid of
- * pa_decode alone.
+ * its contents need no initialisation and are scratch after the call; it may
+ * be NULL when the single-pass form is taken.  Launches, on `stream`, one
+ * kernel (single-pass form), two (dense form: attention, reduce) or three
+ * (work-list form: plan, attention, reduce).
  */
 PA_API int pa_decode_auto(void *out, const void *query, const void *key_cache,
                    const void *value_cache, const int32_t *block_tables,
                    const int32_t *seq_lens, int num_seqs, int num_q_heads,
                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
                    int max_blocks_per_seq, float scale, int max_seq_len,
-                   int single_pass_max_len, int partition_size, void *workspace,
-                   size_t workspace_bytes, pa_dtype_t dtype, void *stream);
+                   long long max_total_tokens, int single_pass_max_len, int partition_size,
+                   void *workspace, size_t workspace_bytes, pa_dtype_t dtype, void *stream);
 
 /* Phases of pa_decode_auto_phases (bit mask). */
 enum { PA_PHASE_PLAN = 1, PA_PHASE_ATTEND = 2, PA_PHASE_REDUCE = 4 };
 
 /*
- * pa_decode_auto_phases -- pa_decode_auto split into its three launches so
- * a caller can order other stream work (events, copies) between them:
- * PA_PHASE_PLAN builds the work list in `workspace` from seq_lens;
- * PA_PHASE_ATTEND runs the attention kernel over it (single-pass sequences
- * write `out`, partitioned ones write their partials to `workspace`);
- * PA_PHASE_REDUCE merges the partials into `out`.  When max_seq_len is at
- * most the single-pass limit, PA_PHASE_ATTEND runs the single-pass grid and
- * the other two phases do nothing.  All arguments must be the
- * same for the phases of one step and the phases must run in this order on
- * one stream.  phases = PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE is
- * exactly pa_decode_auto.  Other masks return PA_ERR_INVALID_ARGUMENT.
+ * pa_decode_auto_phases -- pa_decode_auto split into its launches so a caller
+ * can order other stream work (events, copies) between them: PA_PHASE_PLAN
+ * builds the work list in `workspace` from seq_lens; PA_PHASE_ATTEND runs the
+ * attention kernel (single-pass sequences write `out`, partitioned ones write
+ * their partials to `workspace`); PA_PHASE_REDUCE merges the partials into
+ * `out`.  A phase the resolved launch form does not have does nothing (the
+ * single-pass form has only PA_PHASE_ATTEND, the dense form no PA_PHASE_PLAN).
+ * All arguments must be the same for the phases of one step and the phases
+ * must run in this order on one stream.  phases = PA_PHASE_PLAN |
+ * PA_PHASE_ATTEND | PA_PHASE_REDUCE is exactly pa_decode_auto.  Other masks
+ * return PA_ERR_INVALID_ARGUMENT.
  */
 PA_API int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
                                  const void *value_cache, const int32_t *block_tables,
                                  const int32_t *seq_lens, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size,
                                  int num_blocks, int max_blocks_per_seq, float scale,
-                                 int max_seq_len, int single_pass_max_len,
-                                 int partition_size, void *workspace, size_t workspace_bytes,
-                                 pa_dtype_t dtype, void *stream, int phases);
+                                 int max_seq_len, long long max_total_tokens,
+                                 int single_pass_max_len, int partition_size, void *workspace,
+                                 size_t workspace_bytes, pa_dtype_t dtype, void *stream,
+                                 int phases);
 
 /*
  * pa_decode_auto_static -- pa_decode_auto for callers that cannot allocate
@@ -218,7 +293,9 @@ PA_API int pa_decode_auto_phases(void *out, const void *query, const void *key_c
  * host that passes in its tensors but exposes no allocator.  This entry point
  * takes the same arguments as pa_decode_auto minus the workspace, and keeps
  * its scratch (work list and partition partials) in one fixed array of
- * PA_STATIC_SCRATCH_BYTES in device memory that belongs to the library.
+ * PA_STATIC_SCRATCH_BYTES (96 MiB) in device memory that belongs to the
+ * library: enough for the partials of 256 sequences of up to 64K tokens and
+ * 2.9M tokens in all at partition size 512 when max_total_tokens is given.
  * Every GPU that loads the library holds that array until the process exits.
  * The call allocates nothing.
  *
@@ -235,15 +312,16 @@ PA_API int pa_decode_auto_phases(void *out, const void *query, const void *key_c
  *     overlap on the GPU (for example on two streams) race on the array:
  *     serialise them.
  */
-#define PA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+#define PA_STATIC_SCRATCH_BYTES ((size_t)96 << 20)
 
 PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_cache,
                                  const void *value_cache, const int32_t *block_tables,
                                  const int32_t *seq_lens, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size,
                                  int num_blocks, int max_blocks_per_seq, float scale,
-                                 int max_seq_len, int single_pass_max_len,
-                                 int partition_size, pa_dtype_t dtype, void *stream);
+                                 int max_seq_len, long long max_total_tokens,
+                                 int single_pass_max_len, int partition_size, pa_dtype_t dtype,
+                                 void *stream);
 
 /*
  * pa_prefill -- prefix prefill over the paged cache (page: project_6 commit
@@ -266,7 +344,7 @@ PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_c
  * are not written and raise PA_DEV_LEN_CLAMPED).  q_start is read on the
  * device only: a sequence whose rows fall outside [0, num_rows], or whose
  * chunk is longer than seq_lens[s], is skipped and raises PA_DEV_BAD_ROWS.
- * Supported: head_dim 64 or 128, block_size a multiple of 16, GQA group
+ * Supported: head_dim 64, 128 or 256, block_size a multiple of 16, GQA group
  * 1..128.  One kernel launch on `stream`; no workspace.
  */
 PA_API int pa_prefill(void *out, const void *query, const void *key_cache,

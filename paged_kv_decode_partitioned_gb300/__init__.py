@@ -22,7 +22,9 @@ import torch
 
 __all__ = [
     "PaError", "load_library", "library_path", "decode", "decode_partitioned",
-    "partition_reduce", "decode_auto", "auto_workspace_bytes", "default_single_pass_max_len",
+    "partition_reduce", "decode_auto", "decode_auto_static", "auto_workspace_bytes",
+    "default_single_pass_max_len", "default_partition_size", "auto_resolve",
+    "partition_workspace_bytes", "AUTO_SINGLE_PASS", "AUTO_DENSE", "AUTO_WORKLIST",
     "prefill", "gather_kv", "device_status", "num_partitions", "version",
     "DEV_BAD_BLOCK", "DEV_LEN_CLAMPED", "DEV_WAIT_TIMEOUT", "DEV_TOO_MANY_PARTITIONS",
     "DEV_BAD_ROWS", "DEV_BAD_EXPERT", "topk_softmax", "moe_sort", "moe_gather",
@@ -34,6 +36,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libpadecode.so")
 
 PA_F16, PA_BF16 = 0, 1
 PHASE_PLAN, PHASE_ATTEND, PHASE_REDUCE = 1, 2, 4
+AUTO_SINGLE_PASS, AUTO_DENSE, AUTO_WORKLIST = 0, 1, 2
 DEV_BAD_BLOCK, DEV_LEN_CLAMPED, DEV_WAIT_TIMEOUT, DEV_TOO_MANY_PARTITIONS = 1, 2, 4, 8
 DEV_BAD_ROWS = 16
 DEV_BAD_EXPERT = 32
@@ -45,19 +48,24 @@ _lib = None
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
 _f = ctypes.c_float
+_ll = ctypes.c_longlong
+_sz = ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
 
 # (name, restype, argtypes) of every entry point in include/pa_decode.h and include/pa_moe.h
 SIGNATURES = [
     ("pa_decode", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _vp]),
     ("pa_decode_partitioned", _i, [_vp] * 8 + [_i] * 7 + [_f, _i, _i, _i, _vp]),
     ("pa_partition_reduce", _i, [_vp] * 5 + [_i] * 6 + [_vp]),
+    ("pa_partition_workspace_bytes", _sz, [_i] * 4),
     ("pa_default_single_pass_max_len", _i, [_i] * 4),
-    ("pa_auto_workspace_bytes", ctypes.c_size_t, [_i] * 7),
-    ("pa_decode_auto", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t, _i,
-                                                    _vp]),
-    ("pa_decode_auto_phases", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _vp, ctypes.c_size_t,
-                                                           _i, _vp, _i]),
-    ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _i, _i, _i, _vp]),
+    ("pa_default_partition_size", _i, [_i] * 6),
+    ("pa_auto_resolve", _i, [_i] * 5 + [_ll] + [_i] * 3 + [_ip] * 3),
+    ("pa_auto_workspace_bytes", _sz, [_i] * 6 + [_ll, _i, _i]),
+    ("pa_decode_auto", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _ll, _i, _i, _vp, _sz, _i, _vp]),
+    ("pa_decode_auto_phases", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _ll, _i, _i, _vp, _sz, _i,
+                                                           _vp, _i]),
+    ("pa_decode_auto_static", _i, [_vp] * 6 + [_i] * 7 + [_f, _i, _ll, _i, _i, _i, _vp]),
     ("pa_prefill", _i, [_vp] * 7 + [_i] * 9 + [_f, _i, _vp]),
     ("pa_gather_kv", _i, [_vp] * 6 + [_i] * 7 + [_i, _vp]),
     ("pa_topk_softmax", _i, [_vp] * 3 + [_i] * 5 + [_vp]),
@@ -179,20 +187,50 @@ def decode(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
     return out
 
 
+def partition_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                              max_num_partitions: int) -> int:
+    """Bytes of the dense phase-1 partials (``pa_partition_workspace_bytes``)."""
+    return int(_load().pa_partition_workspace_bytes(int(num_seqs), int(num_q_heads),
+                                                    int(head_dim), int(max_num_partitions)))
+
+
+def partition_buffers(num_seqs: int, num_q_heads: int, head_dim: int, max_num_partitions: int,
+                      device) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(tmp_out, exp_sums, max_logits) as views of one buffer of
+    ``partition_workspace_bytes`` bytes, in the layout the header states."""
+    S, Hq, D, NP = int(num_seqs), int(num_q_heads), int(head_dim), int(max_num_partitions)
+    total = partition_workspace_bytes(S, Hq, D, NP)
+    if total == 0:
+        raise ValueError("bad partition buffer shape")
+    buf = torch.empty(total // 4, dtype=torch.float32, device=device)
+    rows = S * Hq * NP
+
+    def up(x):
+        return (x + 255) // 256 * 256
+    o_es = up(rows * D * 4)
+    o_ml = up(o_es + rows * 4)
+    tmp_out = buf[:rows * D].view(S, Hq, NP, D)
+    exp_sums = buf[o_es // 4:o_es // 4 + rows].view(S, Hq, NP)
+    max_logits = buf[o_ml // 4:o_ml // 4 + rows].view(S, Hq, NP)
+    return tmp_out, exp_sums, max_logits
+
+
 def decode_partitioned(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
                        partition_size: int, max_num_partitions: int,
                        tmp_out=None, exp_sums=None, max_logits=None
                        ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Phase 1 (``pa_decode_partitioned``); returns (tmp_out, exp_sums, max_logits)."""
+    """Phase 1 (``pa_decode_partitioned``); returns (tmp_out, exp_sums, max_logits).
+
+    Buffers not passed are carved from one allocation sized by
+    ``pa_partition_workspace_bytes``."""
     S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
     NP = int(max_num_partitions)
     dev = query.device
-    if tmp_out is None:
-        tmp_out = torch.empty((S, Hq, NP, D), dtype=torch.float32, device=dev)
-    if exp_sums is None:
-        exp_sums = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
-    if max_logits is None:
-        max_logits = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+    if tmp_out is None or exp_sums is None or max_logits is None:
+        t, e, m = partition_buffers(S, Hq, D, NP, dev)
+        tmp_out = t if tmp_out is None else tmp_out
+        exp_sums = e if exp_sums is None else exp_sums
+        max_logits = m if max_logits is None else max_logits
     with torch.cuda.device(dev):
         st = _load().pa_decode_partitioned(
             _f32(tmp_out, "tmp_out"), _f32(exp_sums, "exp_sums"), _f32(max_logits, "max_logits"),
@@ -225,35 +263,60 @@ def default_single_pass_max_len(num_seqs: int, num_kv_heads: int, partition_size
                                                   num_sms)
 
 
+def default_partition_size(num_seqs: int, num_kv_heads: int, block_size: int, head_dim: int,
+                           max_seq_len: int, num_sms: int = 0) -> int:
+    return _load().pa_default_partition_size(num_seqs, num_kv_heads, block_size, head_dim,
+                                             max_seq_len, num_sms)
+
+
+def auto_resolve(num_seqs: int, num_kv_heads: int, head_dim: int, block_size: int,
+                 max_seq_len: int, single_pass_max_len: int = -1, partition_size: int = 0,
+                 num_sms: int = 0, max_total_tokens: int = 0) -> Tuple[int, int, int]:
+    """(single-pass threshold, partition size, launch form) that ``pa_decode_auto``
+    takes for these host values (``pa_auto_resolve``)."""
+    thr, P, form = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = _load().pa_auto_resolve(int(num_seqs), int(num_kv_heads), int(head_dim),
+                                 int(block_size), int(max_seq_len), int(max_total_tokens),
+                                 int(single_pass_max_len), int(partition_size), int(num_sms),
+                                 ctypes.byref(thr), ctypes.byref(P), ctypes.byref(form))
+    _check(st, "pa_auto_resolve")
+    return thr.value, P.value, form.value
+
+
 def auto_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                         max_seq_len: int, single_pass_max_len: int = 8192,
-                         partition_size: int = 512) -> int:
+                         block_size: int, max_seq_len: int, max_total_tokens: int = 0,
+                         single_pass_max_len: int = -1, partition_size: int = 0) -> int:
     return int(_load().pa_auto_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                               max_seq_len, single_pass_max_len,
-                                               partition_size))
+                                               block_size, max_seq_len, int(max_total_tokens),
+                                               single_pass_max_len, partition_size))
 
 
 def decode_auto(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
-                max_seq_len: int, single_pass_max_len: int = 8192, partition_size: int = 512,
+                max_seq_len: int, single_pass_max_len: int = -1, partition_size: int = 0,
                 workspace: Optional[torch.Tensor] = None,
-                out: Optional[torch.Tensor] = None, phases: Optional[int] = None) -> torch.Tensor:
+                out: Optional[torch.Tensor] = None, phases: Optional[int] = None,
+                max_total_tokens: int = 0) -> torch.Tensor:
     """Whole decode step with the per-sequence V1/V2 choice (``pa_decode_auto``).
 
-    ``phases`` (a PHASE_* mask) calls ``pa_decode_auto_phases`` instead, to
-    run only some of the step's launches; every phase needs the same arguments.
+    ``single_pass_max_len=-1`` and ``partition_size=0`` select the library's
+    launch heuristic; ``max_total_tokens`` (> 0) bounds the batch's total
+    tokens, which shrinks the workspace.  ``phases`` (a PHASE_* mask) calls
+    ``pa_decode_auto_phases`` instead, to run only some of the step's launches;
+    every phase needs the same arguments.
     """
     S, Hq, Hkv, D, bs, nb, mb = _shape(query, key_cache, block_tables)
-    need = auto_workspace_bytes(S, Hq, Hkv, D, max_seq_len, single_pass_max_len, partition_size)
     if workspace is None:
+        need = auto_workspace_bytes(S, Hq, Hkv, D, bs, max_seq_len, max_total_tokens,
+                                    single_pass_max_len, partition_size)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
     if out is None:
         out = torch.empty_like(query)
     args = (_dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
             _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
             _i32(seq_lens, "seq_lens"), S, Hq, Hkv, D, bs, nb, mb, float(scale),
-            int(max_seq_len), int(single_pass_max_len), int(partition_size),
-            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-            _dtype_code(query), _stream(query))
+            int(max_seq_len), int(max_total_tokens), int(single_pass_max_len),
+            int(partition_size), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _dtype_code(query), _stream(query))
     with torch.cuda.device(query.device):
         if phases is None:
             st = _load().pa_decode_auto(*args)
@@ -264,9 +327,9 @@ def decode_auto(query, key_cache, value_cache, block_tables, seq_lens, scale: fl
 
 
 def decode_auto_static(query, key_cache, value_cache, block_tables, seq_lens, scale: float,
-                       max_seq_len: int, single_pass_max_len: int = 8192,
-                       partition_size: int = 512,
-                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                       max_seq_len: int, single_pass_max_len: int = -1,
+                       partition_size: int = 0, out: Optional[torch.Tensor] = None,
+                       max_total_tokens: int = 0) -> torch.Tensor:
     """``pa_decode_auto_static``: ``decode_auto`` with the library's fixed scratch.
 
     For callers that cannot allocate device memory: no workspace is passed and
@@ -282,8 +345,8 @@ def decode_auto_static(query, key_cache, value_cache, block_tables, seq_lens, sc
             _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
             _dev(value_cache, "value_cache"), _i32(block_tables, "block_tables"),
             _i32(seq_lens, "seq_lens"), S, Hq, Hkv, D, bs, nb, mb, float(scale),
-            int(max_seq_len), int(single_pass_max_len), int(partition_size),
-            _dtype_code(query), _stream(query))
+            int(max_seq_len), int(max_total_tokens), int(single_pass_max_len),
+            int(partition_size), _dtype_code(query), _stream(query))
     _check(st, "pa_decode_auto_static")
     return out
 

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -77,7 +79,8 @@ EncodeTiledFn encode_fn() {
 
 // 5-D view of a cache [num_blocks][bs][Hkv][D] for TMA: (element within a
 // 64-element piece, piece index, KV head, row in block, block); one box = one
-// 64-element piece of 16 rows of one KV head (2 KB), 128-byte swizzled.
+// 64-element piece of 16 rows of one KV head (2 KB; 8 rows for block_size 8),
+// 128-byte swizzled.
 // Out-of-range boxes read zeros.
 int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv, int bs,
                    int num_blocks) {
@@ -89,7 +92,9 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
     cuuint64_t strides[4] = {64 * e, D * e, static_cast<cuuint64_t>(Hkv) * D * e,
                              static_cast<cuuint64_t>(bs) * Hkv * D * e};
 #if PA_TILE_PIECES
-    cuuint32_t box[5] = {64, 1, 1, static_cast<cuuint32_t>(kTile), 1};
+    // 16 rows of one block, or 8 (block_size 8: a tile is two 8-row boxes)
+    const cuuint32_t rows = static_cast<cuuint32_t>(bs < kTile ? bs : kTile);
+    cuuint32_t box[5] = {64, 1, 1, rows, 1};
 #else
     cuuint32_t box[5] = {64, static_cast<cuuint32_t>(D / 64), 1, static_cast<cuuint32_t>(kTile), 1};
 #endif
@@ -141,8 +146,8 @@ int check_attention(const Shape &s, pa_dtype_t dtype, const void *query, const v
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARGUMENT;
     if (s.Hq % s.Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
     if (s.D != 64 && s.D != 128 && s.D != 256) return PA_ERR_UNSUPPORTED;
-    if (s.bs % kTile != 0) return PA_ERR_UNSUPPORTED;
-    if (s.Hq / s.Hkv > kHeadsPad) return PA_ERR_UNSUPPORTED;
+    if (s.bs % kTile != 0 && !(s.bs == 8 && PA_TILE_PIECES)) return PA_ERR_UNSUPPORTED;
+    if (s.Hq / s.Hkv > kMaxGroup) return PA_ERR_UNSUPPORTED;
     if (s.S > 65535 || s.Hkv > 65535 || s.Hq > 65535) return PA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(s.max_blocks) * s.bs > INT_MAX) return PA_ERR_UNSUPPORTED;
     if (s.S == 0) return 1;
@@ -156,15 +161,28 @@ int check_attention(const Shape &s, pa_dtype_t dtype, const void *query, const v
 
 // CTAs per (sequence, KV head) of the single-pass grid: enough that the
 // launch has about PA_SINGLE_CLUSTER_FACTOR times as many CTAs as can be
-// resident, at most 8 (the portable cluster size).
+// resident, at most PA_SINGLE_CLUSTER_MAX (8, the portable cluster size).
 #ifndef PA_SINGLE_CLUSTER_FACTOR
 #define PA_SINGLE_CLUSTER_FACTOR 2
+#endif
+#ifndef PA_SINGLE_CLUSTER_MAX
+#define PA_SINGLE_CLUSTER_MAX 8
 #endif
 int single_pass_cluster(int units, int resident_ctas) {
     if (units <= 0 || resident_ctas <= 0) return 1;
     const int64_t want = static_cast<int64_t>(PA_SINGLE_CLUSTER_FACTOR) * resident_ctas;
     const int64_t c = (want + units - 1) / units;
-    return c < 1 ? 1 : (c > 8 ? 8 : static_cast<int>(c));
+    return c < 1 ? 1 : (c > PA_SINGLE_CLUSTER_MAX ? PA_SINGLE_CLUSTER_MAX : static_cast<int>(c));
+}
+
+// Query heads one decode unit holds: 8 (one MMA n-tile), or 16 (two) when the
+// GQA group is larger than 8 and head_dim is 64 or 128.  A group larger than
+// that is split into ceil(group / heads) head groups, each its own unit
+// (reading the same K/V, mostly from L2).
+int unit_heads(int D, int group) { return group > kHeadsPad && D <= 128 ? kHeadsWide : kHeadsPad; }
+int head_groups(int D, int group) {
+    const int hp = unit_heads(D, group);
+    return (group + hp - 1) / hp;
 }
 
 Params base_params(const Shape &s, const void *query, const int32_t *bt, const int32_t *sl,
@@ -183,13 +201,21 @@ Params base_params(const Shape &s, const void *query, const int32_t *bt, const i
     p.num_blocks = s.num_blocks;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.cluster = 1;
+    p.hg_count = head_groups(s.D, p.group);
     return p;
 }
 
 cudaError_t attn(pa_dtype_t dt, int D, int mode, const CUtensorMap &tk, const CUtensorMap &tv,
                  const Params &p, dim3 grid, cudaStream_t st) {
-    return dt == PA_BF16 ? launch_attn<__nv_bfloat16>(D, mode, tk, tv, p, grid, st)
-                         : launch_attn<__half>(D, mode, tk, tv, p, grid, st);
+    const int hp = unit_heads(D, p.group);
+    return dt == PA_BF16 ? launch_attn<__nv_bfloat16>(D, mode, hp, tk, tv, p, grid, st)
+                         : launch_attn<__half>(D, mode, hp, tk, tv, p, grid, st);
+}
+
+int ctas_per_sm(pa_dtype_t dt, int D, int mode, int group) {
+    const int hp = unit_heads(D, group);
+    return dt == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(D, mode, hp)
+                         : attn_ctas_per_sm<__half>(D, mode, hp);
 }
 
 cudaError_t reduce(pa_dtype_t dt, int D, bool compact, const ReduceParams &r, dim3 grid,
@@ -198,7 +224,10 @@ cudaError_t reduce(pa_dtype_t dt, int D, bool compact, const ReduceParams &r, di
                          : launch_reduce<__half>(D, compact, r, grid, st);
 }
 
-// Workspace layout of pa_decode_auto.
+// Workspace layout of pa_decode_auto.  Work-list form: counters, the work
+// list, per-sequence slot bases, the list of partitioned sequences, then the
+// compact partials [slot][Hq] (stats) and [slot][Hq][D] (tmp_out).  Dense
+// form (few sequences): the dense partials of pa_decode_partitioned.
 struct AutoLayout {
     size_t counter, units, part_base, pseq_list, exp_sums, max_logits, tmp_out, total;
     int max_parts, max_slots, max_units;
@@ -206,11 +235,43 @@ struct AutoLayout {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P, AutoLayout *L) {
-    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seq_len < 0 || P <= 0) return false;
+// Dense partials of pa_decode_partitioned in one buffer: tmp_out, exp_sums,
+// max_logits, each region 256-byte aligned.
+bool dense_layout(int S, int Hq, int D, int NP, AutoLayout *L) {
+    if (S < 0 || Hq <= 0 || D <= 0 || NP <= 0) return false;
+    const int64_t rows = static_cast<int64_t>(S) * Hq * NP;
+    if (rows * D > (static_cast<int64_t>(1) << 40)) return false;
+    L->max_parts = NP;
+    L->max_slots = 0;
+    L->max_units = 0;
+    L->counter = L->units = L->part_base = L->pseq_list = 0;
+    size_t off = 0;
+    L->tmp_out = off;
+    off = align256(off + static_cast<size_t>(rows) * D * sizeof(float));
+    L->exp_sums = off;
+    off = align256(off + static_cast<size_t>(rows) * sizeof(float));
+    L->max_logits = off;
+    off = align256(off + static_cast<size_t>(rows) * sizeof(float));
+    L->total = off;
+    return true;
+}
+
+// Work-list layout.  Partition slots: at most ceil(max_seq_len / P) per
+// partitioned sequence, and, when the caller bounds the batch's total tokens
+// T, at most floor((T + S_p (P - 1)) / P) in all, S_p <= min(S, T / (thr + 1))
+// being the most sequences that can be longer than the threshold.
+bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, long long max_total, int thr,
+                 int P, AutoLayout *L) {
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seq_len < 0 || P <= 0 || thr < 0)
+        return false;
     const int64_t parts = max_seq_len > thr ? (static_cast<int64_t>(max_seq_len) + P - 1) / P : 0;
-    const int64_t slots = static_cast<int64_t>(S) * parts;
-    const int64_t units = static_cast<int64_t>(S) * Hkv * (parts > 1 ? parts : 1);
+    int64_t slots = static_cast<int64_t>(S) * parts;
+    if (max_total > 0 && parts > 0) {
+        const int64_t sp = std::min<int64_t>(S, max_total / (static_cast<int64_t>(thr) + 1));
+        slots = std::min<int64_t>(slots, (max_total + sp * (P - 1)) / P);
+    }
+    // units: (sequence or partition) x KV head x head group
+    const int64_t units = (static_cast<int64_t>(S) + slots) * Hkv * head_groups(D, Hq / Hkv);
     if (slots * Hq > INT_MAX || units > INT_MAX) return false;
     L->max_parts = static_cast<int>(parts);
     L->max_slots = static_cast<int>(slots);
@@ -234,9 +295,108 @@ bool auto_layout(int S, int Hq, int Hkv, int D, int max_seq_len, int thr, int P,
     return true;
 }
 
+// The single-pass threshold of the launch heuristic: the pages' 8192 when the
+// batch has at least as many (sequence, KV head) units as SMs, else the
+// partition size (too few units to fill the GPU: split everything longer than
+// one partition).
 int default_thr(int S, int Hkv, int P, int num_sms) {
     const int64_t units = static_cast<int64_t>(S) * Hkv;
     return units >= static_cast<int64_t>(num_sms) ? 8192 : P;
+}
+
+// Resident attention CTAs per SM of the partitioned grid (head_dim 64 and 128:
+// 3, head_dim 256: 3; queried once from the occupancy calculator).
+int partitioned_slots_per_sm(int D) {
+    static std::atomic<int> cache[3];
+    const int k = D == 64 ? 0 : (D == 128 ? 1 : 2);
+    int v = cache[k].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = attn_ctas_per_sm<__nv_bfloat16>(D, kModePartitioned, kHeadsPad);
+        if (v <= 0) v = 3;
+        cache[k].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// The partition size of the launch heuristic: the smallest of 256, 512 and
+// 1024 tokens whose partition units (sequence x KV head x partition) fit in
+// one wave of resident CTAs, else 1024 (more than a wave of work anyway:
+// fewer, longer partitions write fewer partials).  Rounded up to a multiple
+// of the block size.  Measured on GB300 over 1..256 sequences of 1K..64K
+// tokens (one wave of 256 long units beat two waves of 512 shorter ones).
+int default_partition(int S, int Hkv, int bs, int max_seq_len, int num_sms, int slots_per_sm) {
+    const int64_t wave = static_cast<int64_t>(num_sms) * slots_per_sm;
+    int P = 1024;
+    for (int cand : {256, 512, 1024}) {
+        const int64_t units = static_cast<int64_t>(S) * Hkv * ((max_seq_len + cand - 1) / cand);
+        if (units <= wave) {
+            P = cand;
+            break;
+        }
+    }
+    if (bs > 0 && P % bs != 0) P = (P + bs - 1) / bs * bs;
+    return P;
+}
+
+// The launch form pa_decode_auto takes for a batch (host values only):
+//   single   -- every sequence fits the single-pass limit: the single-pass grid;
+//   dense    -- few (sequence, KV head) units and every sequence longer than one
+//               partition is split: the partitioned grid of pa_decode_partitioned
+//               with its partials in the workspace, then the dense reduce (two
+//               launches, no planner);
+//   worklist -- the planner's device work list (single-pass and partition units
+//               in one attention launch), then the reduce over the partitioned
+//               sequences.
+struct AutoPlan {
+    int thr, P, form;
+    bool uniform;   // the host bounds say every sequence has about max_seq_len tokens
+};
+
+// A batch whose token bound T is at least 9/10 of S * max_seq_len has nearly
+// equal lengths: one pass per (sequence, KV head) is then balanced by itself.
+bool near_uniform(int S, int max_seq_len, long long max_total) {
+    return max_total > 0 && S > 0 && max_seq_len > 0 &&
+           10 * max_total >= 9 * static_cast<long long>(S) * max_seq_len;
+}
+
+int resolve_auto(int S, int Hkv, int D, int bs, int max_seq_len, long long max_total, int thr_in,
+                 int P_in, int num_sms, AutoPlan *a) {
+    if (S < 0 || Hkv <= 0 || bs <= 0 || max_seq_len < 0 || num_sms <= 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    int P = P_in;
+    if (P <= 0)
+        P = default_partition(S, Hkv, bs, max_seq_len, num_sms,
+                              D == 64 || D == 128 || D == 256 ? partitioned_slots_per_sm(D) : 3);
+    if (P % bs != 0) return PA_ERR_UNSUPPORTED;
+    const bool uniform = near_uniform(S, max_seq_len, max_total);
+    int thr = thr_in;
+    if (thr < 0) {
+        thr = default_thr(S, Hkv, P, num_sms);
+        // enough units and (nearly) equal lengths: the single pass is balanced
+        // and writes no partials, at any length (measured on GB300 at 64 and
+        // 256 sequences of 16K-64K tokens: 2-4 % faster than partitioning)
+        if (uniform && static_cast<int64_t>(S) * Hkv >= num_sms && max_seq_len > thr)
+            thr = max_seq_len;
+    }
+    int form = PA_AUTO_WORKLIST;
+    if (max_seq_len <= thr)
+        form = PA_AUTO_SINGLE_PASS;
+    else if (thr <= P && static_cast<int64_t>(S) * Hkv < num_sms)
+        form = PA_AUTO_DENSE;
+    a->thr = thr;
+    a->P = P;
+    a->form = form;
+    a->uniform = uniform;
+    return PA_OK;
+}
+
+bool plan_layout(int S, int Hq, int Hkv, int D, int max_seq_len, long long max_total,
+                 const AutoPlan &a, AutoLayout *L) {
+    if (a.form == PA_AUTO_DENSE)
+        return dense_layout(S, Hq, D, static_cast<int>((static_cast<int64_t>(max_seq_len) + a.P - 1) /
+                                                         a.P),
+                            L);
+    return auto_layout(S, Hq, Hkv, D, max_seq_len, max_total, a.thr, a.P, L);
 }
 
 int num_sms_now() {
@@ -248,17 +408,26 @@ int num_sms_now() {
 
 // The single-pass grid: each (sequence, KV head) split over a cluster of CTAs
 // when the batch has too few units to keep every SM streaming (few or
-// unequal sequences).
+// unequal sequences).  `uniform`: the caller's bounds say the lengths are
+// nearly equal; with at least half a wave of units the units are then not
+// split (a cluster's merge and the extra CTAs' set-up cost more than the
+// balance they buy: 64 x 1024 tokens 28.7 against 38.9 us, 64 x 8192 158.8
+// against 171.0 us on GB300).
 int launch_single_pass(const Shape &s, void *out, const void *query, const int32_t *bt,
                        const int32_t *sl, float scale, pa_dtype_t dtype, const CUtensorMap &tk,
-                       const CUtensorMap &tv, const DevInfo *di, cudaStream_t st) {
+                       const CUtensorMap &tv, const DevInfo *di, cudaStream_t st,
+                       bool uniform = false) {
     Params p = base_params(s, query, bt, sl, scale, di->status);
     p.out = out;
-    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(s.D, kModeSingle)
-                                        : attn_ctas_per_sm<__half>(s.D, kModeSingle);
+    const int per_sm = ctas_per_sm(dtype, s.D, kModeSingle, p.group);
     if (per_sm <= 0) return PA_ERR_CUDA;
-    p.cluster = single_pass_cluster(s.S * s.Hkv, per_sm * di->num_sms);
-    const dim3 grid(p.cluster, s.Hkv, s.S);
+    const int vheads = s.Hkv * p.hg_count;
+    const int64_t units = static_cast<int64_t>(s.S) * vheads;
+    const int64_t resident = static_cast<int64_t>(per_sm) * di->num_sms;
+    p.cluster = uniform && 2 * units >= resident
+                    ? 1
+                    : single_pass_cluster(static_cast<int>(units), static_cast<int>(resident));
+    const dim3 grid(p.cluster, vheads, s.S);
     return attn(dtype, s.D, kModeSingle, tk, tv, p, grid, st) == cudaSuccess ? PA_OK
                                                                              : PA_ERR_CUDA;
 }
@@ -341,7 +510,7 @@ int pa_decode_partitioned(float *tmp_out, float *exp_sums, float *max_logits, co
     p.max_logits = max_logits;
     p.partition_size = partition_size;
     p.max_parts = max_num_partitions;
-    const dim3 grid(max_num_partitions, num_kv_heads, num_seqs);
+    const dim3 grid(max_num_partitions, num_kv_heads * p.hg_count, num_seqs);
     return attn(dtype, head_dim, kModePartitioned, tk, tv, p, grid,
                 static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
@@ -390,15 +559,56 @@ int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int partition
     return default_thr(num_seqs, num_kv_heads, partition_size, num_sms);
 }
 
-size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                               int max_seq_len, int single_pass_max_len, int partition_size) {
-    if (partition_size <= 0 || num_kv_heads <= 0) return 0;
-    const int thr = single_pass_max_len >= 0
-                        ? single_pass_max_len
-                        : pa_default_single_pass_max_len(num_seqs, num_kv_heads, partition_size, 0);
+int pa_default_partition_size(int num_seqs, int num_kv_heads, int block_size, int head_dim,
+                              int max_seq_len, int num_sms) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || block_size <= 0 || max_seq_len < 0) return 0;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return 0;
+    if (num_sms <= 0) num_sms = num_sms_now();
+    if (num_sms <= 0) num_sms = 1;
+    return default_partition(num_seqs, num_kv_heads, block_size, max_seq_len, num_sms,
+                             partitioned_slots_per_sm(head_dim));
+}
+
+int pa_auto_resolve(int num_seqs, int num_kv_heads, int head_dim, int block_size,
+                    int max_seq_len, long long max_total_tokens, int single_pass_max_len,
+                    int partition_size, int num_sms, int *out_single_pass_max_len,
+                    int *out_partition_size, int *out_form) {
+    if (num_sms <= 0) num_sms = num_sms_now();
+    if (num_sms <= 0) num_sms = 1;
+    AutoPlan a;
+    const int rc = resolve_auto(num_seqs, num_kv_heads, head_dim, block_size, max_seq_len,
+                                max_total_tokens, single_pass_max_len, partition_size, num_sms,
+                                &a);
+    if (rc != PA_OK) return rc;
+    if (out_single_pass_max_len) *out_single_pass_max_len = a.thr;
+    if (out_partition_size) *out_partition_size = a.P;
+    if (out_form) *out_form = a.form;
+    return PA_OK;
+}
+
+size_t pa_partition_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                    int max_num_partitions) {
     AutoLayout L;
-    if (!auto_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, thr,
-                     partition_size, &L))
+    if (!dense_layout(num_seqs, num_q_heads, head_dim, max_num_partitions, &L)) return 0;
+    return L.total;
+}
+
+size_t pa_auto_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_seq_len, long long max_total_tokens,
+                               int single_pass_max_len, int partition_size) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+    int num_sms = 0;
+    if (single_pass_max_len < 0 || partition_size <= 0) num_sms = num_sms_now();
+    if (num_sms <= 0) num_sms = 1;
+    AutoPlan a;
+    if (resolve_auto(num_seqs, num_kv_heads, head_dim, block_size, max_seq_len,
+                     max_total_tokens, single_pass_max_len, partition_size, num_sms,
+                     &a) != PA_OK)
+        return 0;
+    AutoLayout L;
+    if (a.form == PA_AUTO_SINGLE_PASS) return 256;   // no scratch is used
+    if (!plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                     max_total_tokens, a, &L))
         return 0;
     return L.total;
 }
@@ -408,33 +618,40 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
                           const int32_t *seq_lens, int num_seqs, int num_q_heads,
                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
                           int max_blocks_per_seq, float scale, int max_seq_len,
-                          int single_pass_max_len, int partition_size, void *workspace,
-                          size_t workspace_bytes, pa_dtype_t dtype, void *stream, int phases) {
+                          long long max_total_tokens, int single_pass_max_len,
+                          int partition_size, void *workspace, size_t workspace_bytes,
+                          pa_dtype_t dtype, void *stream, int phases) {
     const Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                   max_blocks_per_seq};
     int rc = check_attention(s, dtype, query, key_cache, value_cache, block_tables, seq_lens);
     if (rc < 0) return rc;
-    if (partition_size <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (max_seq_len < 0) return PA_ERR_INVALID_ARGUMENT;
     if (phases <= 0 || (phases & ~(PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE)) != 0)
         return PA_ERR_INVALID_ARGUMENT;
-    if (partition_size % block_size != 0) return PA_ERR_UNSUPPORTED;
+    if (partition_size > 0 && partition_size % block_size != 0) return PA_ERR_UNSUPPORTED;
     if (rc > 0) return PA_OK;
     if (!out) return PA_ERR_INVALID_ARGUMENT;
     if (!aligned(out, 16)) return PA_ERR_MISALIGNED;
+    // The heuristic reads the device's SM count; without a device the
+    // arguments are still checked (as pa_auto_workspace_bytes sizes them)
+    // before the missing device is reported.
     DevInfo *di = nullptr;
-    int thr = single_pass_max_len;
-    if (thr < 0) {   // the heuristic needs the device's SM count
-        if ((rc = device_info(&di)) != PA_OK) return rc;
-        thr = default_thr(num_seqs, num_kv_heads, partition_size, di->num_sms);
+    const int dev_rc = device_info(&di);
+    AutoPlan a;
+    if ((rc = resolve_auto(num_seqs, num_kv_heads, head_dim, block_size, max_seq_len,
+                           max_total_tokens, single_pass_max_len, partition_size,
+                           dev_rc == PA_OK ? di->num_sms : 1, &a)) != PA_OK)
+        return rc;
+    AutoLayout L{};
+    if (a.form != PA_AUTO_SINGLE_PASS) {
+        if (!plan_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                         max_total_tokens, a, &L))
+            return PA_ERR_INVALID_ARGUMENT;
+        if (!workspace) return PA_ERR_INVALID_ARGUMENT;
+        if (!aligned(workspace, 256)) return PA_ERR_MISALIGNED;
+        if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
     }
-    AutoLayout L;
-    if (!auto_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, thr,
-                     partition_size, &L))
-        return PA_ERR_INVALID_ARGUMENT;
-    if (!workspace) return PA_ERR_INVALID_ARGUMENT;
-    if (!aligned(workspace, 256)) return PA_ERR_MISALIGNED;
-    if (workspace_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
-    if (!di && (rc = device_info(&di)) != PA_OK) return rc;
+    if (dev_rc != PA_OK) return dev_rc;
     CUtensorMap tk, tv;
     if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
                              num_blocks)) != PA_OK)
@@ -442,24 +659,59 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
                              num_blocks)) != PA_OK)
         return rc;
-    if (L.max_parts == 0) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (a.form == PA_AUTO_SINGLE_PASS) {
         // Every sequence fits the single-pass limit: no work list and no
         // partials, just the single-pass grid (the plan and reduce phases have
         // nothing to do).
         if (!(phases & PA_PHASE_ATTEND)) return PA_OK;
         return launch_single_pass(s, out, query, block_tables, seq_lens, scale, dtype, tk, tv,
-                                  di, static_cast<cudaStream_t>(stream));
+                                  di, st, a.uniform);
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *es = reinterpret_cast<float *>(ws + L.exp_sums);
+    float *ml = reinterpret_cast<float *>(ws + L.max_logits);
+    float *tmp = reinterpret_cast<float *>(ws + L.tmp_out);
+    const int len_cap = max_blocks_per_seq * block_size;
+
+    if (a.form == PA_AUTO_DENSE) {
+        // Few sequences, each split at P: the partitioned grid and the dense
+        // reduce, as pa_decode_partitioned + pa_partition_reduce (no planner).
+        if (phases & PA_PHASE_ATTEND) {
+            Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
+            p.tmp_out = tmp;
+            p.exp_sums = es;
+            p.max_logits = ml;
+            p.partition_size = a.P;
+            p.max_parts = L.max_parts;
+            if (attn(dtype, head_dim, kModePartitioned, tk, tv, p,
+                     dim3(L.max_parts, num_kv_heads * p.hg_count, num_seqs), st) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+        if (phases & PA_PHASE_REDUCE) {
+            ReduceParams r{};
+            r.out = out;
+            r.tmp_out = tmp;
+            r.exp_sums = es;
+            r.max_logits = ml;
+            r.seq_lens = seq_lens;
+            r.status = di->status;
+            r.num_q_heads = num_q_heads;
+            r.partition_size = a.P;
+            r.max_parts = L.max_parts;
+            r.single_pass_max_len = -1;
+            r.len_cap = len_cap;
+            if (reduce(dtype, head_dim, false, r, dim3(num_q_heads, num_seqs), st) !=
+                cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+        return PA_OK;
+    }
+
     int *counter = reinterpret_cast<int *>(ws + L.counter);
     int4 *units = reinterpret_cast<int4 *>(ws + L.units);
     int32_t *part_base = reinterpret_cast<int32_t *>(ws + L.part_base);
     int4 *pseq_list = reinterpret_cast<int4 *>(ws + L.pseq_list);
-    float *es = reinterpret_cast<float *>(ws + L.exp_sums);
-    float *ml = reinterpret_cast<float *>(ws + L.max_logits);
-    float *tmp = reinterpret_cast<float *>(ws + L.tmp_out);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int len_cap = max_blocks_per_seq * block_size;
 
     PlanParams pp{};
     pp.seq_lens = seq_lens;
@@ -471,11 +723,12 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     pp.pseq_count = counter + 2;
     pp.status = di->status;
     pp.num_seqs = num_seqs;
-    pp.num_kv_heads = num_kv_heads;
-    pp.partition_size = partition_size;
-    pp.single_pass_max_len = thr;
+    pp.num_kv_heads = num_kv_heads * head_groups(head_dim, num_q_heads / num_kv_heads);
+    pp.partition_size = a.P;
+    pp.single_pass_max_len = a.thr;
     pp.len_cap = len_cap;
     pp.max_parts = L.max_parts;
+    pp.max_slots = L.max_slots;
     if ((phases & PA_PHASE_PLAN) && launch_plan(pp, st) != cudaSuccess) return PA_ERR_CUDA;
 
     Params p = base_params(s, query, block_tables, seq_lens, scale, di->status);
@@ -487,11 +740,10 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
     p.unit_counter = counter;
     p.unit_count = counter + 1;
     p.part_base = part_base;
-    p.partition_size = partition_size;
+    p.partition_size = a.P;
     p.max_parts = L.max_parts;
-    p.single_pass_max_len = thr;
-    const int per_sm = dtype == PA_BF16 ? attn_ctas_per_sm<__nv_bfloat16>(head_dim, kModeWorklist)
-                                        : attn_ctas_per_sm<__half>(head_dim, kModeWorklist);
+    p.single_pass_max_len = a.thr;
+    const int per_sm = ctas_per_sm(dtype, head_dim, kModeWorklist, p.group);
     if (per_sm <= 0) return PA_ERR_CUDA;
     int64_t ctas = static_cast<int64_t>(per_sm) * di->num_sms;
     if (ctas > L.max_units) ctas = L.max_units;
@@ -513,9 +765,9 @@ int pa_decode_auto_phases(void *out, const void *query, const void *key_cache,
         r.pseq_count = counter + 2;
         r.status = di->status;
         r.num_q_heads = num_q_heads;
-        r.partition_size = partition_size;
+        r.partition_size = a.P;
         r.max_parts = L.max_parts;
-        r.single_pass_max_len = thr;
+        r.single_pass_max_len = a.thr;
         r.len_cap = len_cap;
         // one CTA per (partitioned sequence, head): rows past the planner's
         // count exit at once
@@ -530,13 +782,13 @@ int pa_decode_auto(void *out, const void *query, const void *key_cache, const vo
                    const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                    int num_blocks, int max_blocks_per_seq, float scale, int max_seq_len,
-                   int single_pass_max_len, int partition_size, void *workspace,
-                   size_t workspace_bytes, pa_dtype_t dtype, void *stream) {
+                   long long max_total_tokens, int single_pass_max_len, int partition_size,
+                   void *workspace, size_t workspace_bytes, pa_dtype_t dtype, void *stream) {
     return pa_decode_auto_phases(out, query, key_cache, value_cache, block_tables, seq_lens,
                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  num_blocks, max_blocks_per_seq, scale, max_seq_len,
-                                 single_pass_max_len, partition_size, workspace, workspace_bytes,
-                                 dtype, stream,
+                                 max_total_tokens, single_pass_max_len, partition_size, workspace,
+                                 workspace_bytes, dtype, stream,
                                  PA_PHASE_PLAN | PA_PHASE_ATTEND | PA_PHASE_REDUCE);
 }
 

@@ -1,7 +1,6 @@
 // pa_aux.cu -- the work-list planner of the mixed decode step and the
 // block-table gather test kernel, with their launchers.
-#include "pa_kernels.cuh"
-#include "pa_launch.h"
+#include "pa_launch.cuh"
 
 namespace pa {
 
@@ -14,9 +13,14 @@ constexpr int kPlanThreads = 256;
 
 __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams pp) {
     __shared__ int s_red[2][kPlanThreads / 32];
+    grid_dep_wait();      // seq_lens are complete
+    grid_dep_trigger();   // the attention kernel may launch: it waits for this grid
     const int s = blockIdx.x;
     const int P = pp.partition_size, thr = pp.single_pass_max_len;
-    auto parts_of = [&](int L) { return L <= thr ? 0 : (L + P - 1) / P; };
+    // partitions a sequence gets: ceil(L / P), at most max_parts (the
+    // planner's prefix sums use the same clamped count, so the units and
+    // slots of the sequences stay contiguous when one is cut short)
+    auto parts_of = [&](int L) { return L <= thr ? 0 : min((L + P - 1) / P, pp.max_parts); };
     auto len_of = [&](int i) {
         int L = __ldg(pp.seq_lens + i);
         return L < 0 ? 0 : (L > pp.len_cap ? pp.len_cap : L);
@@ -68,11 +72,16 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
         if (threadIdx.x == 0) pp.part_base[s] = -1;
     } else {
         int np = (L + P - 1) / P;
-        if (np > pp.max_parts) {   // the workspace was sized for fewer partitions
+        // The workspace was sized for at most max_parts partitions per
+        // sequence and max_slots in all (the caller's bounds on the longest
+        // sequence and on the batch's tokens): partitions past either bound
+        // are dropped and flagged.
+        const int room = slots_before < pp.max_slots ? pp.max_slots - slots_before : 0;
+        if (np > pp.max_parts || np > room) {
             if (threadIdx.x == 0) atomicOr(pp.status, kTooManyParts);
-            np = pp.max_parts;
+            np = min(np, min(pp.max_parts, room));
         }
-        const int base_unit = singles_all * Hkv + slots_before * Hkv;
+        const int base_unit = singles_all * Hkv + min(slots_before, pp.max_slots) * Hkv;
         for (int k = threadIdx.x; k < np * Hkv; k += kPlanThreads)
             pp.units[base_unit + k] = make_int4(s, k % Hkv, k / Hkv, kOutPartialCompact);
         if (threadIdx.x == 0) {
@@ -82,7 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
         }
     }
     if (s == 0 && threadIdx.x == 0) {
-        *pp.unit_count = (singles_all + slots_all) * Hkv;
+        *pp.unit_count = (singles_all + min(slots_all, pp.max_slots)) * Hkv;
         *pp.unit_counter = 0;
         *pp.pseq_count = pp.num_seqs - singles_all;
     }
@@ -113,13 +122,21 @@ __global__ void __launch_bounds__(32)
         fence_mbar_init();
     }
     __syncwarp();
-    const int b = __ldg(gp.block_tables + static_cast<size_t>(s) * gp.max_blocks + tt / gp.block_size);
+    const int32_t *bt_row = gp.block_tables + static_cast<size_t>(s) * gp.max_blocks;
+    const bool split = gp.block_size < kTile;   // block_size 8: two blocks per tile
+    const int b = __ldg(bt_row + tt / gp.block_size);
+    // second block of a block-size-8 tile, when the tile reaches into it
+    const bool need2 = split && tt + 8 < Lc;
+    const int b2 = need2 ? __ldg(bt_row + tt / gp.block_size + 1) : -1;
     if (lane == 0) {
         if (static_cast<unsigned>(b) >= static_cast<unsigned>(gp.num_blocks))
             atomicOr(gp.status, kBadBlock);
+        if (need2 && static_cast<unsigned>(b2) >= static_cast<unsigned>(gp.num_blocks))
+            atomicOr(gp.status, kBadBlock);
+        const int row = split ? 0 : tt % gp.block_size;
         mbar_expect_tx(bar, 2 * kTileBytes);
-        tma_load_tile<D>(smem_u32(smem), &tmK, bar, kvh, tt % gp.block_size, b);
-        tma_load_tile<D>(smem_u32(smem) + kTileBytes, &tmV, bar, kvh, tt % gp.block_size, b);
+        tma_load_tile<D>(smem_u32(smem), &tmK, bar, kvh, row, b, b2, split);
+        tma_load_tile<D>(smem_u32(smem) + kTileBytes, &tmV, bar, kvh, row, b, b2, split);
     }
     if (!mbar_wait_bounded(bar, 0)) {
         if (lane == 0) atomicOr(gp.status, kWaitTimeout);
@@ -160,8 +177,9 @@ cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, c
 
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st) {
     if (pp.num_seqs <= 0) return cudaSuccess;
-    pa_plan_kernel<<<pp.num_seqs, kPlanThreads, 0, st>>>(pp);
-    return cudaGetLastError();
+    const cudaError_t e = launch_dependent(pa_plan_kernel, dim3(pp.num_seqs), dim3(kPlanThreads),
+                                           0, st, nullptr, pp);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D>

@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Programmatic dependent launch: the decode step's kernels are launched so the
+// next one may start while the previous one drains.  A kernel waits, before
+// its first global access, until the previous grid in the stream has
+// completed with its memory visible (a no-op when launched without the
+// attribute), and lets the next grid launch once its own work is done.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -203,17 +213,23 @@ __device__ __forceinline__ uint32_t row_piece_offset(int row, int c) {
                       : static_cast<uint32_t>((row * (D / 64) + c) * 128);
 }
 
-// Load one 16-row tile of (block b, rows row..row+15, KV head kvh), all
-// completing on `bar`: one TMA per 64-element piece, or one for the tile.
+// Load one 16-row tile of KV head kvh, all completing on `bar`: rows
+// row..row+15 of block b0 (block_size >= 16: one box of 16 rows per 64-element
+// piece), or, with `split` (block_size 8), rows 0..7 of block b0 and rows 0..7
+// of block b1 as two 8-row boxes per piece.  The second box lands 1024 bytes
+// into the piece, on a whole 128-byte-swizzle period, so both halves have the
+// layout of one 16-row box.
 template <int D>
 __device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                              int kvh, int row, int b) {
+                                              int kvh, int row, int b0, int b1, bool split) {
     if constexpr (kPiecewise) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-            tma_load_5d(dst + c * kPieceBytes, map, bar, 0, c, kvh, row, b);
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_5d(dst + c * kPieceBytes, map, bar, 0, c, kvh, row, b0);
+            if (split) tma_load_5d(dst + c * kPieceBytes + 1024, map, bar, 0, c, kvh, 0, b1);
+        }
     } else {
-        tma_load_5d(dst, map, bar, 0, 0, kvh, row, b);
+        tma_load_5d(dst, map, bar, 0, 0, kvh, row, b0);   // block_size 8 is refused on the host
     }
 }
 
@@ -250,19 +266,37 @@ __device__ __forceinline__ int clamp_len(const int32_t *seq_lens, int s, int cap
     return L;
 }
 
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_s32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory plan of the attention kernel
 // ---------------------------------------------------------------------------
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, int HP>
 struct Smem {
     static constexpr int kTileBytes = kTile * D * 2;            // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
     static constexpr int kStagesBytes = NW * NS * kStageBytes;
-    static constexpr int kMergeBytes = NW * kHeadsPad * (D + 2) * 4;
-    // CTA result handed to the cluster leader: o [8][D], m [8], l [8], abort flag
-    static constexpr int kClusterOffset = (kMergeBytes + 15) / 16 * 16;
-    static constexpr int kClusterBytes = kHeadsPad * (D + 2) * 4 + 16;
-    static constexpr int kUsed = kClusterOffset + kClusterBytes;
+    static constexpr int kMergeBytes = NW * HP * (D + 2) * 4;
+    // Cluster merge of the single-pass grid: CTA r of the cluster finishes the
+    // r-th slice of the unit's output elements, so it receives from every CTA
+    // (itself included) that CTA's merged values of the slice, o_in
+    // [rank][slice] (at most HP * D + 8 floats for any cluster size), and its
+    // per-head maximum and sum, m_in / l_in [rank][HP], and abort flag.
+    // Written only after every CTA of the cluster has finished with its stages
+    // and its own merge area, so it overlaps both.
+    static constexpr int kMaxCluster = 8;
+    static constexpr int kInO = 0;
+    static constexpr int kInM = kInO + (HP * D + kMaxCluster) * 4;
+    static constexpr int kInL = kInM + kMaxCluster * HP * 4;
+    static constexpr int kInAbort = kInL + kMaxCluster * HP * 4;
+    static constexpr int kClusterEnd = kInAbort + kMaxCluster * 4;
+    static constexpr int kUsed = kMergeBytes > kClusterEnd ? kMergeBytes : kClusterEnd;
     static constexpr int kBarOffset =
         ((kStagesBytes > kUsed ? kStagesBytes : kUsed) + 15) / 16 * 16;
     static constexpr int kBytes = kBarOffset + NW * NS * 8 + 16;
@@ -270,83 +304,124 @@ struct Smem {
 };
 
 // ---------------------------------------------------------------------------
-// One work unit: tokens [t0, t1) of (seq, kvh), all heads of the GQA group.
+// One work unit: tokens [t0, t1) of (seq, head group v), v = (KV head kvh,
+// head group hg) with kvh = v / hg_count: the query heads hg*HP .. hg*HP+HP-1
+// of kvh's GQA group (all of them when the group has at most HP heads), so a
+// K/V byte is read once per head group.  HP = 8 or 16 heads: one or two n8
+// tiles of the warp MMAs.
+// `span()` gives t1 once the unit's first loads are in flight: the block-table
+// window and the query fragments do not wait for the sequence length, so the
+// length read and the table reads overlap.  A negative t1 means the unit does
+// not exist (a partition past the sequence end): nothing is written.
 // With a cluster of `csize` CTAs (single-pass grid only), CTA `crank` takes
-// every csize-th group of NW tiles and the leader merges the CTAs' states
-// through distributed shared memory.  Returns false if a pipeline wait gave
-// up (the CTA must stop).
+// every csize-th group of NW tiles and the other CTAs push their merged
+// states into the leader's shared memory, which writes the output.  Returns
+// false if a pipeline wait gave up (the CTA must stop).
 // ---------------------------------------------------------------------------
-template <typename T, int D, int NW, int NS>
+template <typename T, int D, int NW, int NS, int HP, typename Span>
 __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *tmK,
                                             const CUtensorMap *tmV, uint8_t *smem, uint32_t bar0,
-                                            uint32_t &uses, int seq, int kvh, int t0, int t1,
+                                            uint32_t &uses, int seq, int vkh, int t0, Span span,
                                             int out_kind, int part, int slot, int *s_abort,
                                             int crank = 0, int csize = 1) {
-    using SM = Smem<D, NW, NS>;
+    using SM = Smem<D, NW, NS, HP>;
     constexpr int KT = D / 16;   // k-steps of S^T, m-tiles of O^T
+    constexpr int NT8 = HP / 8;  // n8 tiles (heads) of S^T and O^T
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int g = p.group;
-    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int kvh = vkh / p.hg_count;
+    const int h0 = (vkh - kvh * p.hg_count) * HP;        // first head of the group
+    const int gh = min(HP, p.group - h0);                // heads of this unit
+    const int qhead0 = kvh * p.group + h0;               // its first query head
     const int woff = crank * NW + warp;    // this warp's first tile
     const int wstride = csize * NW;        // tiles between two of this warp's tiles
-    const int my_tiles = woff < ntiles ? (ntiles - woff + wstride - 1) / wstride : 0;
     const int32_t *bt_row = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
+    const bool split = p.block_size < kTile;   // block_size 8: two blocks per tile
 
-    // Block-table window: lane l holds the physical block of local tile base+l.
-    auto fetch = [&](int i) -> int {
-        if (i >= my_tiles) return 0;
-        const int tok = t0 + (woff + i * wstride) * kTile;
-        const int b = __ldg(bt_row + tok / p.block_size);
-        if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
-            atomicOr(p.status, kBadBlock);
-        return b;
+    // Block-table window: lane l holds the entry of local tile base+l (with
+    // block_size 8, of the tile's first block; the second is the next entry).
+    // Reads are bounded by the table row, not by the length, which is not
+    // known yet; an entry is checked against the cache when its tile is issued.
+    auto entry = [&](long long j) -> int { return j < p.max_blocks ? __ldg(bt_row + j) : 0; };
+    auto fetch = [&](int i, int second) -> int {
+        const long long tok = t0 + (static_cast<long long>(woff) + static_cast<long long>(i) *
+                                                                        wstride) * kTile;
+        return entry(tok / p.block_size + second);
     };
-    int win_cur = fetch(lane);
-    int win_next = fetch(32 + lane);
+    int win_cur = fetch(lane, 0);
+    int win_next = fetch(32 + lane, 0);
+    int win2_cur = split ? fetch(lane, 1) : 0;
+    int win2_next = split ? fetch(32 + lane, 1) : 0;
     int win_base = 0;
-    auto phys_of = [&](int i) -> int {   // warp-uniform, called with i = 0, 1, 2, ...
+
+    // Query fragments (the B operand of S^T = K Q^T): lane holds head
+    // lane/4 + 8 nt of the unit, dims 2*(lane%4)+{0,1} and +8 of every 16-dim
+    // step; padded heads are 0.
+    uint32_t qf[NT8][KT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+        const int h = (lane >> 2) + 8 * nt;
+        const T *qrow = static_cast<const T *>(p.q) +
+                        (static_cast<size_t>(seq) * p.num_q_heads + qhead0 + (h < gh ? h : 0)) * D;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            qf[nt][kk][0] = h < gh ? __ldg(q32 + (kk * 16 + 2 * (lane & 3)) / 2) : 0u;
+            qf[nt][kk][1] = h < gh ? __ldg(q32 + (kk * 16 + 8 + 2 * (lane & 3)) / 2) : 0u;
+        }
+    }
+
+    const int t1 = span();
+    if (t1 < 0) return true;   // CTA-uniform: every thread resolves the same span
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int my_tiles = woff < ntiles ? (ntiles - woff + wstride - 1) / wstride : 0;
+
+    auto advance = [&](int i) {   // warp-uniform, called with i = 0, 1, 2, ...
         if (i - win_base >= 32) {
             win_cur = win_next;
+            win2_cur = win2_next;
             win_base += 32;
-            win_next = fetch(win_base + 32 + lane);
+            win_next = fetch(win_base + 32 + lane, 0);
+            if (split) win2_next = fetch(win_base + 32 + lane, 1);
         }
-        return __shfl_sync(0xffffffffu, win_cur, i - win_base);
     };
 
     const uint32_t stage0 = smem_u32(smem) + warp * NS * SM::kStageBytes;
     auto issue = [&](int i) {
-        const int b = phys_of(i);
+        advance(i);
+        const int b = __shfl_sync(0xffffffffu, win_cur, i - win_base);
+        int b2 = split ? __shfl_sync(0xffffffffu, win2_cur, i - win_base) : 0;
         if (lane == 0) {
+            const int tt = t0 + (woff + i * wstride) * kTile;
+            // an entry outside the cache becomes an out-of-range TMA box (zeros)
+            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
+                atomicOr(p.status, kBadBlock);
+            if (split) {
+                // the second block only when the tile reaches into it; else an
+                // out-of-range box (zeros, never read: its rows are masked)
+                if (tt + 8 >= t1)
+                    b2 = -1;
+                else if (static_cast<unsigned>(b2) >= static_cast<unsigned>(p.num_blocks))
+                    atomicOr(p.status, kBadBlock);
+            }
             const uint32_t st = (uses + i) % NS;
             const uint32_t bar = bar0 + (warp * NS + st) * 8;
             const uint32_t dk = stage0 + st * SM::kStageBytes;
-            const int row = (t0 + (woff + i * wstride) * kTile) % p.block_size;
+            const int row = split ? 0 : tt % p.block_size;
             mbar_expect_tx(bar, SM::kStageBytes);
-            tma_load_tile<D>(dk, tmK, bar, kvh, row, b);
-            tma_load_tile<D>(dk + SM::kTileBytes, tmV, bar, kvh, row, b);
+            tma_load_tile<D>(dk, tmK, bar, kvh, row, b, b2, split);
+            tma_load_tile<D>(dk + SM::kTileBytes, tmV, bar, kvh, row, b, b2, split);
         }
     };
 
-    // Query fragments (the B operand of S^T = K Q^T): lane holds head lane/4,
-    // dims 2*(lane%4)+{0,1} and +8 of every 16-dim step; padded heads are 0.
-    uint32_t qf[KT][2];
-    {
-        const int h = lane >> 2;
-        const T *qrow = static_cast<const T *>(p.q) +
-                        (static_cast<size_t>(seq) * p.num_q_heads + kvh * g + (h < g ? h : 0)) * D;
-        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+    float o[KT][NT8][4];
 #pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            qf[kk][0] = h < g ? __ldg(q32 + (kk * 16 + 2 * (lane & 3)) / 2) : 0u;
-            qf[kk][1] = h < g ? __ldg(q32 + (kk * 16 + 8 + 2 * (lane & 3)) / 2) : 0u;
-        }
-    }
-
-    float o[KT][4];
+    for (int mt = 0; mt < KT; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        for (int nt = 0; nt < NT8; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    float m[NT8][2], l[NT8][2];
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
 
     const int mi = lane >> 3, ri = lane & 7;
     const int rowK = (mi & 1) * 8 + ri, hiK = mi >> 1;   // S^T A operand (K, row-major)
@@ -386,49 +461,57 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
             __syncwarp();
         }
 
-        // S^T[16 tokens][8 heads] = K[16][D] . Q^T[D][8]
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T[16 tokens][HP heads] = K[16][D] . Q^T[D][HP]
+        float sacc[NT8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
             uint32_t a[4];
             ldsm_x4(a, kb + swz<D>(rowK, kk * 16 + hiK * 8));
-            Mma<T>::run(s, a, qf[kk][0], qf[kk][1]);
-        }
-        // lane: tokens r0 and r0+8, heads 2*(lane%4) and +1; log2-domain logits
-        const float y0 = r0 < nvalid ? s[0] * p.scale_log2 : -INFINITY;
-        const float y1 = r0 < nvalid ? s[1] * p.scale_log2 : -INFINITY;
-        const float y2 = r0 + 8 < nvalid ? s[2] * p.scale_log2 : -INFINITY;
-        const float y3 = r0 + 8 < nvalid ? s[3] * p.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
 #pragma unroll
-        for (int x = 4; x < 32; x <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            for (int nt = 0; nt < NT8; ++nt) Mma<T>::run(sacc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);
-        const float p0 = ex2(y0 - mn0), p1 = ex2(y1 - mn1);
-        const float p2 = ex2(y2 - mn0), p3 = ex2(y3 - mn1);
-        l0 = l0 * a0 + (p0 + p2);
-        l1 = l1 * a1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
+        uint32_t pb0[NT8], pb1[NT8];
 #pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-            o[mt][0] *= a0;
-            o[mt][1] *= a1;
-            o[mt][2] *= a0;
-            o[mt][3] *= a1;
+        for (int nt = 0; nt < NT8; ++nt) {
+            // lane: tokens r0 and r0+8, heads 2*(lane%4)+{0,1} of n-tile nt
+            const float y0 = r0 < nvalid ? sacc[nt][0] * p.scale_log2 : -INFINITY;
+            const float y1 = r0 < nvalid ? sacc[nt][1] * p.scale_log2 : -INFINITY;
+            const float y2 = r0 + 8 < nvalid ? sacc[nt][2] * p.scale_log2 : -INFINITY;
+            const float y3 = r0 + 8 < nvalid ? sacc[nt][3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(y0, y2), mx1 = fmaxf(y1, y3);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+            const float a0 = ex2(m[nt][0] - mn0), a1 = ex2(m[nt][1] - mn1);
+            const float p0 = ex2(y0 - mn0), p1 = ex2(y1 - mn1);
+            const float p2 = ex2(y2 - mn0), p3 = ex2(y3 - mn1);
+            l[nt][0] = l[nt][0] * a0 + (p0 + p2);
+            l[nt][1] = l[nt][1] * a1 + (p1 + p3);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                o[mt][nt][0] *= a0;
+                o[mt][nt][1] *= a1;
+                o[mt][nt][2] *= a0;
+                o[mt][nt][3] *= a1;
+            }
+            // P^T operand: transpose the (token, head) pairs into (head, token) pairs.
+            pb0[nt] = movmatrix_t(Mma<T>::pack(p0, p1));
+            pb1[nt] = movmatrix_t(Mma<T>::pack(p2, p3));
         }
-        // P^T operand: transpose the (token, head) pairs into (head, token) pairs.
-        const uint32_t b0 = movmatrix_t(Mma<T>::pack(p0, p1));
-        const uint32_t b1 = movmatrix_t(Mma<T>::pack(p2, p3));
-        // O^T[D][8 heads] += V^T[D][16] . P^T[16][8]
+        // O^T[D][HP heads] += V^T[D][16] . P^T[16][HP]
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
             uint32_t a[4];
             ldsm_x4_t(a, vb + swz<D>(rowV, mt * 16 + hiV * 8));
-            Mma<T>::run(o[mt], a, b0, b1);
+#pragma unroll
+            for (int nt = 0; nt < NT8; ++nt) Mma<T>::run(o[mt][nt], a, pb0[nt], pb1[nt]);
         }
         __syncwarp();
         if (i + NS < my_tiles) issue(i + NS);
@@ -438,109 +521,161 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
 
     // Per-lane exp-sums cover the lane's tokens: sum over the 8 lanes of a head.
 #pragma unroll
-    for (int x = 4; x < 32; x <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
-    }
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], x);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], x);
+        }
 
     __syncthreads();   // every warp is done reading its stages
-    float *sm_o = reinterpret_cast<float *>(smem);              // [NW][8][D]
-    float *sm_m = sm_o + NW * kHeadsPad * D;                     // [NW][8]
-    float *sm_l = sm_m + NW * kHeadsPad;                         // [NW][8]
-    if (lane < 4) {
-        sm_m[warp * kHeadsPad + 2 * lane] = m0;
-        sm_m[warp * kHeadsPad + 2 * lane + 1] = m1;
-        sm_l[warp * kHeadsPad + 2 * lane] = l0;
-        sm_l[warp * kHeadsPad + 2 * lane + 1] = l1;
-    }
-    {
-        const int h0 = 2 * (lane & 3);
-        float *w0 = sm_o + (warp * kHeadsPad + h0) * D;
+    float *sm_o = reinterpret_cast<float *>(smem);              // [NW][HP][D]
+    float *sm_m = sm_o + NW * HP * D;                            // [NW][HP]
+    float *sm_l = sm_m + NW * HP;                                // [NW][HP]
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+        const int hb = 8 * nt + 2 * (lane & 3);
+        if (lane < 4) {
+            sm_m[warp * HP + hb] = m[nt][0];
+            sm_m[warp * HP + hb + 1] = m[nt][1];
+            sm_l[warp * HP + hb] = l[nt][0];
+            sm_l[warp * HP + hb + 1] = l[nt][1];
+        }
+        float *w0 = sm_o + (warp * HP + hb) * D;
         float *w1 = w0 + D;
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
             const int dim = mt * 16 + r0;
-            w0[dim] = o[mt][0];
-            w1[dim] = o[mt][1];
-            w0[dim + 8] = o[mt][2];
-            w1[dim + 8] = o[mt][3];
+            w0[dim] = o[mt][nt][0];
+            w1[dim] = o[mt][nt][1];
+            w0[dim + 8] = o[mt][nt][2];
+            w1[dim + 8] = o[mt][nt][3];
         }
     }
     __syncthreads();
     const bool write = (*s_abort == 0);
     const int Hq = p.num_q_heads;
-    // Cluster mode: each CTA parks its merged state for the leader instead of
-    // writing the output.
-    const bool to_leader = csize > 1;
-    float *cl_o = reinterpret_cast<float *>(smem + SM::kClusterOffset);   // [8][D]
-    float *cl_m = cl_o + kHeadsPad * D;                                    // [8]
-    float *cl_l = cl_m + kHeadsPad;                                        // [8]
-    int *cl_abort = reinterpret_cast<int *>(cl_l + kHeadsPad);
-    for (int e = threadIdx.x; e < g * D && write; e += NW * 32) {
-        const int h = e / D, dim = e - (e / D) * D;
+    constexpr int NT = NW * 32;
+    constexpr int KE = (HP * D + NT - 1) / NT;   // output elements per thread, at most
+    const bool clustered = csize > 1;
+    // Per head: the merged maximum M and sum L of the warps' states, and the
+    // weight of each warp's normalised output, exp(m_w - M) / L * (its own
+    // sum, folded into o_w), so that an output element is a plain weighted
+    // sum of the warps' o_w: one pass over the heads, not one per element.
+    __shared__ float s_coef[NW][HP];
+    __shared__ float s_hm[HP], s_hl[HP];
+    if (threadIdx.x < gh) {
+        const int h = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * kHeadsPad + h]);
-        float Ls = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * HP + h]);
+        float c[NW], L = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float wt = ex2(sm_m[w * kHeadsPad + h] - M);
-                Ls += wt * sm_l[w * kHeadsPad + h];
-                acc += wt * sm_o[(w * kHeadsPad + h) * D + dim];
-            }
+        for (int w = 0; w < NW; ++w) {
+            c[w] = M != -INFINITY ? ex2(sm_m[w * HP + h] - M) : 0.f;
+            L += c[w] * sm_l[w * HP + h];
         }
-        const float res = Ls > 0.f ? acc / Ls : 0.f;
-        const int head = kvh * g + h;
-        if (to_leader) {
-            cl_o[h * D + dim] = res;
-            if (dim == 0) {
-                cl_m[h] = M;
-                cl_l[h] = Ls;
-            }
-        } else if (out_kind == kOutFinal) {
-            static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + head) * D + dim] =
-                Mma<T>::cvt(res);
-        } else {
-            size_t srow;
-            if (out_kind == kOutPartialDense)
-                srow = (static_cast<size_t>(seq) * Hq + head) * p.max_parts + part;
-            else
-                srow = static_cast<size_t>(slot) * Hq + head;
-            p.tmp_out[srow * D + dim] = res;
-            if (dim == 0) {
-                p.exp_sums[srow] = Ls;
-                p.max_logits[srow] = M == -INFINITY ? -INFINITY : M * kLn2;
-            }
-        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s_coef[w][h] = c[w] * inv;
+        s_hm[h] = M;
+        s_hl[h] = L;
     }
-    if (to_leader) {
-        if (threadIdx.x == 0) *cl_abort = write ? 0 : 1;
-        cluster_sync();   // every CTA's state is in its shared memory
-        if (crank == 0) {
-            bool any_abort = false;
-            for (int r = 0; r < csize; ++r)
-                any_abort |= dsmem_ld_s32(dsmem_addr(smem_u32(cl_abort), r)) != 0;
-            for (int e = threadIdx.x; e < g * D && !any_abort; e += NW * 32) {
-                const int h = e / D, dim = e - (e / D) * D;
-                float M = -INFINITY;
-                for (int r = 0; r < csize; ++r)
-                    M = fmaxf(M, dsmem_ld_f32(dsmem_addr(smem_u32(cl_m + h), r)));
-                float Ls = 0.f, acc = 0.f;
-                if (M != -INFINITY) {
-                    for (int r = 0; r < csize; ++r) {
-                        const float mr = dsmem_ld_f32(dsmem_addr(smem_u32(cl_m + h), r));
-                        const float wt =
-                            ex2(mr - M) * dsmem_ld_f32(dsmem_addr(smem_u32(cl_l + h), r));
-                        Ls += wt;
-                        acc += wt * dsmem_ld_f32(dsmem_addr(smem_u32(cl_o + h * D + dim), r));
-                    }
+    __syncthreads();
+    auto merged = [&](int h, int dim) -> float {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) acc += s_coef[w][h] * sm_o[(w * HP + h) * D + dim];
+        return acc;
+    };
+    if (!clustered) {
+        for (int e = threadIdx.x; e < gh * D && write; e += NT) {
+            const int h = e / D, dim = e - (e / D) * D;
+            const float res = merged(h, dim);
+            const int head = qhead0 + h;
+            if (out_kind == kOutFinal) {
+                static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + head) * D + dim] =
+                    Mma<T>::cvt(res);
+            } else {
+                size_t srow;
+                if (out_kind == kOutPartialDense)
+                    srow = (static_cast<size_t>(seq) * Hq + head) * p.max_parts + part;
+                else
+                    srow = static_cast<size_t>(slot) * Hq + head;
+                p.tmp_out[srow * D + dim] = res;
+                if (dim == 0) {
+                    p.exp_sums[srow] = s_hl[h];
+                    p.max_logits[srow] = s_hm[h] == -INFINITY ? -INFINITY : s_hm[h] * kLn2;
                 }
-                static_cast<T *>(p.out)[(static_cast<size_t>(seq) * Hq + kvh * g + h) * D + dim] =
-                    Mma<T>::cvt(Ls > 0.f ? acc / Ls : 0.f);
             }
         }
-        cluster_sync();   // the leader has finished reading the other CTAs
+    } else {
+        // this CTA's merged output for the thread's elements, kept in registers
+        float keep[KE];
+#pragma unroll
+        for (int k = 0; k < KE; ++k) {
+            const int e = threadIdx.x + k * NT;
+            keep[k] = e < gh * D ? merged(e / D, e - (e / D) * D) : 0.f;
+        }
+        cluster_sync();   // every CTA is done with its stages and its merge area
+        // send each of this CTA's values to the CTA that finishes its slice
+        const int E = gh * D;
+        const int slice = (E + csize - 1) / csize;
+        const uint32_t base = smem_u32(smem);
+        if (write) {
+#pragma unroll
+            for (int k = 0; k < KE; ++k) {
+                const int e = threadIdx.x + k * NT;
+                if (e < E) {
+                    const int owner = e / slice;
+                    dsmem_st_f32(dsmem_addr(base + SM::kInO + (crank * slice + e - owner * slice) * 4,
+                                            owner),
+                                 keep[k]);
+                }
+            }
+            for (int t = threadIdx.x; t < csize * gh; t += NT) {
+                const int dst = t / gh, h = t - dst * gh;
+                dsmem_st_f32(dsmem_addr(base + SM::kInM + (crank * HP + h) * 4, dst), s_hm[h]);
+                dsmem_st_f32(dsmem_addr(base + SM::kInL + (crank * HP + h) * 4, dst), s_hl[h]);
+            }
+        }
+        if (threadIdx.x < csize)
+            dsmem_st_s32(dsmem_addr(base + SM::kInAbort + crank * 4, threadIdx.x), write ? 0 : 1);
+        cluster_sync();   // every CTA's values of this CTA's slice have arrived
+        const float *in_o = reinterpret_cast<const float *>(smem + SM::kInO);
+        const float *in_m = reinterpret_cast<const float *>(smem + SM::kInM);
+        const float *in_l = reinterpret_cast<const float *>(smem + SM::kInL);
+        const int *in_abort = reinterpret_cast<const int *>(smem + SM::kInAbort);
+        bool any_abort = false;
+        for (int r = 0; r < csize; ++r) any_abort |= in_abort[r] != 0;
+        const int e0 = crank * slice, e1 = min(e0 + slice, E);
+        if (!any_abort && e0 < e1) {
+            // per head of the slice: the weight of each CTA's normalised output
+            __shared__ float s_cw[SM::kMaxCluster][HP];
+            const int h_lo = e0 / D, h_hi = (e1 - 1) / D;
+            if (threadIdx.x <= h_hi - h_lo) {
+                const int h = h_lo + threadIdx.x;
+                float M = -INFINITY;
+                for (int r = 0; r < csize; ++r) M = fmaxf(M, in_m[r * HP + h]);
+                float L = 0.f;
+                for (int r = 0; r < csize; ++r) {
+                    const float w = M != -INFINITY ? ex2(in_m[r * HP + h] - M) * in_l[r * HP + h]
+                                                   : 0.f;
+                    s_cw[r][h] = w;
+                    L += w;
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                for (int r = 0; r < csize; ++r) s_cw[r][h] *= inv;
+            }
+            __syncthreads();
+            T *orow = static_cast<T *>(p.out) + (static_cast<size_t>(seq) * Hq + qhead0) * D;
+            for (int e = e0 + threadIdx.x; e < e1; e += NT) {
+                const int h = e / D;
+                float acc = 0.f;
+                for (int r = 0; r < csize; ++r) acc += s_cw[r][h] * in_o[r * slice + e - e0];
+                orow[e] = Mma<T>::cvt(acc);
+            }
+        }
     }
     // The merge wrote this memory through the generic proxy; order those
     // writes before any later TMA into it, then let every thread finish.
@@ -551,12 +686,13 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
 
 // ---------------------------------------------------------------------------
 // Attention kernel: single-pass grid, partitioned grid, or persistent work list.
+// Grid y / the units' second field index (KV head, head group) pairs.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int NW, int NS, int MODE>
+template <typename T, int D, int NW, int NS, int MODE, int HP>
 __global__ void __launch_bounds__(NW * 32)
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
-    using SM = Smem<D, NW, NS>;
+    using SM = Smem<D, NW, NS, HP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -571,29 +707,34 @@ __global__ void __launch_bounds__(NW * 32)
     if (threadIdx.x < NW * NS) mbar_init(bar0 + threadIdx.x * 8, 1);
     fence_mbar_init();
     __syncthreads();
+    grid_dep_wait();   // inputs (and the work list) are complete from here on
 
     uint32_t uses = 0;
     const int cap = p.max_blocks * p.block_size;
     if constexpr (MODE == kModeSingle) {
-        // grid (cluster size, Hkv, S); the CTAs of one cluster share a unit
-        const int crank = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-        const int L = clamp_len(p.seq_lens, seq, cap, p.status);
-        attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, 0, L, kOutFinal, 0,
-                                  0, &s_abort, crank, p.cluster);
+        // grid (cluster size, Hkv x head groups, S); the CTAs of one cluster share a unit
+        const int crank = blockIdx.x, vkh = blockIdx.y, seq = blockIdx.z;
+        attend_unit<T, D, NW, NS, HP>(
+            p, &tmK, &tmV, smem, bar0, uses, seq, vkh, 0,
+            [&]() { return clamp_len(p.seq_lens, seq, cap, p.status); }, kOutFinal, 0, 0,
+            &s_abort, crank, p.cluster);
     } else if constexpr (MODE == kModePartitioned) {
-        const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-        const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+        const int part = blockIdx.x, vkh = blockIdx.y, seq = blockIdx.z;
         const int P = p.partition_size;
-        int n = (L + P - 1) / P;
-        if (n > p.max_parts) {
-            if (part == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kTooManyParts);
-            n = p.max_parts;
-        }
-        if (part >= n) return;
         const int t0 = part * P;
-        const int t1 = min(t0 + P, L);
-        attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, t0, t1,
-                                  kOutPartialDense, part, 0, &s_abort);
+        attend_unit<T, D, NW, NS, HP>(
+            p, &tmK, &tmV, smem, bar0, uses, seq, vkh, t0,
+            [&]() {
+                const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+                int n = (L + P - 1) / P;
+                if (n > p.max_parts) {
+                    if (part == 0 && vkh == 0 && threadIdx.x == 0)
+                        atomicOr(p.status, kTooManyParts);
+                    n = p.max_parts;
+                }
+                return part < n ? min(t0 + P, L) : -1;
+            },
+            kOutPartialDense, part, 0, &s_abort);
     } else {
         const int total = *p.unit_count;
         if (threadIdx.x == 0) s_next = atomicAdd(p.unit_counter, 1);
@@ -603,19 +744,20 @@ __global__ void __launch_bounds__(NW * 32)
             int nxt = 0;
             if (threadIdx.x == 0) nxt = atomicAdd(p.unit_counter, 1);   // prefetch the next unit
             const int4 d = p.units[u];
-            const int seq = d.x, kvh = d.y, part = d.z, kind = d.w;
-            const int L = clamp_len(p.seq_lens, seq, cap, p.status);
+            const int seq = d.x, vkh = d.y, part = d.z, kind = d.w;
             bool ok;
             if (kind == kOutFinal) {
-                ok = attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, 0, L,
-                                               kOutFinal, 0, 0, &s_abort);
+                ok = attend_unit<T, D, NW, NS, HP>(
+                    p, &tmK, &tmV, smem, bar0, uses, seq, vkh, 0,
+                    [&]() { return clamp_len(p.seq_lens, seq, cap, p.status); }, kOutFinal, 0, 0,
+                    &s_abort);
             } else {
                 const int P = p.partition_size;
                 const int t0 = part * P;
-                const int t1 = min(t0 + P, L);
-                ok = attend_unit<T, D, NW, NS>(p, &tmK, &tmV, smem, bar0, uses, seq, kvh, t0, t1,
-                                               kOutPartialCompact, part,
-                                               __ldg(p.part_base + seq) + part, &s_abort);
+                ok = attend_unit<T, D, NW, NS, HP>(
+                    p, &tmK, &tmV, smem, bar0, uses, seq, vkh, t0,
+                    [&]() { return min(t0 + P, clamp_len(p.seq_lens, seq, cap, p.status)); },
+                    kOutPartialCompact, part, __ldg(p.part_base + seq) + part, &s_abort);
             }
             if (threadIdx.x == 0) s_next = nxt;
             __syncthreads();
@@ -623,6 +765,7 @@ __global__ void __launch_bounds__(NW * 32)
             u = s_next;
         }
     }
+    grid_dep_trigger();   // the reduce (or the next step) may launch
 }
 
 // ---------------------------------------------------------------------------
@@ -767,12 +910,20 @@ __global__ void __launch_bounds__(ReduceThreads<COMPACT>::value, 2)
     constexpr int NT = ReduceThreads<COMPACT>::value;
     const int h = blockIdx.x;
     const int Hq = r.num_q_heads;
+    grid_dep_wait();   // the attention kernel's partials are complete
+    grid_dep_trigger();
     if constexpr (COMPACT) {
         const int count = *r.pseq_count;
         for (int y = blockIdx.y; y < count; y += gridDim.y) {
             const int4 e = r.pseq_list[y];   // (sequence, first slot, partitions, -)
-            reduce_one<T, D, NT>(r, e.x, h, static_cast<size_t>(e.y) * Hq + h, Hq, max(e.z, 1),
-                                 e.z);
+            if (e.z <= 0) {
+                // every partition of the sequence was dropped by the planner
+                // (flagged there): zeros, and no slot is read
+                T *o = static_cast<T *>(r.out) + (static_cast<size_t>(e.x) * Hq + h) * D;
+                for (int i = threadIdx.x; i < D; i += NT) o[i] = Mma<T>::cvt(0.f);
+                continue;
+            }
+            reduce_one<T, D, NT>(r, e.x, h, static_cast<size_t>(e.y) * Hq + h, Hq, e.z, e.z);
         }
     } else {
         const int s = blockIdx.y;

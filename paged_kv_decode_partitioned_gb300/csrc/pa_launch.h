@@ -12,11 +12,12 @@
 
 namespace pa {
 
+// hp: query heads a unit holds (8, or 16 for head_dim 64 / 128)
 template <typename T>
-cudaError_t launch_attn(int D, int mode, const CUtensorMap &tmK, const CUtensorMap &tmV,
+cudaError_t launch_attn(int D, int mode, int hp, const CUtensorMap &tmK, const CUtensorMap &tmV,
                         const Params &p, dim3 grid, cudaStream_t st);
 template <typename T>
-int attn_ctas_per_sm(int D, int mode);
+int attn_ctas_per_sm(int D, int mode, int hp);
 template <typename T>
 cudaError_t launch_reduce(int D, bool compact, const ReduceParams &r, dim3 grid, cudaStream_t st);
 

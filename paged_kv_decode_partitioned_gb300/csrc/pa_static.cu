@@ -41,25 +41,25 @@ extern "C" int pa_decode_auto_static(void *out, const void *query, const void *k
                                      const int32_t *seq_lens, int num_seqs, int num_q_heads,
                                      int num_kv_heads, int head_dim, int block_size,
                                      int num_blocks, int max_blocks_per_seq, float scale,
-                                     int max_seq_len, int single_pass_max_len,
-                                     int partition_size, pa_dtype_t dtype, void *stream) {
-    if (partition_size <= 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARGUMENT;
-    // Resolve the heuristic here so the size check below sees the real split.
-    const int thr = single_pass_max_len >= 0
-                        ? single_pass_max_len
-                        : pa_default_single_pass_max_len(num_seqs, num_kv_heads,
-                                                         partition_size, 0);
+                                     int max_seq_len, long long max_total_tokens,
+                                     int single_pass_max_len, int partition_size,
+                                     pa_dtype_t dtype, void *stream) {
+    // The size check resolves the launch heuristic (threshold, partition
+    // size, launch form) exactly as pa_decode_auto will on this device.
     const size_t need = pa_auto_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                max_seq_len, thr, partition_size);
+                                                block_size, max_seq_len, max_total_tokens,
+                                                single_pass_max_len, partition_size);
     if (need == 0) return PA_ERR_INVALID_ARGUMENT;
     if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE_TOO_SMALL;
     void *scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != PA_OK) return rc;
-    // The planner (first kernel of the step) resets the work-list cursor and
-    // rewrites the work list; every partial is written before it is read.
+    // The planner (first kernel of the work-list form) resets the work-list
+    // cursor and rewrites the work list; every partial is written before it
+    // is read.
     return pa_decode_auto(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                          max_blocks_per_seq, scale, max_seq_len, thr, partition_size, scratch,
-                          PA_STATIC_SCRATCH_BYTES, dtype, stream);
+                          max_blocks_per_seq, scale, max_seq_len, max_total_tokens,
+                          single_pass_max_len, partition_size, scratch, PA_STATIC_SCRATCH_BYTES,
+                          dtype, stream);
 }

@@ -8,7 +8,9 @@
 namespace pa {
 
 constexpr int kTile = 16;       // tokens per pipeline tile (the MMA M of S^T)
-constexpr int kHeadsPad = 8;    // query heads per KV head, padded to the MMA N
+constexpr int kHeadsPad = 8;    // query heads of one MMA n-tile (the MMA N)
+constexpr int kHeadsWide = 16;  // query heads a decode unit holds in registers at most
+constexpr int kMaxGroup = 128;  // largest GQA group the decode kernels take (head groups)
 constexpr int kPrefillRows = 128;   // largest GQA group the prefill kernel takes
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -42,6 +44,8 @@ struct Params {
     int num_seqs, num_q_heads, num_kv_heads, group, block_size, max_blocks, num_blocks;
     int partition_size, max_parts, single_pass_max_len;
     int cluster;                // CTAs per unit of the single-pass grid (1..8)
+    int hg_count;               // head groups per KV head: a unit's "KV head" index v is
+                                // (KV head v / hg_count, head group v % hg_count)
     float scale_log2;           // scale * log2(e)
 };
 
@@ -68,6 +72,7 @@ struct PlanParams {
     int *pseq_count;
     int *status;
     int num_seqs, num_kv_heads, partition_size, single_pass_max_len, len_cap, max_parts;
+    int max_slots;              // partition slots the workspace holds
 };
 
 struct PrefillParams {

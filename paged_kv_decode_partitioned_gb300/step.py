@@ -12,7 +12,10 @@ heuristic and the V2 description):
   with one partition size for every sequence (V2, phase 1 + phase 2);
 * ``"auto"``        -- ``pa_decode_auto``: sequences up to
   ``single_pass_max_len`` tokens in one pass, longer ones partitioned and
-  merged, one work list on the device.
+  merged; the library picks the launch form (single-pass grid, dense
+  partitioned grid + reduce, or the device work list) and, when asked
+  (``single_pass_max_len=-1``, ``partition_size=0``), the threshold and the
+  partition size.
 """
 from __future__ import annotations
 
@@ -20,8 +23,9 @@ from typing import Optional
 
 import torch
 
-from . import (PHASE_ATTEND, PHASE_PLAN, PHASE_REDUCE, auto_workspace_bytes, decode,
-               decode_auto, decode_partitioned, num_partitions, partition_reduce)
+from . import (AUTO_DENSE, AUTO_SINGLE_PASS, PHASE_ATTEND, PHASE_PLAN, PHASE_REDUCE,
+               auto_resolve, auto_workspace_bytes, decode, decode_auto, decode_partitioned,
+               num_partitions, partition_buffers, partition_reduce)
 
 MODES = ("single", "partitioned", "auto")
 
@@ -29,7 +33,8 @@ MODES = ("single", "partitioned", "auto")
 class DecodeStep:
     def __init__(self, mode: str, query, key_cache, value_cache, block_tables, seq_lens,
                  scale: float, *, max_seq_len: int, partition_size: int = 512,
-                 single_pass_max_len: int = 8192, out: Optional[torch.Tensor] = None):
+                 single_pass_max_len: int = 8192, out: Optional[torch.Tensor] = None,
+                 max_total_tokens: int = 0):
         if mode not in MODES:
             raise ValueError(f"mode must be one of {MODES}")
         self.mode = mode
@@ -44,32 +49,46 @@ class DecodeStep:
         Hkv = key_cache.shape[2]
         dev = query.device
         self.tmp_out = self.exp_sums = self.max_logits = self.workspace = None
+        self.max_total_tokens = int(max_total_tokens)
         if mode == "partitioned":
             self.max_num_partitions = max(1, num_partitions(self.max_seq_len, partition_size))
-            NP = self.max_num_partitions
-            self.tmp_out = torch.empty((S, Hq, NP, D), dtype=torch.float32, device=dev)
-            self.exp_sums = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
-            self.max_logits = torch.empty((S, Hq, NP), dtype=torch.float32, device=dev)
+            self.tmp_out, self.exp_sums, self.max_logits = partition_buffers(
+                S, Hq, D, self.max_num_partitions, dev)
         elif mode == "auto":
-            need = auto_workspace_bytes(S, Hq, Hkv, D, self.max_seq_len,
-                                        self.single_pass_max_len, partition_size)
+            bs = key_cache.shape[1]
+            with torch.cuda.device(dev):
+                self.resolved = auto_resolve(S, Hkv, D, bs, self.max_seq_len,
+                                             self.single_pass_max_len, self.partition_size,
+                                             max_total_tokens=self.max_total_tokens)
+                need = auto_workspace_bytes(S, Hq, Hkv, D, bs, self.max_seq_len,
+                                            self.max_total_tokens, self.single_pass_max_len,
+                                            self.partition_size)
             self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
     @property
+    def form(self) -> Optional[int]:
+        """The launch form ``pa_decode_auto`` takes (auto mode; AUTO_* of the binding)."""
+        return self.resolved[2] if self.mode == "auto" else None
+
+    @property
     def kernels_per_call(self) -> int:
-        """Kernel launches one call makes (single: 1; partitioned: 2; auto: 3, or 1 when
-        every sequence fits the single-pass limit)."""
+        """Kernel launches one call makes (single: 1; partitioned: 2; auto: 1, 2 or 3 by
+        the resolved launch form)."""
         if self.mode == "single":
             return 1
         if self.mode == "partitioned":
             return 2
-        return 3 if self.max_seq_len > self.single_pass_max_len else 1
+        return {AUTO_SINGLE_PASS: 1, AUTO_DENSE: 2}.get(self.form, 3)
 
     @property
     def attention_kernel(self) -> str:
         """Name of the kernel that reads the KV cache (the step's dominant kernel)."""
-        return {"single": "pa_attn_kernel<single>", "partitioned": "pa_attn_kernel<partitioned>",
-                "auto": "pa_attn_kernel<worklist>"}[self.mode]
+        if self.mode == "auto":
+            return {AUTO_SINGLE_PASS: "pa_attn_kernel<single>",
+                    AUTO_DENSE: "pa_attn_kernel<partitioned>"}.get(
+                        self.form, "pa_attn_kernel<worklist>")
+        return {"single": "pa_attn_kernel<single>",
+                "partitioned": "pa_attn_kernel<partitioned>"}[self.mode]
 
     def launches(self):
         """The step as (label, callable) pairs in launch order, one kernel each.
@@ -97,9 +116,12 @@ class DecodeStep:
                                        self.block_tables, self.seq_lens, self.scale,
                                        self.max_seq_len, self.single_pass_max_len,
                                        self.partition_size, workspace=self.workspace,
-                                       out=self.out, phases=mask)
-        if self.max_seq_len <= self.single_pass_max_len:   # one single-pass launch
+                                       out=self.out, phases=mask,
+                                       max_total_tokens=self.max_total_tokens)
+        if self.form == AUTO_SINGLE_PASS:   # one single-pass launch
             return [("attention", phase(PHASE_PLAN | PHASE_ATTEND | PHASE_REDUCE))]
+        if self.form == AUTO_DENSE:          # partitioned grid, then the dense reduce
+            return [("attention", phase(PHASE_ATTEND)), ("reduce", phase(PHASE_REDUCE))]
         return [("plan", phase(PHASE_PLAN)), ("attention", phase(PHASE_ATTEND)),
                 ("reduce", phase(PHASE_REDUCE))]
 
@@ -117,4 +139,5 @@ class DecodeStep:
         return decode_auto(self.query, self.key_cache, self.value_cache, self.block_tables,
                            self.seq_lens, self.scale, self.max_seq_len,
                            self.single_pass_max_len, self.partition_size,
-                           workspace=self.workspace, out=self.out)
+                           workspace=self.workspace, out=self.out,
+                           max_total_tokens=self.max_total_tokens)

@@ -3,17 +3,22 @@
 For every (num_seqs, seq_len) of the grid below, with equal lengths in the
 batch, times ``pa_decode`` (single pass), ``pa_decode_partitioned`` +
 ``pa_partition_reduce`` for each partition size, and ``pa_decode_auto`` with
-the library's default heuristic, and prints one JSON line per point plus a
-markdown table of the winner.  It is the data behind the launch heuristic's
-threshold (``pa_default_single_pass_max_len``): the pages split sequences
+the library's default heuristic (threshold, partition size and launch form
+all chosen by the library), and prints one JSON line per point plus a
+markdown table of the winner.  It is the data behind the launch heuristic
+(``pa_default_single_pass_max_len``, ``pa_default_partition_size``,
+``pa_auto_resolve``): the pages split sequences
 longer than 8192 tokens (project_6 commit cd0d9e1, the forward_decode
 heuristic) and report partition sizes of 512 and 256 (blame of
 optimizations/prefix_prefill_patch.py, the _PARTITION_SIZE note); this
 measures where the split pays off on GB300.
 
-Usage: ``python -m paged_kv_decode_partitioned_gb300.sweep [--reps 20]``.
-Timing: CUDA events on the launching stream, median over reps, L2 flushed
-between reps (one 2x-L2 buffer written, another read).
+Usage: ``python -m paged_kv_decode_partitioned_gb300.sweep [--reps 60]``.
+Timing: CUDA events on the launching stream, L2 flushed between reps (one
+2x-L2 buffer written, another read).  The event clock of the GPU ticks in
+steps of about 2 us, so a single rep of a 15 us call reads one of a few
+values; the figure is the mean over reps after dropping the top and bottom
+tenth (the tick falls at a random phase, so the mean resolves well below it).
 """
 from __future__ import annotations
 
@@ -23,8 +28,8 @@ import statistics
 
 import torch
 
-from . import (auto_workspace_bytes, decode, decode_auto, decode_partitioned,
-               default_single_pass_max_len, num_partitions, partition_reduce)
+from . import (auto_resolve, auto_workspace_bytes, decode, decode_auto, decode_partitioned,
+               num_partitions, partition_buffers, partition_reduce)
 
 SEQS = (1, 4, 16, 64, 256)
 LENS = (1024, 2048, 4096, 8192, 16384, 32768, 65536)
@@ -46,10 +51,13 @@ def _timer(fn, reps, flush):
         e1.record(stream)
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
-    return statistics.median(times)
+    times.sort()
+    cut = len(times) // 10
+    kept = times[cut:len(times) - cut] if len(times) > 2 * cut else times
+    return statistics.fmean(kept)
 
 
-def run(reps: int = 20, seqs=SEQS, lens=LENS, parts=PARTS, hq=24, hkv=4, d=128, bs=16):
+def run(reps: int = 60, seqs=SEQS, lens=LENS, parts=PARTS, hq=24, hkv=4, d=128, bs=16):
     import sys
     import os
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -81,22 +89,22 @@ def run(reps: int = 20, seqs=SEQS, lens=LENS, parts=PARTS, hq=24, hkv=4, d=128, 
             res["single"] = _timer(lambda: decode(*args, out=out), reps, flush)
             for P in parts:
                 NP = num_partitions(L, P)
-                tmp = torch.empty((S, hq, NP, d), dtype=torch.float32, device="cuda")
-                es = torch.empty((S, hq, NP), dtype=torch.float32, device="cuda")
-                ml = torch.empty((S, hq, NP), dtype=torch.float32, device="cuda")
+                tmp, es, ml = partition_buffers(S, hq, d, NP, "cuda")
 
                 def part_step(P=P, NP=NP, tmp=tmp, es=es, ml=ml):
                     decode_partitioned(*args, P, NP, tmp, es, ml)
                     partition_reduce(tmp, es, ml, case.seq_lens, P, out=out, dtype=out.dtype)
                 res[f"P{P}"] = _timer(part_step, reps, flush)
-            thr = default_single_pass_max_len(S, hkv, 512, sms)
-            ws = torch.empty(max(256, auto_workspace_bytes(S, hq, hkv, d, L, thr, 512)),
+            thr, Pa, form = auto_resolve(S, hkv, d, bs, L, -1, 0, sms, max_total_tokens=S * L)
+            ws = torch.empty(max(256, auto_workspace_bytes(S, hq, hkv, d, bs, L, S * L, -1, 0)),
                              dtype=torch.uint8, device="cuda")
 
             def auto_step():
-                decode_auto(*args, L, thr, 512, workspace=ws, out=out)
+                decode_auto(*args, L, -1, 0, workspace=ws, out=out, max_total_tokens=S * L)
             res["auto"] = _timer(auto_step, reps, flush)
             res["auto_threshold"] = thr
+            res["auto_partition"] = Pa
+            res["auto_form"] = ("single", "dense", "worklist")[form]
             modes = ["single"] + [f"P{P}" for P in parts]
             best = min(modes, key=lambda m: res[m])
             res["best"] = best
@@ -114,20 +122,21 @@ def run(reps: int = 20, seqs=SEQS, lens=LENS, parts=PARTS, hq=24, hkv=4, d=128, 
 
 def markdown(rows, parts=PARTS):
     head = "| seqs | seq_len | single ms | " + " | ".join(f"P={P} ms" for P in parts) + \
-        " | best | best GB/s | auto ms (threshold) | auto GB/s |"
-    sep = "|" + "---|" * (7 + len(parts))
+        " | best | best GB/s | auto ms (threshold, P, form) | auto GB/s | auto / best |"
+    sep = "|" + "---|" * (8 + len(parts))
     lines = [head, sep]
     for r in rows:
         lines.append(f"| {r['num_seqs']} | {r['seq_len']} | {r['single']} | " +
                      " | ".join(str(r[f'P{P}']) for P in parts) +
-                     f" | {r['best']} | {r['best_gbs']} | {r['auto']} ({r['auto_threshold']}) "
-                     f"| {r['auto_gbs']} |")
+                     f" | {r['best']} | {r['best_gbs']} | {r['auto']} ({r['auto_threshold']}, "
+                     f"{r['auto_partition']}, {r['auto_form']}) | {r['auto_gbs']} | "
+                     f"{r['auto'] / r[r['best']]:.3f} |")
     return "\n".join(lines)
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--reps", type=int, default=60)
     a = ap.parse_args()
     from . import build
     build.build()

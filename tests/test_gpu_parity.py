@@ -25,8 +25,20 @@ SHAPES = [
     ([77, 640, 31], 4, 4, 64, 16, torch.bfloat16, 2.0),
     ([33, 129, 2048], 12, 6, 64, 32, torch.float16, 1.0),
     ([5, 700], 6, 1, 256, 16, torch.float16, 1.0),
+    # GQA groups above 8: 16 heads in one unit (head_dim 64 / 128), 12 (padded to
+    # 16), and head groups (32 = 2 x 16; head_dim 256: 16 = 2 x 8)
+    ([300, 1, 2000, 4097], 64, 4, 128, 16, torch.bfloat16, 1.0),
+    ([1000, 17, 513], 48, 4, 128, 16, torch.float16, 2.0),
+    ([700, 33], 16, 1, 64, 16, torch.bfloat16, 1.0),
+    ([900, 5, 64], 32, 1, 128, 16, torch.bfloat16, 1.0),
+    ([600, 40], 32, 2, 256, 32, torch.float16, 1.0),
+    # block_size 8: a 16-token tile spans two blocks
+    ([1, 7, 8, 9, 15, 16, 17, 1000], 24, 4, 128, 8, torch.bfloat16, 1.0),
+    ([513, 31], 16, 2, 256, 8, torch.bfloat16, 1.0),
+    ([129, 300], 32, 2, 64, 8, torch.float16, 2.0),
 ]
-IDS = [f"d{s[3]}_g{s[1] // s[2]}_bs{s[4]}_{str(s[5])[6:]}" for s in SHAPES]
+IDS = [f"d{s[3]}_hq{s[1]}_hkv{s[2]}_bs{s[4]}_{str(s[5])[6:]}" for s in SHAPES]
+assert len(set(IDS)) == len(IDS)
 
 
 @pytest.fixture(scope="module")
@@ -80,21 +92,68 @@ def test_partitioned_partials_and_reduce_match_oracle(pa, shaped, pmul):
     assert pa.device_status() == 0
 
 
-@pytest.mark.parametrize("thr_mul", [0, 2, 1000])
-def test_auto_matches_oracle(pa, shaped, thr_mul):
+@pytest.mark.parametrize("thr_mul,pmul", [(0, 2), (2, 2), (3, 2), (1000, 2), (-1, 2), (-1, 0),
+                                          (3, 0)])
+def test_auto_matches_oracle(pa, shaped, thr_mul, pmul):
+    """Every launch form of pa_decode_auto: thr 0 / 2bs (<= P: dense grid on these
+    few-sequence batches), 3bs (> P: the work list with single-pass and partitioned
+    sequences), huge (single pass), and the library's heuristic (thr = -1, P = 0)."""
     host, dev, ref = shaped
     bs = host.workload.block_size
-    P = 2 * bs
-    thr = thr_mul * bs   # 0: everything partitioned; huge: everything single-pass
+    P = pmul * bs
+    thr = -1 if thr_mul < 0 else thr_mul * bs
     out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
                          dev.seq_lens, host.scale, host.max_seq_len, thr, P)
-    assert_out_close(out, ref, f"pa_decode_auto thr={thr} P={P}")
+    form = pa.auto_resolve(host.num_seqs, dev.key_cache.shape[2], dev.query.shape[2], bs,
+                           host.max_seq_len, thr, P)[2]
+    assert_out_close(out, ref, f"pa_decode_auto thr={thr} P={P} form={form}")
+    assert pa.device_status() == 0
+
+
+def test_auto_total_token_bound_and_its_overflow_flag(pa):
+    """A correct total-token bound gives the same result from a smaller workspace; a
+    bound below the batch's real total drops partitions and raises the flag (the
+    planner caps the work list at the workspace's slots; no memory past it is used)."""
+    lengths = [5000, 3000, 700, 12000, 9000, 100] * 6
+    w = custom_workload(num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                        dtype=torch.bfloat16)
+    host = make_case(w, lengths=lengths, seed=301)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    T = host.total_tokens
+    thr, P = 1024, 512
+    full = pa.auto_workspace_bytes(host.num_seqs, 8, 2, 128, 16, host.max_seq_len, 0, thr, P)
+    tight = pa.auto_workspace_bytes(host.num_seqs, 8, 2, 128, 16, host.max_seq_len, T, thr, P)
+    assert tight < full
+    ws = torch.full((tight,), 0xAB, dtype=torch.uint8, device="cuda")
+    out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
+                         dev.seq_lens, host.scale, host.max_seq_len, thr, P, workspace=ws,
+                         max_total_tokens=T)
+    assert_out_close(out, ref, "auto with a total-token bound")
+    assert pa.device_status() == 0
+    # a bound far below the real total: the workspace is sized for too few slots
+    small = T // 4
+    need = pa.auto_workspace_bytes(host.num_seqs, 8, 2, 128, 16, host.max_seq_len, small, thr, P)
+    guard = 1 << 20
+    ws = torch.full((need + guard,), 0xCD, dtype=torch.uint8, device="cuda")
+    out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
+                         dev.seq_lens, host.scale, host.max_seq_len, thr, P,
+                         workspace=ws[:need], max_total_tokens=small)
+    torch.cuda.synchronize()
+    assert pa.device_status() & pa.DEV_TOO_MANY_PARTITIONS
+    assert bool((ws[need:] == 0xCD).all()), "the call wrote past its workspace"
+    assert torch.isfinite(out.float()).all()
+    # single-pass sequences are unaffected by the dropped partitions
+    short = [i for i, L in enumerate(lengths) if L <= thr]
+    assert_out_close(out[short], ref[short], "single-pass sequences under an overflow")
     assert pa.device_status() == 0
 
 
 def test_gather_is_bit_exact(pa):
     for i, (D, bs, dt) in enumerate([(128, 16, torch.bfloat16), (256, 32, torch.float16),
-                                      (64, 16, torch.float16), (128, 48, torch.bfloat16)]):
+                                      (64, 16, torch.float16), (128, 48, torch.bfloat16),
+                                      (128, 8, torch.bfloat16), (256, 8, torch.float16)]):
         case, dk, dv = make_dense_case(lengths=[1, 16, 47, 130, 0], num_q_heads=4,
                                        num_kv_heads=2, head_dim=D, block_size=bs, dtype=dt,
                                        seed=50 + i)

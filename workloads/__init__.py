@@ -79,6 +79,24 @@ WORKLOADS = {
 }
 
 
+# More decode workloads of the same recipe, for the benchmark only (the parity
+# tests sweep these shapes at reduced sizes): the mixed serving batch with a
+# Qwen-style GQA group of 16 (64 query / 4 KV heads), and with block size 8.
+EXTRA_WORKLOADS = {
+    6: Workload(6, "mixed256_L128-65536log_hq64_hkv4_d128_bs16_bf16_auto8192_P512", 256,
+                64, 4, 128, 16, torch.bfloat16, ("loguniform", 128, 65536), "auto",
+                (512,), single_pass_max_len=8192),
+    7: Workload(7, "mixed256_L128-65536log_hq24_hkv4_d128_bs8_bf16_auto8192_P512", 256,
+                24, 4, 128, 8, torch.bfloat16, ("loguniform", 128, 65536), "auto",
+                (512,), single_pass_max_len=8192),
+}
+
+
+def workload(wid: int) -> "Workload":
+    """A decode workload by id: the five of WORKLOADS, or one of EXTRA_WORKLOADS."""
+    return WORKLOADS[wid] if wid in WORKLOADS else EXTRA_WORKLOADS[wid]
+
+
 @dataclass
 class Case:
     """Materialised inputs of one workload (tensors on ``device``)."""
@@ -177,7 +195,7 @@ def make_case(w, *, device="cpu", seed: Optional[int] = None,
     on ``device`` seeded the same way.
     """
     if isinstance(w, int):
-        w = WORKLOADS[w]
+        w = workload(w)
     seed = SEED_BASE + w.wid if seed is None else seed
     hgen = torch.Generator().manual_seed(seed)
     overridden = num_seqs is not None or lengths is not None
