@@ -15,10 +15,10 @@ measures where the split pays off on GB300.
 
 Usage: ``python -m paged_kv_decode_partitioned_gb300.sweep [--reps 60]``.
 Timing: CUDA events on the launching stream, L2 flushed between reps (one
-2x-L2 buffer written, another read).  The event clock of the GPU ticks in
-steps of about 2 us, so a single rep of a 15 us call reads one of a few
-values; the figure is the mean over reps after dropping the top and bottom
-tenth (the tick falls at a random phase, so the mean resolves well below it).
+2x-L2 buffer written, another read).  The event times of a short call
+cluster just below multiples of about 2.05 us, so a single rep of a 15 us
+call reads one of a few values; the figure is the mean over reps after
+dropping the top and bottom tenth, which resolves below that step.
 """
 from __future__ import annotations
 
