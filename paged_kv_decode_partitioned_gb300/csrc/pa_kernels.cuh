@@ -270,6 +270,12 @@ __device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -286,13 +292,14 @@ struct Smem {
     // Cluster merge of the single-pass grid: CTA r of the cluster finishes the
     // r-th slice of the unit's output elements, so it receives from every CTA
     // (itself included) that CTA's merged values of the slice, o_in
-    // [rank][slice] (at most HP * D + 8 floats for any cluster size), and its
+    // [rank][slice] (slices of whole quads: at most HP * D + 32 floats for any
+    // cluster size), and its
     // per-head maximum and sum, m_in / l_in [rank][HP], and abort flag.
     // Written only after every CTA of the cluster has finished with its stages
     // and its own merge area, so it overlaps both.
     static constexpr int kMaxCluster = 8;
     static constexpr int kInO = 0;
-    static constexpr int kInM = kInO + (HP * D + kMaxCluster) * 4;
+    static constexpr int kInM = kInO + (HP * D + 4 * kMaxCluster) * 4;
     static constexpr int kInL = kInM + kMaxCluster * HP * 4;
     static constexpr int kInAbort = kInL + kMaxCluster * HP * 4;
     static constexpr int kClusterEnd = kInAbort + kMaxCluster * 4;
@@ -611,26 +618,41 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
         }
     } else {
         // this CTA's merged output for the thread's elements, kept in registers
-        float keep[KE];
+        // Values go four at a time (a thread holds quads of consecutive output
+        // elements, sent with 16-byte stores): a quarter of the transfers.
+        constexpr int KQ = (HP * D / 4 + NT - 1) / NT;   // quads per thread, at most
+        float4 keep[KQ];
 #pragma unroll
-        for (int k = 0; k < KE; ++k) {
-            const int e = threadIdx.x + k * NT;
-            keep[k] = e < gh * D ? merged(e / D, e - (e / D) * D) : 0.f;
+        for (int k = 0; k < KQ; ++k) {
+            const int e = 4 * (threadIdx.x + k * NT);
+            keep[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < gh * D) {
+                const int h = e / D, dim = e - (e / D) * D;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float c = s_coef[w][h];
+                    const float4 v = *reinterpret_cast<const float4 *>(sm_o + (w * HP + h) * D + dim);
+                    keep[k].x += c * v.x;
+                    keep[k].y += c * v.y;
+                    keep[k].z += c * v.z;
+                    keep[k].w += c * v.w;
+                }
+            }
         }
         cluster_sync();   // every CTA is done with its stages and its merge area
         // send each of this CTA's values to the CTA that finishes its slice
         const int E = gh * D;
-        const int slice = (E + csize - 1) / csize;
+        const int slice = ((E + csize - 1) / csize + 3) / 4 * 4;   // whole quads
         const uint32_t base = smem_u32(smem);
         if (write) {
 #pragma unroll
-            for (int k = 0; k < KE; ++k) {
-                const int e = threadIdx.x + k * NT;
+            for (int k = 0; k < KQ; ++k) {
+                const int e = 4 * (threadIdx.x + k * NT);
                 if (e < E) {
                     const int owner = e / slice;
-                    dsmem_st_f32(dsmem_addr(base + SM::kInO + (crank * slice + e - owner * slice) * 4,
-                                            owner),
-                                 keep[k]);
+                    dsmem_st_v4(dsmem_addr(base + SM::kInO + (crank * slice + e - owner * slice) * 4,
+                                           owner),
+                                keep[k]);
                 }
             }
             for (int t = threadIdx.x; t < csize * gh; t += NT) {
