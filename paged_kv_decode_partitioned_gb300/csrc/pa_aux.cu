@@ -5,17 +5,29 @@
 namespace pa {
 
 // ---------------------------------------------------------------------------
-// Work-list planner: one CTA per sequence.  Unit order: every single-pass
-// unit (sequence order), then every partition unit (slot-major, KV head
-// minor).  part_base[s] is the compact partial slot of partition 0 of s.
+// Work-list planner: one CTA per chunk of 1 .. kPlanSeqs sequences.  Unit order:
+// every single-pass unit (sequence order), then every partition unit
+// (slot-major, head group minor).  part_base[s] is the compact partial slot of
+// partition 0 of s.  Each CTA sums the counts of the sequences before its
+// chunk (and of all of them) with one pass over the lengths, then a warp scan
+// gives each sequence of the chunk its offsets, and the chunk's units are
+// written by all of the CTA's threads (a long sequence has hundreds): the
+// lengths are read at most 256 S times in all (S^2 / 32 past 8192 sequences),
+// not S^2.
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 256;
+constexpr int kPlanSeqs = 32;   // sequences per CTA at most: one lane each of the scan warp
+constexpr int kPlanCtas = 256;  // CTAs the planner aims for: one sequence each up to 256
+                                // sequences, then ceil(S / 256) per CTA (at most 32)
 
 __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams pp) {
     __shared__ int s_red[2][kPlanThreads / 32];
+    __shared__ int s_unit_off[kPlanSeqs + 1], s_dst[kPlanSeqs], s_kind[kPlanSeqs];
+    const int chunk = pp.chunk;   // sequences of this CTA (1 .. kPlanSeqs)
     grid_dep_wait();      // seq_lens are complete
     grid_dep_trigger();   // the attention kernel may launch: it waits for this grid
-    const int s = blockIdx.x;
+    const int s0 = blockIdx.x * chunk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int P = pp.partition_size, thr = pp.single_pass_max_len;
     // partitions a sequence gets: ceil(L / P), at most max_parts (the
     // planner's prefix sums use the same clamped count, so the units and
@@ -25,7 +37,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
         int L = __ldg(pp.seq_lens + i);
         return L < 0 ? 0 : (L > pp.len_cap ? pp.len_cap : L);
     };
-    // counts over sequences before s (and the totals over all of them)
+    // counts over sequences before the chunk (and the totals over all of them)
     int singles_before = 0, slots_before = 0, singles_all = 0, slots_all = 0;
     for (int i = threadIdx.x; i < pp.num_seqs; i += kPlanThreads) {
         const int L = len_of(i);
@@ -33,7 +45,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
         const int single = (L <= thr) ? 1 : 0;
         singles_all += single;
         slots_all += np;
-        if (i < s) {
+        if (i < s0) {
             singles_before += single;
             slots_before += np;
         }
@@ -45,9 +57,9 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
             b += __shfl_xor_sync(0xffffffffu, b, x);
         }
         __syncthreads();
-        if ((threadIdx.x & 31) == 0) {
-            s_red[0][threadIdx.x >> 5] = a;
-            s_red[1][threadIdx.x >> 5] = b;
+        if (lane == 0) {
+            s_red[0][warp] = a;
+            s_red[1][warp] = b;
         }
         __syncthreads();
         a = b = 0;
@@ -60,37 +72,80 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(const PlanParams 
     block_sum2(singles_before, slots_before);
     block_sum2(singles_all, slots_all);
 
+    // offsets of the chunk's sequences: an exclusive warp scan (lane = sequence)
+    // of their single-pass units, partition slots and work-list units
     const int Hkv = pp.num_kv_heads;
-    int L = __ldg(pp.seq_lens + s);
-    if (L < 0 || L > pp.len_cap) {
-        if (threadIdx.x == 0) atomicOr(pp.status, kLenClamped);
-        L = L < 0 ? 0 : pp.len_cap;
-    }
-    if (L <= thr) {
-        for (int k = threadIdx.x; k < Hkv; k += kPlanThreads)
-            pp.units[singles_before * Hkv + k] = make_int4(s, k, 0, kOutFinal);
-        if (threadIdx.x == 0) pp.part_base[s] = -1;
-    } else {
-        int np = (L + P - 1) / P;
-        // The workspace was sized for at most max_parts partitions per
-        // sequence and max_slots in all (the caller's bounds on the longest
-        // sequence and on the batch's tokens): partitions past either bound
-        // are dropped and flagged.
-        const int room = slots_before < pp.max_slots ? pp.max_slots - slots_before : 0;
-        if (np > pp.max_parts || np > room) {
-            if (threadIdx.x == 0) atomicOr(pp.status, kTooManyParts);
-            np = min(np, min(pp.max_parts, room));
+    if (warp == 0) {
+        const int s = s0 + lane;
+        const bool mine = lane < chunk && s < pp.num_seqs;   // a sequence of the chunk
+        int L = 0;
+        if (mine) {
+            L = __ldg(pp.seq_lens + s);
+            if (L < 0 || L > pp.len_cap) {
+                atomicOr(pp.status, kLenClamped);
+                L = L < 0 ? 0 : pp.len_cap;
+            }
         }
-        const int base_unit = singles_all * Hkv + min(slots_before, pp.max_slots) * Hkv;
-        for (int k = threadIdx.x; k < np * Hkv; k += kPlanThreads)
-            pp.units[base_unit + k] = make_int4(s, k % Hkv, k / Hkv, kOutPartialCompact);
-        if (threadIdx.x == 0) {
-            pp.part_base[s] = slots_before;
+        const int single = mine && L <= thr ? 1 : 0;
+        const int np = mine ? parts_of(L) : 0;
+        int inc_single = single, inc_slots = np;
+#pragma unroll
+        for (int x = 1; x < 32; x <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, inc_single, x);
+            const int b = __shfl_up_sync(0xffffffffu, inc_slots, x);
+            if (lane >= x) {
+                inc_single += a;
+                inc_slots += b;
+            }
+        }
+        const int sb = singles_before + inc_single - single;   // single-pass units before s
+        const int pb = slots_before + inc_slots - np;         // partition slots before s
+        // the sequence's partitions after the workspace's bounds (the caller's
+        // bounds on the longest sequence and on the batch's tokens): partitions
+        // past either bound are dropped and flagged
+        int npw = 0;
+        if (mine && !single) {
+            npw = (L + P - 1) / P;
+            const int room = pb < pp.max_slots ? pp.max_slots - pb : 0;
+            if (npw > pp.max_parts || npw > room) {
+                atomicOr(pp.status, kTooManyParts);
+                npw = min(npw, min(pp.max_parts, room));
+            }
+            pp.part_base[s] = pb;
             // entry at the sequence's rank among the partitioned sequences
-            pp.pseq_list[s - singles_before] = make_int4(s, slots_before, np, 0);
+            pp.pseq_list[s - sb] = make_int4(s, pb, npw, 0);
+        } else if (mine) {
+            pp.part_base[s] = -1;
         }
+        const int nu = mine ? (single ? Hkv : npw * Hkv) : 0;   // its units
+        int inc_u = nu;
+#pragma unroll
+        for (int x = 1; x < 32; x <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, inc_u, x);
+            if (lane >= x) inc_u += a;
+        }
+        if (lane < chunk) {
+            s_unit_off[lane] = inc_u - nu;
+            s_dst[lane] = single ? sb * Hkv : singles_all * Hkv + min(pb, pp.max_slots) * Hkv;
+            s_kind[lane] = single;
+        }
+        if (lane == chunk - 1) s_unit_off[chunk] = inc_u;
     }
-    if (s == 0 && threadIdx.x == 0) {
+    __syncthreads();
+    // the chunk's units, spread over all threads: u -> (sequence j, index k)
+    const int total_u = s_unit_off[chunk];
+    for (int u = threadIdx.x; u < total_u; u += kPlanThreads) {
+        int lo = 0, hi = chunk - 1;   // last j with s_unit_off[j] <= u
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_unit_off[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        const int j = lo, k = u - s_unit_off[j];
+        pp.units[s_dst[j] + k] = s_kind[j] ? make_int4(s0 + j, k, 0, kOutFinal)
+                                           : make_int4(s0 + j, k % Hkv, k / Hkv,
+                                                       kOutPartialCompact);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         *pp.unit_count = (singles_all + min(slots_all, pp.max_slots)) * Hkv;
         *pp.unit_counter = 0;
         *pp.pseq_count = pp.num_seqs - singles_all;
@@ -177,8 +232,12 @@ cudaError_t launch_wait_timeout_test(int *status, unsigned long long limit_ns, c
 
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st) {
     if (pp.num_seqs <= 0) return cudaSuccess;
-    const cudaError_t e = launch_dependent(pa_plan_kernel, dim3(pp.num_seqs), dim3(kPlanThreads),
-                                           0, st, nullptr, pp);
+    PlanParams q = pp;
+    q.chunk = (pp.num_seqs + kPlanCtas - 1) / kPlanCtas;
+    if (q.chunk > kPlanSeqs) q.chunk = kPlanSeqs;
+    const cudaError_t e =
+        launch_dependent(pa_plan_kernel, dim3((pp.num_seqs + q.chunk - 1) / q.chunk),
+                         dim3(kPlanThreads), 0, st, nullptr, q);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

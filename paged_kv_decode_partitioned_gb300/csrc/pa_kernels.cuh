@@ -118,6 +118,38 @@ __device__ __forceinline__ void grid_dep_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// L2 eviction-priority policies.  Decode reads every K/V byte once, so its
+// tile loads are marked evict-first and do not push out of L2 the partial
+// results (written evict-last) that the reduce reads right after.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 5-D tiled TMA load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int c0, int c1, int c2, int c3,
+                                                 int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_global_hint(float *ptr, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -230,6 +262,23 @@ __device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *m
         }
     } else {
         tma_load_5d(dst, map, bar, 0, 0, kvh, row, b0);   // block_size 8 is refused on the host
+    }
+}
+
+// The same with an L2 cache policy on every copy.
+template <int D>
+__device__ __forceinline__ void tma_load_tile_hint(uint32_t dst, const CUtensorMap *map,
+                                                   uint32_t bar, int kvh, int row, int b0, int b1,
+                                                   bool split, uint64_t policy) {
+    if constexpr (kPiecewise) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_5d_hint(dst + c * kPieceBytes, map, bar, 0, c, kvh, row, b0, policy);
+            if (split)
+                tma_load_5d_hint(dst + c * kPieceBytes + 1024, map, bar, 0, c, kvh, 0, b1, policy);
+        }
+    } else {
+        tma_load_5d_hint(dst, map, bar, 0, 0, kvh, row, b0, policy);
     }
 }
 
@@ -416,8 +465,9 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
             const uint32_t dk = stage0 + st * SM::kStageBytes;
             const int row = split ? 0 : tt % p.block_size;
             mbar_expect_tx(bar, SM::kStageBytes);
-            tma_load_tile<D>(dk, tmK, bar, kvh, row, b, b2, split);
-            tma_load_tile<D>(dk + SM::kTileBytes, tmV, bar, kvh, row, b, b2, split);
+            const uint64_t once = l2_evict_first_policy();   // read once: evict first
+            tma_load_tile_hint<D>(dk, tmK, bar, kvh, row, b, b2, split, once);
+            tma_load_tile_hint<D>(dk + SM::kTileBytes, tmV, bar, kvh, row, b, b2, split, once);
         }
     };
 
@@ -563,7 +613,6 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
     const bool write = (*s_abort == 0);
     const int Hq = p.num_q_heads;
     constexpr int NT = NW * 32;
-    constexpr int KE = (HP * D + NT - 1) / NT;   // output elements per thread, at most
     const bool clustered = csize > 1;
     // Per head: the merged maximum M and sum L of the warps' states, and the
     // weight of each warp's normalised output, exp(m_w - M) / L * (its own
@@ -609,10 +658,13 @@ __device__ __forceinline__ bool attend_unit(const Params &p, const CUtensorMap *
                     srow = (static_cast<size_t>(seq) * Hq + head) * p.max_parts + part;
                 else
                     srow = static_cast<size_t>(slot) * Hq + head;
-                p.tmp_out[srow * D + dim] = res;
+                // the reduce reads the partials next: keep them in L2
+                const uint64_t keep_l2 = l2_evict_last_policy();
+                st_global_hint(p.tmp_out + srow * D + dim, res, keep_l2);
                 if (dim == 0) {
-                    p.exp_sums[srow] = s_hl[h];
-                    p.max_logits[srow] = s_hm[h] == -INFINITY ? -INFINITY : s_hm[h] * kLn2;
+                    st_global_hint(p.exp_sums + srow, s_hl[h], keep_l2);
+                    st_global_hint(p.max_logits + srow,
+                                   s_hm[h] == -INFINITY ? -INFINITY : s_hm[h] * kLn2, keep_l2);
                 }
             }
         }

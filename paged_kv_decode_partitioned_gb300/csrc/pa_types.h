@@ -73,6 +73,7 @@ struct PlanParams {
     int *status;
     int num_seqs, num_kv_heads, partition_size, single_pass_max_len, len_cap, max_parts;
     int max_slots;              // partition slots the workspace holds
+    int chunk;                  // sequences per planner CTA (set by the launcher)
 };
 
 struct PrefillParams {

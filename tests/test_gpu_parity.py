@@ -338,3 +338,26 @@ def test_many_short_sequences(pa):
                     host.scale)
     assert_out_close(out, ref, "single pass, 1000 sequences")
     assert pa.device_status() == 0
+
+
+def test_planner_thousands_of_sequences(pa):
+    """5000 sequences through the work list: the planner's chunked prefix sums (one CTA
+    per 32 sequences) place single-pass and partition units of every sequence, including
+    a chunk boundary falling inside runs of partitioned sequences."""
+    g = torch.Generator().manual_seed(95)
+    lengths = [int(x) for x in torch.randint(1, 400, (5000,), generator=g)]
+    for i in range(0, 5000, 37):
+        lengths[i] = 1500 + i % 700          # partitioned (> threshold 256)
+    w = custom_workload(num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                        dtype=torch.bfloat16)
+    host = make_case(w, lengths=lengths, seed=96)
+    dev = host.to("cuda")
+    ref = oracle.attention(host.query, host.key_cache, host.value_cache, host.block_tables,
+                           host.seq_lens, host.scale)
+    out = pa.decode_auto(dev.query, dev.key_cache, dev.value_cache, dev.block_tables,
+                         dev.seq_lens, host.scale, host.max_seq_len, 256, 128,
+                         max_total_tokens=host.total_tokens)
+    assert pa.auto_resolve(5000, 2, 64, 16, host.max_seq_len, 256, 128,
+                           max_total_tokens=host.total_tokens)[2] == pa.AUTO_WORKLIST
+    assert_out_close(out, ref, "auto, 5000 sequences")
+    assert pa.device_status() == 0
