@@ -117,8 +117,9 @@ def qo_bytes(case) -> int:
 KERNEL_SOURCES = {
     "decode": ["pa_kernels.cuh", "pa_launch.cuh", "pa_launch.h", "pa_types.h", "pa_inst_bf16.cu",
                "pa_inst_f16.cu", "pa_aux.cu", "pa_api.cu", "../../include/pa_decode.h"],
-    "prefill": ["pa_prefill_tc.cuh", "pa_tc05.cuh", "pa_prefill.cu", "pa_kernels.cuh",
-                "pa_launch.cuh", "pa_types.h", "pa_api.cu", "../../include/pa_decode.h"],
+    "prefill": ["pa_prefill_tc.cuh", "pa_prefill_pair.cuh", "pa_tc05.cuh", "pa_prefill.cu",
+                "pa_kernels.cuh", "pa_launch.cuh", "pa_launch.h", "pa_types.h", "pa_api.cu",
+                "../../include/pa_decode.h"],
     "moe": ["pa_moe.cu", "pa_types.h", "pa_api.cu", "../../include/pa_moe.h"],
 }
 

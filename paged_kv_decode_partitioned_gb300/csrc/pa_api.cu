@@ -80,8 +80,7 @@ EncodeTiledFn encode_fn() {
 // 5-D view of a cache [num_blocks][bs][Hkv][D] for TMA: (element within a
 // 64-element piece, piece index, KV head, row in block, block); one box = one
 // 64-element piece of 16 rows of one KV head (2 KB; 8 rows for block_size 8),
-// 128-byte swizzled.
-// Out-of-range boxes read zeros.
+// 128-byte swizzled.  Out-of-range boxes read zeros.
 int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv, int bs,
                    int num_blocks) {
     EncodeTiledFn fn = encode_fn();
@@ -98,6 +97,31 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
 #else
     cuuint32_t box[5] = {64, static_cast<cuuint32_t>(D / 64), 1, static_cast<cuuint32_t>(kTile), 1};
 #endif
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    5, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// 5-D view of a cache with the row in the block ahead of the piece: (element
+// within a 64-element piece, row in block, piece, KV head, block); one box =
+// `pieces` consecutive 64-element pieces of 16 rows of one KV head, landing
+// piece after piece ([piece][16 rows][128 B], 128-byte swizzled), so one copy
+// moves several pieces of a block.  Used for the V tiles of the prefill
+// kernels (block_size a multiple of 16).
+int make_cache_map_pieces(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv,
+                          int bs, int num_blocks, int pieces) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PA_ERR_NO_DEVICE;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(D / 64),
+                          static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
+    cuuint64_t strides[4] = {static_cast<cuuint64_t>(Hkv) * D * e, 64 * e, D * e,
+                             static_cast<cuuint64_t>(bs) * Hkv * D * e};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(pieces), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -864,8 +888,9 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
                              num_blocks)) != PA_OK)
         return rc;
-    if ((rc = make_cache_map(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
-                             num_blocks)) != PA_OK)
+    // V tiles move one 16-token box (all of a CTA's pieces of it) per copy
+    if ((rc = make_cache_map_pieces(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+                                    num_blocks, prefill_v_box_pieces(head_dim))) != PA_OK)
         return rc;
     PrefillParams p{};
     p.q = query;

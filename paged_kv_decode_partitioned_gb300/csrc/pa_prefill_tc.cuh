@@ -75,6 +75,10 @@ struct PrefillTcCfg {
     static constexpr int kKvPiece = kN * 128;                    // bytes of one K (V) piece
     static constexpr int kQBytes = kPieces * kQPiece;
     static constexpr int kTileBytes = kPieces * kKvPiece;        // K (or V) of one stage
+    // K lands piece by piece ([piece][N rows][128 B], the K-major operand);
+    // V one 16-token box at a time with all its pieces ([box][piece][16 rows]
+    // [128 B], the MN-major operand), one copy per box
+    static constexpr int kVBox = kPieces * 2048;
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
     // barriers: q_full, vtail, mma_done, k_full[NS], v_full[NS], k_empty[NS],
@@ -290,13 +294,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         constexpr int kOps = kBoxes * C::kPieces;   // copies per K (or V) tile
         static_assert(kOps <= 32, "one copy per lane");
         const int op_box = (lane % kOps) / C::kPieces, op_piece = (lane % kOps) % C::kPieces;
-        // block of this lane's box of tile jt (0 when the lane has no copy).  The
-        // read goes out a tile ahead and is checked only when the copy is issued,
-        // so its latency overlaps the stage waits in between (with one stage, a
-        // read consumed at once put ~3000 cycles on every tile's K load).
-        auto box_block = [&](int jt) -> int {
-            const int bx = jt * kBoxes + op_box;
-            if (lane >= kOps || bx >= nbox) return 0;
+        const int v_box = lane % kBoxes;   // V: one copy per box moves all its pieces
+        // block of this lane's K (V) box of tile jt (0 when the lane has no copy).
+        // The read goes out a tile ahead and is checked only when the copy is
+        // issued, so its latency overlaps the stage waits in between (with one
+        // stage, a read consumed at once put ~3000 cycles on every tile's K load).
+        auto box_block = [&](int jt, int box, bool has) -> int {
+            const int bx = jt * kBoxes + box;
+            if (!has || bx >= nbox) return 0;
             return __ldg(bt_row + (bx * kTile) / p.block_size);
         };
         auto check_block = [&](int b) {
@@ -320,14 +325,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             for (int c = 0; c < C::kPieces; ++c)
                 tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
         }
-        int jt_next = rot, phys_next = box_block(rot);
+        const bool k_has = lane < kOps, v_has = lane < kBoxes;
+        int jt_next = rot, phys_next = box_block(rot, op_box, k_has), vphys_next = box_block(rot, v_box, v_has);
         int issued = 0;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
             const int st = j % NS;
-            const int jt = jt_next, op_phys = phys_next;
+            const int jt = jt_next, op_phys = phys_next, v_phys = vphys_next;
             jt_next = jt + 1 == ntiles ? 0 : jt + 1;
-            if (j + 1 < ntiles) phys_next = box_block(jt_next);   // next tile's table entries
+            if (j + 1 < ntiles) {   // next tile's table entries
+                phys_next = box_block(jt_next, op_box, k_has);
+                vphys_next = box_block(jt_next, v_box, v_has);
+            }
             const uint32_t kdst = stage0 + st * C::kStageBytes, vdst = kdst + C::kTileBytes;
             const bool last = jt == ntiles - 1;   // the context's tail tile
             const uint32_t vbar = last ? vtail : v_full + st * 8;
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             // bound by the issue latency of each copy, not by the TMA engine
             if (lane == 0) mbar_expect_tx(k_full + st * 8, bytes);
             __syncwarp();
-            if (lane < kOps && jt * kBoxes + op_box < nbox)
+            if (k_has && jt * kBoxes + op_box < nbox)
                 tma_load_5d(kdst + op_piece * C::kKvPiece + op_box * 2048, &tmK, k_full + st * 8,
                             0, op_piece, kvh, ((jt * kBoxes + op_box) * kTile) % p.block_size,
                             op_phys);
@@ -361,11 +370,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     break;
                 }
             }
+            check_block(v_phys);
             if (lane == 0) mbar_expect_tx(vbar, bytes);
             __syncwarp();
-            if (lane < kOps && jt * kBoxes + op_box < nbox)
-                tma_load_5d(vdst + op_piece * C::kKvPiece + op_box * 2048, &tmV, vbar, 0, op_piece,
-                            kvh, ((jt * kBoxes + op_box) * kTile) % p.block_size, op_phys);
+            // the V map has the row ahead of the piece: (element, row, piece, head, block)
+            if (v_has && jt * kBoxes + v_box < nbox)
+                tma_load_5d(vdst + v_box * C::kVBox, &tmV, vbar, 0,
+                            ((jt * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, v_phys);
             issued = j + 1;
             if (last) {
                 // V rows at or past kv_end hold cache data past the context (or
@@ -376,12 +387,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     break;
                 }
                 const int first_row = kv_end - jt * N;
-                const int nchunks = (N - first_row) * 8;   // 16-byte chunks per piece
-                for (int c = 0; c < C::kPieces; ++c)
-                    for (int e = lane; e < nchunks; e += 32)
-                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + c * C::kKvPiece +
-                                                   first_row * 128 + e * 16) =
-                            make_uint4(0, 0, 0, 0);
+                const int nchunks = (N - first_row) * C::kPieces * 8;   // 16-byte chunks
+                for (int e = lane; e < nchunks; e += 32) {
+                    const int r = first_row + e / (C::kPieces * 8);
+                    const int c = (e / 8) % C::kPieces;
+                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox +
+                                               c * 2048 + (r & 15) * 128 + (e & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(v_full + st * 8);
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                             tc05::mma_ts(tcol + C::kOCol,
                                          tcol + (j % SB) * N +
                                              ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
-                                         tc05::sw128_desc(vst + kt * 2048, C::kKvPiece, 1024),
+                                         tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024),
                                          idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
                         // s_free: with one S buffer the commit of the QK issued next
                         // (S_{j+1}) tracks this PV as well, so none is needed
@@ -638,16 +651,6 @@ inline cudaError_t launch_prefill_tc_d(const CUtensorMap &tmQ, const CUtensorMap
     if (e != cudaSuccess) return e;
     k<<<grid, C::kThreads, C::kLaunchBytes, st>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
-}
-
-template <typename T>
-cudaError_t launch_prefill_tc(int D, const CUtensorMap &tmQ, const CUtensorMap &tmK,
-                              const CUtensorMap &tmV, const PrefillParams &p, dim3 grid,
-                              cudaStream_t st) {
-    if (D == 64) return launch_prefill_tc_d<T, 64>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 128) return launch_prefill_tc_d<T, 128>(tmQ, tmK, tmV, p, grid, st);
-    if (D == 256) return launch_prefill_tc_d<T, 256>(tmQ, tmK, tmV, p, grid, st);
-    return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

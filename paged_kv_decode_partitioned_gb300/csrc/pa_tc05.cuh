@@ -94,6 +94,56 @@ __device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
                  : "memory");
 }
 
+// ---- the 2-SM forms (cta_group::2): one CTA pair of a cluster shares each MMA ----
+// An M = 256 MMA issued by one thread of the pair's even CTA: rows 0..127 of A
+// and D live in the even CTA (its shared memory, its tensor memory), rows
+// 128..255 in the odd one, at the same addresses; B's N columns are split the
+// same way, N / 2 in each CTA.  Every tcgen05 instruction of a kernel that uses
+// these takes cta_group::2.
+
+__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` of every CTA in `cta_mask` when
+// the pair's MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void commit2(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Pair allocation: one warp of EACH CTA of the pair executes it; both get the
+// same columns in their own tensor memory.  The peer CTA must be running.
+__device__ __forceinline__ void alloc2(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+
 // N consecutive 32-bit columns of this thread's lane (warp w reads lanes
 // 32*(w%4) .. +31; `taddr` carries that lane base in bits 16..).  Loads wait
 // in the same statement, so no use of the registers can move above the wait.
