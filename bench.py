@@ -51,13 +51,26 @@ FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged prefix-prefill attention: TFLOP/s on the bf16 tensor cores"
 MOE_METRIC = ("MoE router + sort-by-expert regroup + scatter-back: GB/s of algorithmic HBM "
               "traffic; tokens/s")
-# prefix-prefill workloads: (context tokens, chunk tokens, sequences); 24 query /
-# 4 KV heads, head_dim 128, block 16, bf16 (the decode workloads' model shape)
+# prefix-prefill workloads: (context tokens, chunk tokens, sequences, query heads,
+# KV heads, head_dim); block 16, bf16.  The first three have the decode
+# workloads' model shape (24 query / 4 KV heads, head_dim 128); the last the
+# head_dim-256 attention of the pages' Qwen-family notes (16 query / 2 KV heads).
 PREFILL_WORKLOADS = {
-    "chunk2048_ctx16384_x16": (16384, 2048, 16),
-    "full100k_x1": (0, 100000, 1),
-    "chunk512_ctx4096_x64": (4096, 512, 64),
+    "chunk2048_ctx16384_x16": (16384, 2048, 16, 24, 4, 128),
+    "full100k_x1": (0, 100000, 1, 24, 4, 128),
+    "chunk512_ctx4096_x64": (4096, 512, 64, 24, 4, 128),
+    "d256_chunk2048_ctx16384_x8": (16384, 2048, 8, 16, 2, 256),
 }
+
+
+def prefill_workload_name(name):
+    _, _, _, hq, hkv, d = PREFILL_WORKLOADS[name]
+    return f"prefill_{name}_hq{hq}_hkv{hkv}_d{d}_bs16_bf16"
+
+
+def prefill_kernel_name(name):
+    # head_dim 256 runs on CTA pairs sharing 2-SM MMAs, the others on single CTAs
+    return "pa_prefill_pair_kernel" if PREFILL_WORKLOADS[name][5] == 256 else "pa_prefill_tc_kernel"
 
 
 def parse_args():
@@ -511,8 +524,8 @@ def timed_e2e(fn, K, flush_l2, stream):
 def make_prefill_inputs(name, device, rank=0):
     import torch
     from workloads import custom_workload, make_prefill_case
-    ctx, n, S = PREFILL_WORKLOADS[name]
-    w = custom_workload(num_q_heads=24, num_kv_heads=4, head_dim=128, block_size=16,
+    ctx, n, S, hq, hkv, d = PREFILL_WORKLOADS[name]
+    w = custom_workload(num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=16,
                         dtype=torch.bfloat16, name=f"prefill_{name}")
     return make_prefill_case(w, ctx_lens=[ctx] * S, q_lens=[n] * S, device=device,
                              seed=20261400 + 1000 * rank), (ctx, n, S)
@@ -627,7 +640,7 @@ def run_next_path(args, rank, world, local_rank):
                    "kind": "oracle",
                    "sample": f"the last {rows} chunk rows of sequence 0 ({fl / 1e9:.1f} GFLOP), "
                              f"{secs:.1f} s"}
-        name = f"prefill_{args.prefill_workload}_hq24_hkv4_d128_bs16_bf16"
+        name = prefill_workload_name(args.prefill_workload)
         line = {
             "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -638,7 +651,7 @@ def run_next_path(args, rank, world, local_rank):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed between steps (outside the events)"},
             "prefill_tokens_per_s": round(tok_all / (ms * 1e-3), 1),
-            "roofline": {"bound": "tensor", "kernel": "pa_prefill_tc_kernel",
+            "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(args.prefill_workload),
                          "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": committed_traffic(f"prefill_{args.prefill_workload}"),
@@ -788,7 +801,7 @@ def run_next_reference(args, world):
         mean = sum(steps) / len(steps)
         value, unit = fl / mean / 1e12, "TFLOP/s"
         sample = f"the last {rows} chunk rows of sequence 0 per step"
-        metric, wl = PREFILL_METRIC, f"prefill_{args.prefill_workload}_hq24_hkv4_d128_bs16_bf16"
+        metric, wl = PREFILL_METRIC, prefill_workload_name(args.prefill_workload)
     else:
         from workloads import make_moe_case
         case = make_moe_case(device=dev, seed=20261500)

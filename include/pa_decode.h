@@ -340,8 +340,10 @@ PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_c
  * Layouts: query, out [num_rows][num_q_heads][head_dim] (the sequences'
  * chunks one after another); q_start int32 [num_seqs + 1], non-decreasing,
  * q_start[0] = 0 and q_start[num_seqs] = num_rows; caches, block_tables,
- * seq_lens as above.  max_q_len: an upper bound of every n_s (rows past it
- * are not written and raise PA_DEV_LEN_CLAMPED).  q_start is read on the
+ * seq_lens as above.  max_q_len: an upper bound of every n_s; the launch
+ * covers max_q_len rounded up to whole CTAs (whole CTA pairs at head_dim 256),
+ * and a chunk longer than that coverage raises PA_DEV_LEN_CLAMPED with its rows
+ * past the coverage not written.  q_start is read on the
  * device only: a sequence whose rows fall outside [0, num_rows], or whose
  * chunk is longer than seq_lens[s], is skipped and raises PA_DEV_BAD_ROWS.
  * Supported: head_dim 64, 128 or 256, block_size a multiple of 16, GQA group

@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
                 const int lim = pos - jt * N - hf * HC;
                 const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
-                const float pm = full ? tile_row_max<HC, false>(sb, lim) : tile_row_max<HC, true>(sb, lim);
+                const float pm = full ? tile_row_max<HC, false, true>(sb, lim)
+                                      : tile_row_max<HC, true, true>(sb, lim);
                 xch[(j & 1) * 256 + hf * 128 + rl] = pm;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
@@ -540,8 +541,8 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     }
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
-                l += full ? tile_row_p<T, HC, false>(sb, lim, sl2, mu)
-                          : tile_row_p<T, HC, true>(sb, lim, sl2, mu);
+                l += full ? tile_row_p<T, HC, false, true>(sb, lim, sl2, mu)
+                          : tile_row_p<T, HC, true, true>(sb, lim, sl2, mu);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();

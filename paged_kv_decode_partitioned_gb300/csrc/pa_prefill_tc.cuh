@@ -58,10 +58,9 @@ namespace pa {
 // two Q tiles of S + O still fit 512 columns, and each MMA group does 1.5x the
 // work for the same issue overhead: 736 -> 825 TFLOP/s).  head_dim 64 / 128 run
 // two Q tiles per CTA, each with one S buffer in tensor memory (the two tiles
-// take turns on the tensor pipe); head_dim 256 (its O alone takes 256 columns) runs
-// one Q tile with two S buffers, and its 128 KB K+V tile leaves room for one
-// shared-memory stage next to the 64 KB Q tile (64-token tiles with two
-// stages ran QK at N = 64: 737 against 911 TFLOP/s).
+// take turns on the tensor pipe).  head_dim 256 (its O alone takes 256
+// columns) runs on CTA pairs (pa_prefill_pair.cuh); the one-Q-tile layout with
+// two S buffers below is what it ran on single CTAs.
 template <int D>
 struct PrefillTcCfg {
     static constexpr int kQTiles = D <= 128 ? 2 : 1;
@@ -148,10 +147,40 @@ __device__ __forceinline__ bool mbar_wait_cycles(uint32_t bar, uint32_t parity) 
     }
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Row max of one S tile in tensor memory (raw logits, columns c <= lim only
 // when MASK), read in 32-column chunks with the next chunk's load in flight
-// while the current one is reduced.
-template <int N, bool MASK>
+// while the current one is reduced.  Unmasked and PACKED, each step folds two
+// values into one of eight chains with a three-input max.
+template <int N, bool MASK, bool PACKED>
 __device__ __forceinline__ float tile_row_max(uint32_t sb, int lim) {
     uint32_t rr[2][32];
     float mt = -INFINITY;
@@ -161,14 +190,24 @@ __device__ __forceinline__ float tile_row_max(uint32_t sb, int lim) {
         tc05::wait_ld(rr[h & 1]);
         if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
         float mx[8];   // eight independent max chains
+        if constexpr (PACKED && !MASK) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float v = __uint_as_float(rr[h & 1][c]);
-            const float u = (!MASK || h * 32 + c <= lim) ? v : -INFINITY;
-            mx[c & 7] = c < 8 ? u : fmaxf(mx[c & 7], u);
+            for (int k = 0; k < 16; ++k) {
+                const float v0 = __uint_as_float(rr[h & 1][2 * k]);
+                const float v1 = __uint_as_float(rr[h & 1][2 * k + 1]);
+                mx[k & 7] = k < 8 ? fmaxf(v0, v1) : fmax3(mx[k & 7], v0, v1);
+            }
+            mt = fmax3(mt, fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float v = __uint_as_float(rr[h & 1][c]);
+                const float u = (!MASK || h * 32 + c <= lim) ? v : -INFINITY;
+                mx[c & 7] = c < 8 ? u : fmaxf(mx[c & 7], u);
+            }
+            mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
         }
-        mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
     }
     return mt;
 }
@@ -176,31 +215,61 @@ __device__ __forceinline__ float tile_row_max(uint32_t sb, int lim) {
 // P = exp2(s * sl2 - mu) of one S tile (0 past lim when MASK), written as
 // 16-bit pairs over the first N / 2 columns of the tile (chunk h's S has been
 // read before its P lands on columns [16h, 16h + 16)); returns the row sum.
-template <typename T, int N, bool MASK>
+//
+// Unmasked and PACKED, the arithmetic runs on column pairs: one packed fma
+// forms both exponents (s * sl2 - mu), one packed add folds both values into
+// one of four pair-sum chains (A/B on GB300: +2 % at head_dim 128 and 256; at
+// head_dim 64 the pairs spill registers of the 576-thread CTA, so it keeps the
+// scalar form).
+template <typename T, int N, bool MASK, bool PACKED>
 __device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, float mu) {
     uint32_t rr[2][32];
-    float sm[8];   // eight independent sum chains
     tc05::ld32_async(sb, rr[0]);
+    if constexpr (PACKED && !MASK) {
+        uint64_t sp[4];   // four pair-sum chains
+        const uint64_t scale2 = f2(sl2, sl2), neg_mu2 = f2(-mu, -mu);
 #pragma unroll
-    for (int h = 0; h < N / 32; ++h) {
-        tc05::wait_ld(rr[h & 1]);
-        if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
-        uint32_t pk[16];
+        for (int h = 0; h < N / 32; ++h) {
+            tc05::wait_ld(rr[h & 1]);
+            if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
+            uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c = h * 32 + 2 * i;
-            float e0 = ex2(__uint_as_float(rr[h & 1][2 * i]) * sl2 - mu);
-            float e1 = ex2(__uint_as_float(rr[h & 1][2 * i + 1]) * sl2 - mu);
-            if (MASK) {
-                e0 = c <= lim ? e0 : 0.f;
-                e1 = c + 1 <= lim ? e1 : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const float2 x = f2_split(ffma2(
+                    f2(__uint_as_float(rr[h & 1][2 * i]), __uint_as_float(rr[h & 1][2 * i + 1])),
+                    scale2, neg_mu2));
+                const float e0 = ex2(x.x), e1 = ex2(x.y);
+                const uint64_t e = f2(e0, e1);
+                sp[i & 3] = (h == 0 && i < 4) ? e : fadd2(sp[i & 3], e);
+                pk[i] = Mma<T>::pack(e0, e1);
             }
-            sm[i & 7] = (h == 0 && i < 8) ? e0 + e1 : sm[i & 7] + (e0 + e1);
-            pk[i] = Mma<T>::pack(e0, e1);
+            tc05::st16(sb + h * 16, pk);
         }
-        tc05::st16(sb + h * 16, pk);
+        const float2 a = f2_split(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
+        return a.x + a.y;
+    } else {
+        float sm[8];   // eight independent sum chains
+#pragma unroll
+        for (int h = 0; h < N / 32; ++h) {
+            tc05::wait_ld(rr[h & 1]);
+            if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, rr[(h + 1) & 1]);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = h * 32 + 2 * i;
+                float e0 = ex2(__uint_as_float(rr[h & 1][2 * i]) * sl2 - mu);
+                float e1 = ex2(__uint_as_float(rr[h & 1][2 * i + 1]) * sl2 - mu);
+                if (MASK) {
+                    e0 = c <= lim ? e0 : 0.f;
+                    e1 = c + 1 <= lim ? e1 : 0.f;
+                }
+                sm[i & 7] = (h == 0 && i < 8) ? e0 + e1 : sm[i & 7] + (e0 + e1);
+                pk[i] = Mma<T>::pack(e0, e1);
+            }
+            tc05::st16(sb + h * 16, pk);
+        }
+        return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
     }
-    return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
 }
 
 template <typename T, int D>
@@ -542,7 +611,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 const int lim = pos - jt * N - hf * HC;   // own columns c <= lim are visible
                 // pass 1: this half's row max, swapped with the other half's
                 const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
-                const float pm = full ? tile_row_max<HC, false>(sb, lim) : tile_row_max<HC, true>(sb, lim);
+                const float pm = full ? tile_row_max<HC, false, (D >= 128)>(sb, lim)
+                                      : tile_row_max<HC, true, (D >= 128)>(sb, lim);
                 xch[(j & 1) * 256 + hf * 128 + rl] = pm;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
@@ -585,8 +655,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 }
                 // pass 2: P of this half over the first half of its own S columns
                 const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
-                l += full ? tile_row_p<T, HC, false>(sb, lim, sl2, mu)
-                          : tile_row_p<T, HC, true>(sb, lim, sl2, mu);
+                l += full ? tile_row_p<T, HC, false, (D >= 128)>(sb, lim, sl2, mu)
+                          : tile_row_p<T, HC, true, (D >= 128)>(sb, lim, sl2, mu);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
