@@ -16,12 +16,14 @@
 // 256 rows.  Warp roles (64 + 256 NQ threads):
 //   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
 //              x the CTA's chunk tokens), then K and V tiles of the context
-//              (128 tokens, 192 at head_dim 64) through NS shared-memory stages; each lane looks up the
-//              block of one (16-row box, 64-element piece) and issues its
-//              copy, so a tile's copies go out in parallel.  Each CTA starts
-//              its walk at its own tile and wraps around;
+//              (128 tokens, 192 at head_dim 64) through NS shared-memory
+//              stages; each lane looks up the block of one copy and issues it,
+//              so a tile's copies go out in parallel: K one (16-row box,
+//              64-element piece) per copy, V one 16-row box with all its pieces
+//              per copy (a cache map with the row ahead of the piece).  Each
+//              CTA starts its walk at its own tile and wraps around;
 //   warp 1     tensor-memory owner and MMA issuer (one thread): for each Q
-//              tile, S_j = Q K_j^T into one of two S buffers in tensor memory
+//              tile, S_j = Q K_j^T into the tile's S buffer in tensor memory
 //              and O += P_j V_j with P read from tensor memory (the S buffer
 //              it was written over) and O accumulating in tensor memory; it
 //              polls its barriers and issues whichever MMA is ready, so the
@@ -32,7 +34,8 @@
 //              tensor-memory lane): S -> causal mask -> scale -> the half's
 //              row max, swapped with the other half's through shared memory
 //              -> exp2 -> P (bf16 or f16) written back over the half's own S
-//              columns; O is rescaled in tensor memory (each half its own O
+//              columns (at head_dim >= 128 on column pairs: three-input max,
+//              packed f32x2 fma and add); O is rescaled in tensor memory (each half its own O
 //              columns) only when a row's max grows by more than 2^8 (exponents
 //              stay below 2^8 in between and the final division by the running
 //              sum is exact either way); finally O / l -> out.

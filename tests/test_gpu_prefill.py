@@ -34,6 +34,10 @@ SHAPES = [
     ([500, 130], [250, 9], 32, 4, 64, 128, torch.float16),
     ([700], [60], 16, 2, 256, 80, torch.bfloat16),
     ([1100, 40], [130, 31], 24, 4, 128, 112, torch.bfloat16),
+    # head_dim 256 on CTA pairs: one chunk token per CTA (GQA 128), odd CTA counts;
+    # a long context walked by several pairs of one sequence
+    ([50, 3], [5, 2], 128, 1, 256, 16, torch.bfloat16),
+    ([5000], [300], 4, 2, 256, 16, torch.float16),
 ]
 IDS = [f"d{s[4]}_g{s[2] // s[3]}_bs{s[5]}_{str(s[6])[6:]}" for s in SHAPES]
 
