@@ -168,14 +168,14 @@ PA_API int pa_default_single_pass_max_len(int num_seqs, int num_kv_heads, int pa
 
 /*
  * pa_default_partition_size -- the launch heuristic's partition size (the
- * pages use 512 in one file and 256 in another).  Returns the smallest of
- * 256, 512 and 1024 tokens for which the batch's partition units
- * num_seqs * num_kv_heads * ceil(max_seq_len / P) fit in one wave of resident
- * attention CTAs (num_sms x CTAs per SM), else 1024; rounded up to a multiple
- * of block_size.  Measured on GB300: one wave of long partitions beats two
- * waves of short ones, and at more than a wave the longer partitions write
- * fewer partials.  num_sms <= 0 queries the current device.  Returns 0 on bad
- * arguments.
+ * pages use 512 in one file and 256 in another).  Of 256, 512 and 1024
+ * tokens (each rounded up to a multiple of block_size), returns the P that
+ * minimises ceil(U_P / W) * (P + 256), where U_P = num_seqs * num_kv_heads *
+ * ceil(max_seq_len / P) partition units run in waves of W = num_sms x resident
+ * attention CTAs per SM, and 256 tokens stand for a unit's fixed cost; ties go
+ * to the larger P (fewer partials).  Fitted to a GB300 sweep over 1..256
+ * sequences of 1K..64K tokens.  num_sms <= 0 queries the current device.
+ * Returns 0 on bad arguments.
  */
 PA_API int pa_default_partition_size(int num_seqs, int num_kv_heads, int block_size,
                                      int head_dim, int max_seq_len, int num_sms);
@@ -201,6 +201,11 @@ enum {
  *   PA_AUTO_DENSE when threshold <= partition size (every sequence longer
  *     than one partition is split) and num_seqs * num_kv_heads < num_sms;
  *   PA_AUTO_WORKLIST otherwise.
+ * With the default threshold, a batch that would take the dense form runs
+ * single pass instead (threshold raised to max_seq_len) when its single-pass
+ * grid, each unit split over a cluster of C CTAs, fits one wave of resident
+ * CTAs and ceil(max_seq_len / C) <= partition size: one launch for a batch
+ * that small.
  * Any output pointer may be NULL.  num_sms <= 0 queries the current device.
  * Returns PA_OK, PA_ERR_INVALID_ARGUMENT or PA_ERR_UNSUPPORTED (a partition
  * size that is not a multiple of block_size).

@@ -342,24 +342,28 @@ int partitioned_slots_per_sm(int D) {
     return v;
 }
 
-// The partition size of the launch heuristic: the smallest of 256, 512 and
-// 1024 tokens whose partition units (sequence x KV head x partition) fit in
-// one wave of resident CTAs, else 1024 (more than a wave of work anyway:
-// fewer, longer partitions write fewer partials).  Rounded up to a multiple
-// of the block size.  Measured on GB300 over 1..256 sequences of 1K..64K
-// tokens (one wave of 256 long units beat two waves of 512 shorter ones).
+// The partition size of the launch heuristic: of 256, 512 and 1024 tokens
+// (each rounded up to a multiple of the block size), the one that minimises
+// waves x (P + 256): the partition units (sequence x KV head x partition) run
+// in ceil(units / resident CTAs) waves, each as long as a partition plus a
+// fixed cost worth ~256 tokens (a unit's set-up, its partials, its share of
+// the reduce); ties go to the longer partition, which writes fewer partials.
+// Fitted to the GB300 sweep over 1..256 sequences of 1K..64K tokens, where it
+// picks the fastest size, or one within 1 % of it, at every point.
 int default_partition(int S, int Hkv, int bs, int max_seq_len, int num_sms, int slots_per_sm) {
     const int64_t wave = static_cast<int64_t>(num_sms) * slots_per_sm;
-    int P = 1024;
-    for (int cand : {256, 512, 1024}) {
-        const int64_t units = static_cast<int64_t>(S) * Hkv * ((max_seq_len + cand - 1) / cand);
-        if (units <= wave) {
-            P = cand;
-            break;
+    int best = 0;
+    int64_t best_cost = 0;
+    for (int cand : {1024, 512, 256}) {
+        const int P = bs > 0 && cand % bs != 0 ? (cand + bs - 1) / bs * bs : cand;
+        const int64_t units = static_cast<int64_t>(S) * Hkv * ((max_seq_len + P - 1) / P);
+        const int64_t cost = (units + wave - 1) / wave * (P + 256);
+        if (best == 0 || cost < best_cost) {
+            best = P;
+            best_cost = cost;
         }
     }
-    if (bs > 0 && P % bs != 0) P = (P + bs - 1) / bs * bs;
-    return P;
+    return best;
 }
 
 // The launch form pa_decode_auto takes for a batch (host values only):
@@ -407,6 +411,22 @@ int resolve_auto(int S, int Hkv, int D, int bs, int max_seq_len, long long max_t
         form = PA_AUTO_SINGLE_PASS;
     else if (thr <= P && static_cast<int64_t>(S) * Hkv < num_sms)
         form = PA_AUTO_DENSE;
+    if (form == PA_AUTO_DENSE && thr_in < 0) {
+        // A batch so small that the single-pass grid (each unit split over a
+        // cluster of C CTAs, C as launch_single_pass picks it) fits one wave
+        // with no CTA taking more tokens than a partition: one launch instead
+        // of two (1 x 1024 tokens on GB300: 10.2 against 12.3 us).
+        const int64_t units = static_cast<int64_t>(S) * Hkv;
+        const int64_t resident = static_cast<int64_t>(num_sms) *
+                                 (D == 64 || D == 128 || D == 256 ? partitioned_slots_per_sm(D) : 3);
+        const int64_t C = units > 0 ? single_pass_cluster(static_cast<int>(units),
+                                                          static_cast<int>(resident))
+                                    : 1;
+        if (units * C <= resident && (max_seq_len + C - 1) / C <= P) {
+            thr = max_seq_len;
+            form = PA_AUTO_SINGLE_PASS;
+        }
+    }
     a->thr = thr;
     a->P = P;
     a->form = form;

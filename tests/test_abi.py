@@ -170,12 +170,15 @@ def test_default_threshold_uses_sm_count(lib):
 
 
 @pytest.mark.parametrize("S,L,want", [
-    # smallest of 256 / 512 / 1024 whose S * 4 * ceil(L / P) units fit one wave of
-    # 152 SMs x 3 resident CTAs (456); 1024 when none does
+    # of 256 / 512 / 1024, the P minimising ceil(S * 4 * ceil(L / P) / 456) * (P + 256)
+    # (152 SMs x 3 resident CTAs per wave), ties to the larger P
     (1, 1024, 256), (1, 16384, 256), (1, 32768, 512), (1, 65536, 1024),
     (4, 4096, 256), (4, 8192, 512), (4, 16384, 1024), (4, 65536, 1024),
     (16, 1024, 256), (16, 2048, 512), (16, 4096, 1024), (16, 65536, 1024),
     (256, 65536, 1024),
+    # 512 units at P = 1024 are a wave and a bit: three waves of 512-token
+    # partitions (2304) beat two of 1024 (2560)
+    (4, 32768, 512), (16, 8192, 512),
 ])
 def test_default_partition_size_from_units_and_sms(lib, S, L, want):
     assert lib.pa_default_partition_size(S, 4, 16, 128, L, 152) == want
@@ -199,8 +202,15 @@ def test_auto_resolve_launch_forms(lib):
     # few units: everything longer than one partition is split on the dense grid
     assert _resolve(lib, 1, 4, 65536, -1, 0) == (0, (1024, 1024, 1))
     assert _resolve(lib, 16, 4, 16384, -1, 0) == (0, (1024, 1024, 1))
-    assert _resolve(lib, 1, 4, 1000, -1, 0) == (0, (256, 256, 1))
     assert _resolve(lib, 1, 4, 200, -1, 0) == (0, (256, 256, 0))   # fits one partition
+    # a batch whose single-pass grid (4 units x clusters of 8) fits a wave with at most a
+    # partition per CTA: one launch, the threshold raised to max_seq_len
+    assert _resolve(lib, 1, 4, 1000, -1, 0) == (0, (1000, 256, 0))
+    assert _resolve(lib, 1, 4, 2048, -1, 0) == (0, (2048, 256, 0))
+    assert _resolve(lib, 1, 4, 4096, -1, 0) == (0, (256, 256, 1))   # 512 tokens per CTA
+    assert _resolve(lib, 16, 4, 1024, -1, 0) == (0, (256, 256, 1))  # 64 x 8 CTAs > a wave
+    assert _resolve(lib, 1, 4, 1000, -1, 256) == (0, (1000, 256, 0))
+    assert _resolve(lib, 1, 4, 1000, 256, 256) == (0, (256, 256, 1))  # explicit: kept
     # enough units: the pages' 8192 threshold, work list above it, single pass below
     assert _resolve(lib, 256, 4, 65536, -1, 512) == (0, (8192, 512, 2))
     assert _resolve(lib, 64, 4, 8192, -1, 512) == (0, (8192, 512, 0))
