@@ -390,6 +390,9 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
+    # rank 0 alone runs the oracle, on every host core (torchrun sets
+    # OMP_NUM_THREADS=1 for its ranks)
+    oracle.set_num_threads(cpu_threads())
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = make_inputs(args.workload, dev, args.num_seqs)
     w = case.workload
@@ -787,6 +790,8 @@ def oracle_moe_sample(case, target_seconds):
 def run_next_reference(args, world):
     """``--impl reference`` for the prefill / MoE paths: the oracle on the host."""
     import torch
+    import oracle
+    oracle.set_num_threads(cpu_threads())   # every host core, whatever torchrun set
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     steps = []
     if args.path == "prefill":
