@@ -54,6 +54,19 @@ namespace pa {
 #define PA_PREFILL_MMA_SLEEP_NS 0
 #endif
 
+// Softmax warpgroups per Q tile: 2 = each row's S columns split between two
+// threads (which swap row maxima and sums), 1 = one thread per whole row.
+#ifndef PA_PREFILL_SPLIT_D64
+#define PA_PREFILL_SPLIT_D64 2
+#endif
+#ifndef PA_PREFILL_SPLIT_D128
+#define PA_PREFILL_SPLIT_D128 1
+#endif
+// Whole rows of head_dim >= 128 hold their S in registers between the passes.
+#ifndef PA_PREFILL_REGROW
+#define PA_PREFILL_REGROW 1
+#endif
+
 // Tile plan per head_dim.  A tcgen05.mma with M = 128 and K = 16 costs about
 // 80 cycles whatever N <= 128 is (measured on GB300: N = 64 reaches 38 % of
 // the tensor peak, N = 128 80 %, N = 256 all of it), so the MMAs are kept
@@ -89,16 +102,19 @@ struct PrefillTcCfg {
     static constexpr int kTileBars = 7;
     static constexpr int kNumBars = 3 + 4 * kStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
-    // each Q tile's softmax runs in two warpgroups, one per half of the S
-    // columns; they swap row maxima (two buffers by tile parity) and, at the
-    // end, row sums through shared memory, synchronised by mbarriers
-    // (xbar[2] and xend per Q tile, one arrive per warp)
-    static constexpr int kHalfCols = kN / 2;
+    // each Q tile's softmax runs in kSplit warpgroups, one per 1 / kSplit of
+    // the S columns of every row; with two, they swap row maxima (two buffers
+    // by tile parity) and, at the end, row sums through shared memory,
+    // synchronised by mbarriers (xbar[2] and xend per Q tile, one arrive per
+    // warp)
+    static constexpr int kSplit = D <= 64 ? PA_PREFILL_SPLIT_D64 : PA_PREFILL_SPLIT_D128;
+    static_assert(kSplit == 1 || kSplit == 2, "one or two softmax warpgroups per Q tile");
+    static constexpr int kHalfCols = kN / kSplit;
     static constexpr int kXBarOffset = kSlotOffset + 16;
     static constexpr int kXOffset = kXBarOffset + kQTiles * 3 * 8 + 8;
     static constexpr int kXBytes = kQTiles * 3 * 2 * 128 * 4;   // [tile][max0, max1, sum][half][row]
     static constexpr int kLaunchBytes = kXOffset + kXBytes + 1024;
-    static constexpr int kThreads = 64 + 256 * kQTiles;
+    static constexpr int kThreads = 64 + 128 * kSplit * kQTiles;
     // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
     static constexpr int kOCol = kSBufs * kN;
     static constexpr int kTileCols = kSBufs * kN + D;
@@ -275,6 +291,67 @@ __device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, flo
     }
 }
 
+// Register-resident form of the two passes, for one thread per whole row
+// with registers to spare: the row's S is read from tensor memory once (each
+// 32-column chunk's read in flight while the previous chunk is reduced to the
+// row max) and the P pass works from the registers.
+template <int N, bool MASK>
+__device__ __forceinline__ float row_load_max(uint32_t (&sr)[N / 32][32], uint32_t sb, int lim) {
+    float mt = -INFINITY;
+    tc05::ld32_async(sb, sr[0]);
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+        tc05::wait_ld(sr[h]);   // the only read in flight is chunk h's
+        if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, sr[h + 1]);
+        float mx[8];
+        if constexpr (!MASK) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float v0 = __uint_as_float(sr[h][2 * k]), v1 = __uint_as_float(sr[h][2 * k + 1]);
+                mx[k & 7] = k < 8 ? fmaxf(v0, v1) : fmax3(mx[k & 7], v0, v1);
+            }
+            mt = fmax3(mt, fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float u = h * 32 + c <= lim ? __uint_as_float(sr[h][c]) : -INFINITY;
+                mx[c & 7] = c < 8 ? u : fmaxf(mx[c & 7], u);
+            }
+            mt = fmaxf(mt, fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))));
+        }
+    }
+    return mt;
+}
+
+template <typename T, int N, bool MASK>
+__device__ __forceinline__ float row_p_regs(const uint32_t (&sr)[N / 32][32], uint32_t sb, int lim,
+                                            float sl2, float mu) {
+    uint64_t sp[4];   // four pair-sum chains
+    const uint64_t scale2 = f2(sl2, sl2), neg_mu2 = f2(-mu, -mu);
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 x = f2_split(ffma2(
+                f2(__uint_as_float(sr[h][2 * i]), __uint_as_float(sr[h][2 * i + 1])), scale2, neg_mu2));
+            float e0 = ex2(x.x), e1 = ex2(x.y);
+            if (MASK) {
+                const int c = h * 32 + 2 * i;
+                e0 = c <= lim ? e0 : 0.f;
+                e1 = c + 1 <= lim ? e1 : 0.f;
+            }
+            const uint64_t e = f2(e0, e1);
+            sp[i & 3] = (h == 0 && i < 4) ? e : fadd2(sp[i & 3], e);
+            pk[i] = Mma<T>::pack(e0, e1);
+        }
+        tc05::st16(sb + h * 16, pk);
+    }
+    const float2 a = f2_split(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
+    return a.x + a.y;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     pa_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -344,11 +421,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             const uint32_t tb = tile_bars + t * 56;
             for (int i = 0; i < 2; ++i) {
                 mbar_init(tb + i * 8, 1);          // s_full
-                mbar_init(tb + 16 + i * 8, 8);     // p_full: one arrive per softmax warp
+                mbar_init(tb + 16 + i * 8, 4 * C::kSplit);   // p_full: one arrive per softmax warp
                 mbar_init(tb + 32 + i * 8, 1);     // s_free
             }
             mbar_init(tb + 48, 1);                 // o_full
-            for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
+            if (C::kSplit > 1)
+                for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
         }
         fence_mbar_init();
     }
@@ -483,109 +561,119 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
-            constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
-            bool ok = mbar_wait_cycles(q_full, 0);
-            int qk[NQ], pv[NQ];
+        // The whole warp runs this loop, its control flow warp-uniform (barrier
+        // tests folded into one vote), and one elected lane issues each MMA and
+        // commit: a lone thread in a divergent branch issued an MMA every ~47
+        // cycles, slower than the pipe once the softmax warps share its scheduler.
+        constexpr uint32_t kAll = 0xffffffffu;
+        constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
+        constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
+        bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
+        int qk[NQ], pv[NQ];
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) qk[t] = pv[t] = 0;
-            bool idle = false;
-            long long idle_since = 0;
-            while (ok) {
-                bool busy = false, progress = false;
+        for (int t = 0; t < NQ; ++t) qk[t] = pv[t] = 0;
+        bool idle = false;
+        long long idle_since = 0;
+        while (ok) {
+            bool busy = false, progress = false;
 #pragma unroll
-                for (int t = 0; t < NQ; ++t) {
-                    if (t >= nq) break;
-                    busy |= pv[t] < ntiles;
-                    const uint32_t tb = tile_bars + t * 56;
-                    const uint32_t tcol = tmem + t * C::kTileCols;
-                    // The tile's three barrier tests go out together, so their
-                    // shared-memory latencies overlap (this thread alone feeds the
-                    // tensor pipe: time spent here is time the pipe may idle).  A
-                    // test of an index past the loop's end is ignored.
-                    const int jp = pv[t], jq = qk[t];
-                    const bool p_ok = mbar_test(tb + 16 + (jp % SB) * 8, (jp / SB) & 1u);
-                    const bool v_ok = mbar_test(v_full + (jp % NS) * 8, (jp / NS) & 1u);
-                    const bool k_ok = mbar_test(k_full + (jq % NS) * 8, (jq / NS) & 1u);
-                    // PV of the oldest tile whose P is ready
-                    int j = jp;
-                    if (j < jq && p_ok && v_ok) {
-                        tc05::fence_after_sync();
-                        const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
+            for (int t = 0; t < NQ; ++t) {
+                if (t >= nq) break;
+                busy |= pv[t] < ntiles;
+                const uint32_t tb = tile_bars + t * 56;
+                const uint32_t tcol = tmem + t * C::kTileCols;
+                // The tile's three barrier tests go out together, so their
+                // shared-memory latencies overlap, and one vote makes the result
+                // uniform over the warp.  A test of an index past the loop's end
+                // is ignored.
+                const int jp = pv[t], jq = qk[t];
+                const uint32_t ready = __reduce_and_sync(
+                    kAll, (mbar_test(tb + 16 + (jp % SB) * 8, (jp / SB) & 1u) ? 1u : 0u) |
+                              (mbar_test(v_full + (jp % NS) * 8, (jp / NS) & 1u) ? 2u : 0u) |
+                              (mbar_test(k_full + (jq % NS) * 8, (jq / NS) & 1u) ? 4u : 0u));
+                // PV of the oldest tile whose P is ready
+                int j = jp;
+                if (j < jq && (ready & 3u) == 3u) {
+                    tc05::fence_after_sync();
+                    const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
-                        for (int kt = 0; kt < N / 16; ++kt)
-                            // tokens [16 kt, 16 kt + 16) lie in half (16 kt) / (N / 2),
-                            // whose P occupies the first half of its own S columns
-                            tc05::mma_ts(tcol + C::kOCol,
-                                         tcol + (j % SB) * N +
-                                             ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
-                                         tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024),
-                                         idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
-                        // s_free: with one S buffer the commit of the QK issued next
-                        // (S_{j+1}) tracks this PV as well, so none is needed
-                        if (SB > 1) tc05::commit(tb + 32 + (j % SB) * 8);
-                        bool last_user = true;   // the V stage is free once every tile used it
+                    for (int kt = 0; kt < N / 16; ++kt)
+                        // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
+                        // whose P occupies the first half of its own S columns
+                        tc05::mma_ts_elect(tcol + C::kOCol,
+                                           tcol + (j % SB) * N +
+                                               ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) +
+                                               kt * 8,
+                                           tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024),
+                                           idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
+                    // s_free: with one S buffer the commit of the QK issued next
+                    // (S_{j+1}) tracks this PV as well, so none is needed
+                    if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
+                    bool last_user = true;   // the V stage is free once every tile used it
 #pragma unroll
-                        for (int u = 0; u < NQ; ++u)
-                            if (u != t && u < nq && pv[u] <= j) last_user = false;
-                        if (last_user) tc05::commit(v_empty + (j % NS) * 8);
-                        if (j == ntiles - 1) tc05::commit(tb + 48);   // o_full
-                        ++pv[t];
-                        progress = true;
-                    }
-                    // QK of the next tile into S buffer j % SB, whose P the PV of
-                    // j - SB reads: that PV only has to be issued, not finished,
-                    // since this thread's MMAs run on the tensor pipe in issue
-                    // order (the QK's writes come after the PV's operand reads)
-                    j = jq;
-                    if (j < ntiles && j <= pv[t] + SB - 1 && k_ok) {
-                        tc05::fence_after_sync();
-                        const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
-                        const uint32_t qst = q_smem + t * C::kQTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            tc05::mma_ss(
-                                tcol + (j % SB) * N,
-                                tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16,
-                                                 1024),
-                                tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16,
-                                                 1024),
-                                idesc_qk, kk > 0 ? 1u : 0u);
-                        tc05::commit(tb + (j % SB) * 8);   // s_full
-                        bool last_user = true;
-#pragma unroll
-                        for (int u = 0; u < NQ; ++u)
-                            if (u != t && u < nq && qk[u] <= j) last_user = false;
-                        if (last_user) tc05::commit(k_empty + (j % NS) * 8);
-                        ++qk[t];
-                        progress = true;
-                    }
+                    for (int u = 0; u < NQ; ++u)
+                        if (u != t && u < nq && pv[u] <= j) last_user = false;
+                    if (last_user) tc05::commit_elect(v_empty + (j % NS) * 8);
+                    if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
+                    ++pv[t];
+                    progress = true;
                 }
-                if (!busy) break;
-                if (progress) {
-                    idle = false;
-                } else if (!idle) {
-                    idle = true;
-                    idle_since = clock64();
-                } else if (clock64() - idle_since > 1000000000ll) {
-                    ok = false;
-                } else if (PA_PREFILL_MMA_SLEEP_NS > 0) {
-                    __nanosleep(PA_PREFILL_MMA_SLEEP_NS);
+                // QK of the next tile into S buffer j % SB, whose P the PV of
+                // j - SB reads: that PV only has to be issued, not finished,
+                // since one thread's MMAs run on the tensor pipe in issue order
+                // (the QK's writes come after the PV's operand reads)
+                j = jq;
+                if (j < ntiles && j <= pv[t] + SB - 1 && (ready & 4u)) {
+                    tc05::fence_after_sync();
+                    const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
+                    const uint32_t qst = q_smem + t * C::kQTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc05::mma_ss_elect(
+                            tcol + (j % SB) * N,
+                            tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
+                            tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16, 1024),
+                            idesc_qk, kk > 0 ? 1u : 0u);
+                    tc05::commit_elect(tb + (j % SB) * 8);   // s_full
+                    bool last_user = true;
+#pragma unroll
+                    for (int u = 0; u < NQ; ++u)
+                        if (u != t && u < nq && qk[u] <= j) last_user = false;
+                    if (last_user) tc05::commit_elect(k_empty + (j % NS) * 8);
+                    ++qk[t];
+                    progress = true;
                 }
             }
-            if (!ok) atomicOr(p.status, kWaitTimeout);
-            // every MMA issued has completed before tensor memory is freed
-            tc05::commit(mma_done);
-            (void)mbar_wait_cycles(mma_done, 0);
+            if (!busy) break;
+            if (progress) {
+                idle = false;
+            } else if (!idle) {
+                idle = true;
+                idle_since = clock64();
+            } else if (__any_sync(kAll, clock64() - idle_since > 1000000000ll)) {
+                ok = false;
+            } else if (PA_PREFILL_MMA_SLEEP_NS > 0) {
+                __nanosleep(PA_PREFILL_MMA_SLEEP_NS);
+            }
         }
+        if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
+        // every MMA issued has completed before tensor memory is freed
+        tc05::commit_elect(mma_done);
+        (void)mbar_wait_cycles(mma_done, 0);
         __syncwarp();
     } else {
         // ------------------------------ softmax ------------------------------
         constexpr int HC = C::kHalfCols;
         const int idx = warp - 2;
-        const int t = idx >> 3;          // the Q tile of this warp
-        const int hf = (idx >> 2) & 1;   // the half of the S columns it handles
+        constexpr int SP = C::kSplit;
+        // column pairs (packed arithmetic) where the registers allow them: the
+        // 18-warp CTA of head_dim 64 with split rows is capped at 96 per thread
+        constexpr bool PK = D >= 128 || SP == 1;
+        // whole rows of head_dim >= 128 keep S in registers between the passes
+        constexpr bool RR = PA_PREFILL_REGROW && SP == 1 && D >= 128;
+        constexpr int RC = RR ? N / 32 : 1;
+        const int t = idx / (4 * SP);     // the Q tile of this warp
+        const int hf = (idx >> 2) % SP;   // the part of the S columns it handles
         if (t < nq) {
             const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
             const int rl = quarter * 32 + lane;   // row within the Q tile
@@ -599,7 +687,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             const uint32_t xbar = base + C::kXBarOffset + t * 3 * 8;   // max exchange x2, sums
             float *xch = reinterpret_cast<float *>(smem + C::kXOffset) + t * 3 * 256;
             const float sl2 = p.scale_log2;
-            float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
+            float m = -INFINITY, l = 0.f;   // l: this part's share of the row sum
             bool ok = true;
             for (int j = 0; j < ntiles; ++j) {
                 const int b = j % SB;
@@ -609,27 +697,36 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     break;
                 }
                 tc05::fence_after_sync();
-                const uint32_t sb = tcol + b * N + hf * HC;   // this half's S columns
+                const uint32_t sb = tcol + b * N + hf * HC;   // this part's S columns
                 const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
                 const int lim = pos - jt * N - hf * HC;   // own columns c <= lim are visible
-                // pass 1: this half's row max, swapped with the other half's
+                // pass 1: this part's row max (with two parts, swapped with the other's)
                 const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
-                const float pm = full ? tile_row_max<HC, false, (D >= 128)>(sb, lim)
-                                      : tile_row_max<HC, true, (D >= 128)>(sb, lim);
-                xch[(j & 1) * 256 + hf * 128 + rl] = pm;
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
-                if (!__all_sync(0xffffffffu, mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
-                    ok = false;
-                    break;
+                uint32_t sr[RC][32];
+                float pm;
+                if constexpr (RR)
+                    pm = full ? row_load_max<N, false>(sr, sb, lim) : row_load_max<N, true>(sr, sb, lim);
+                else
+                    pm = full ? tile_row_max<HC, false, PK>(sb, lim)
+                              : tile_row_max<HC, true, PK>(sb, lim);
+                float mt = pm;
+                if constexpr (SP > 1) {
+                    xch[(j & 1) * 256 + hf * 128 + rl] = pm;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                 }
-                float mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                 mt *= sl2;   // log2 domain (scale > 0)
                 if (j == 0) {
                     m = mt;   // -inf when every column of the first tile is past the row
                 } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
-                    // O must hold P_{j-1} V_{j-1} before it is rescaled (both halves
-                    // see the same maxima, so both take this branch for a row).  With
+                    // O must hold P_{j-1} V_{j-1} before it is rescaled (all parts
+                    // see the same maxima, so all take this branch for a row).  With
                     // one S buffer, PV_{j-1} went out before QK_j from the same thread,
                     // so the S_j commit waited for above has already seen it finish.
                     if (SB > 1) {
@@ -645,27 +742,33 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     const float alpha = m == mn ? 1.f : ex2(m - mn);   // 0 when m was -inf
                     m = mn;
                     l *= alpha;
+                    // this part's O columns, 16 at a time while the S row is held
+                    constexpr int OC = RR ? 16 : 32;
 #pragma unroll
-                    for (int c0 = 0; c0 < D / 2; c0 += 32) {   // this half's O columns
-                        uint32_t rr[32];
-                        const uint32_t oc = tcol + C::kOCol + hf * (D / 2) + c0;
-                        tc05::ld32(oc, rr);
+                    for (int c0 = 0; c0 < D / SP; c0 += OC) {
+                        uint32_t rr[OC];
+                        const uint32_t oc = tcol + C::kOCol + hf * (D / SP) + c0;
+                        if constexpr (RR) tc05::ld16(oc, rr); else tc05::ld32(oc, rr);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
+                        for (int i = 0; i < OC; ++i)
                             rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                        tc05::st32(oc, rr);
+                        if constexpr (RR) tc05::st16(oc, rr); else tc05::st32(oc, rr);
                     }
                 }
-                // pass 2: P of this half over the first half of its own S columns
+                // pass 2: P of this part over the first half of its own S columns
                 const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
-                l += full ? tile_row_p<T, HC, false, (D >= 128)>(sb, lim, sl2, mu)
-                          : tile_row_p<T, HC, true, (D >= 128)>(sb, lim, sl2, mu);
+                if constexpr (RR)
+                    l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu)
+                              : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu);
+                else
+                    l += full ? tile_row_p<T, HC, false, PK>(sb, lim, sl2, mu)
+                              : tile_row_p<T, HC, true, PK>(sb, lim, sl2, mu);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(tb + 16 + b * 8);   // p_full
             }
-            if (ok) {   // the row sum is the two halves' shares
+            if (SP > 1 && ok) {   // the row sum is the two parts' shares
                 xch[2 * 256 + hf * 128 + rl] = l;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(xbar + 16);
@@ -681,11 +784,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 T *orow = static_cast<T *>(p.out) +
                           (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) *
-                              D + hf * (D / 2);
+                              D + hf * (D / SP);
 #pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 32) {   // this half's output columns
+                for (int c0 = 0; c0 < D / SP; c0 += 32) {   // this part's output columns
                     uint32_t rr[32];
-                    tc05::ld32(tcol + C::kOCol + hf * (D / 2) + c0, rr);
+                    tc05::ld32(tcol + C::kOCol + hf * (D / SP) + c0, rr);
                     if (valid) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) {
