@@ -378,94 +378,77 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
         if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
     } else if (warp == 1) {
         // ------------------------- MMA issuer (even CTA) -------------------------
-        // The whole warp runs the loop (warp-uniform control flow, barrier tests
-        // folded into one vote) and one elected lane issues each MMA and commit,
-        // which issues far faster than a lone thread in a divergent branch.
+        // The whole warp runs a fixed issue sequence (warp-uniform control flow)
+        // and one elected lane issues each MMA and commit: QK of the first SB
+        // tiles for every Q tile, then per K/V tile j and Q tile t the PV of j
+        // and the QK of j + SB.  Each step waits (suspending, bounded) on the one
+        // barrier it needs, and every barrier waited on depends only on MMAs
+        // issued earlier in the sequence, so the order cannot deadlock.
         if (rank == 0) {
             constexpr uint32_t kAll = 0xffffffffu;
             constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 256);
             constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 256);
             constexpr uint16_t kBoth = 0x3;
             bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
-            int qk[NQ], pv[NQ];
+            auto wait = [&](uint32_t bar, uint32_t parity) {
+                ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
+                return ok;
+            };
+            // S_j = Q_t K_j^T into S buffer j % SB; the last Q tile's QK frees the K stage
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t tb = tile_bars + t * 56;
+                const uint32_t tcol = tmem + t * C::kTileCols;
+                const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
+                const uint32_t qst = q_smem + t * C::kQTileBytes;
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) qk[t] = pv[t] = 0;
-            bool idle = false;
-            long long idle_since = 0;
-            while (ok) {
-                bool busy = false, progress = false;
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc05::mma2_ss_elect(
+                        tcol + (j % SB) * N,
+                        tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
+                        tc05::sw128_desc(kst + (kk >> 2) * C::kKPiece + (kk & 3) * 32, 16, 1024),
+                        idesc_qk, kk > 0 ? 1u : 0u);
+                tc05::commit2_elect(tb + (j % SB) * 8, kBoth);   // s_full
+                if (t == nq - 1) tc05::commit2_elect(k_empty + (j % NS) * 8, kBoth);
+            };
+            // O_t += P_j V_j; the last Q tile's PV frees the V stage
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t tb = tile_bars + t * 56;
+                const uint32_t tcol = tmem + t * C::kTileCols;
+                const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kKBytes;
 #pragma unroll
-                for (int t = 0; t < NQ; ++t) {
-                    if (t >= nq) break;
-                    busy |= pv[t] < ntiles;
-                    const uint32_t tb = tile_bars + t * 56;
-                    const uint32_t tcol = tmem + t * C::kTileCols;
-                    // the tile's barrier tests go out together, so their latencies
-                    // overlap; one vote makes the result uniform over the warp
-                    const int jp = pv[t], jq = qk[t];
-                    const bool vt_ok = jp != j_tail || mbar_test(vtail2, 0);
-                    const uint32_t ready = __reduce_and_sync(
-                        kAll, (mbar_test(tb + 32 + (jp % SB) * 8, (jp / SB) & 1u) ? 1u : 0u) |
-                                  (mbar_test(v_full + (jp % NS) * 8, (jp / NS) & 1u) && vt_ok ? 2u : 0u) |
-                                  (mbar_test(k_full + (jq % NS) * 8, (jq / NS) & 1u) ? 4u : 0u));
-                    // PV of the oldest tile whose P is ready
-                    int j = jp;
-                    if (j < jq && (ready & 3u) == 3u) {
+                for (int kt = 0; kt < N / 16; ++kt)
+                    // tokens [16 kt, 16 kt + 16) lie in half (16 kt) / HC, whose P
+                    // occupies the first half of that half's S columns
+                    tc05::mma2_ts_elect(tcol + C::kOCol,
+                                        tcol + (j % SB) * N + ((16 * kt) / HC) * (HC / 2) + kt * 8,
+                                        tc05::sw128_desc(vst + kt * C::kVBoxBytes, 2048, 1024),
+                                        idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
+                // s_free: with one S buffer the commit of the QK issued next
+                // (S_{j+1}) tracks this PV as well, so none is needed
+                if (SB > 1) tc05::commit2_elect(tb + 16 + (j % SB) * 8, kBoth);
+                if (t == nq - 1) tc05::commit2_elect(v_empty + (j % NS) * 8, kBoth);
+                if (j == ntiles - 1) tc05::commit2_elect(tb + 48, kBoth);   // o_full
+            };
+            for (int j = 0; ok && j < SB && j < ntiles; ++j) {
+                if (!wait(k_full + (j % NS) * 8, (j / NS) & 1u)) break;
+                tc05::fence_after_sync();
+                for (int t = 0; t < nq; ++t) issue_qk(t, j);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                // V of tile j: both halves landed, and in the tail tile both CTAs'
+                // rows past the context zeroed
+                if (!wait(v_full + (j % NS) * 8, (j / NS) & 1u)) break;
+                if (j == j_tail && !wait(vtail2, 0)) break;
+                const int jn = j + SB;   // the QK issued behind this tile's PV
+                for (int t = 0; t < nq; ++t) {
+                    if (!wait(tile_bars + t * 56 + 32 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
+                    tc05::fence_after_sync();
+                    issue_pv(t, j);
+                    if (jn < ntiles) {
+                        if (t == 0 && !wait(k_full + (jn % NS) * 8, (jn / NS) & 1u)) break;
                         tc05::fence_after_sync();
-                        const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kKBytes;
-#pragma unroll
-                        for (int kt = 0; kt < N / 16; ++kt)
-                            // tokens [16 kt, 16 kt + 16) lie in half (16 kt) / HC, whose P
-                            // occupies the first half of that half's S columns
-                            tc05::mma2_ts_elect(tcol + C::kOCol,
-                                                tcol + (j % SB) * N + ((16 * kt) / HC) * (HC / 2) + kt * 8,
-                                                tc05::sw128_desc(vst + kt * C::kVBoxBytes, 2048, 1024),
-                                                idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
-                        // s_free: with one S buffer the commit of the QK issued next
-                        // (S_{j+1}) tracks this PV as well, so none is needed
-                        if (SB > 1) tc05::commit2_elect(tb + 16 + (j % SB) * 8, kBoth);
-                        bool last_user = true;   // the V stage is free once every tile used it
-#pragma unroll
-                        for (int u = 0; u < NQ; ++u)
-                            if (u != t && u < nq && pv[u] <= j) last_user = false;
-                        if (last_user) tc05::commit2_elect(v_empty + (j % NS) * 8, kBoth);
-                        if (j == ntiles - 1) tc05::commit2_elect(tb + 48, kBoth);   // o_full
-                        ++pv[t];
-                        progress = true;
+                        issue_qk(t, jn);
                     }
-                    // QK of the next tile into S buffer j % SB, whose P the PV of
-                    // j - SB reads: that PV only has to be issued (the pair's MMAs
-                    // run in issue order)
-                    j = jq;
-                    if (j < ntiles && j <= pv[t] + SB - 1 && (ready & 4u)) {
-                        tc05::fence_after_sync();
-                        const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
-                        const uint32_t qst = q_smem + t * C::kQTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            tc05::mma2_ss_elect(
-                                tcol + (j % SB) * N,
-                                tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
-                                tc05::sw128_desc(kst + (kk >> 2) * C::kKPiece + (kk & 3) * 32, 16, 1024),
-                                idesc_qk, kk > 0 ? 1u : 0u);
-                        tc05::commit2_elect(tb + (j % SB) * 8, kBoth);   // s_full
-                        bool last_user = true;
-#pragma unroll
-                        for (int u = 0; u < NQ; ++u)
-                            if (u != t && u < nq && qk[u] <= j) last_user = false;
-                        if (last_user) tc05::commit2_elect(k_empty + (j % NS) * 8, kBoth);
-                        ++qk[t];
-                        progress = true;
-                    }
-                }
-                if (!busy) break;
-                if (progress) {
-                    idle = false;
-                } else if (!idle) {
-                    idle = true;
-                    idle_since = clock64();
-                } else if (__any_sync(kAll, clock64() - idle_since > 1000000000ll)) {
-                    ok = false;
                 }
             }
             if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);

@@ -13,7 +13,7 @@
 // One CTA = NQ Q tiles of 128 query rows of one (sequence, KV head): row =
 // chunk token x query head of the GQA group, so every row of the CTA uses
 // every K/V tile it loads, and with two Q tiles each loaded K/V byte feeds
-// 256 rows.  Warp roles (64 + 256 NQ threads):
+// 256 rows.  Warp roles (64 + 128 kSplit NQ threads):
 //   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
 //              x the CTA's chunk tokens), then K and V tiles of the context
 //              (128 tokens, 192 at head_dim 64) through NS shared-memory
@@ -22,23 +22,25 @@
 //              64-element piece) per copy, V one 16-row box with all its pieces
 //              per copy (a cache map with the row ahead of the piece).  Each
 //              CTA starts its walk at its own tile and wraps around;
-//   warp 1     tensor-memory owner and MMA issuer (one thread): for each Q
-//              tile, S_j = Q K_j^T into the tile's S buffer in tensor memory
-//              and O += P_j V_j with P read from tensor memory (the S buffer
-//              it was written over) and O accumulating in tensor memory; it
-//              polls its barriers and issues whichever MMA is ready, so the
-//              two tiles' MMAs fill the gaps of each other's softmax; a K
-//              (V) stage is released once every Q tile's QK (PV) has used it;
-//   warps 2..  two softmax warpgroups per Q tile, each taking half of the S
-//              columns of every row (a thread per row and half, on the row's
-//              tensor-memory lane): S -> causal mask -> scale -> the half's
-//              row max, swapped with the other half's through shared memory
-//              -> exp2 -> P (bf16 or f16) written back over the half's own S
-//              columns (at head_dim >= 128 on column pairs: three-input max,
-//              packed f32x2 fma and add); O is rescaled in tensor memory (each half its own O
-//              columns) only when a row's max grows by more than 2^8 (exponents
-//              stay below 2^8 in between and the final division by the running
-//              sum is exact either way); finally O / l -> out.
+//   warp 1     tensor-memory owner and MMA issuer: for each Q tile, S_j =
+//              Q K_j^T into the tile's S buffer in tensor memory and O += P_j
+//              V_j with P read from tensor memory (the S buffer it was written
+//              over) and O accumulating in tensor memory; the whole warp runs
+//              a fixed issue sequence (the two tiles take turns, so each tile's
+//              MMAs fill the gap of the other's softmax), each step waiting on
+//              the one barrier it needs, and one elected lane issues each MMA;
+//              a K (V) stage is released once every Q tile's QK (PV) has used it;
+//   warps 2..  kSplit softmax warpgroups per Q tile (one by default: a thread
+//              per row, on the row's tensor-memory lane; with two, each takes
+//              half of the S columns of every row and the halves swap their
+//              row maxima through shared memory): S -> causal mask -> scale ->
+//              row max -> exp2 -> P (bf16 or f16) written back over the first
+//              half of the thread's own S columns (on column pairs: three-input
+//              max, packed f32x2 fma and add; at head_dim 128 the row's S stays
+//              in registers between the max and the P pass); O is rescaled in
+//              tensor memory only when a row's max grows by more than 2^8
+//              (exponents stay below 2^8 in between and the final division by
+//              the running sum is exact either way); finally O / l -> out.
 // Every mbarrier wait is bounded; a role that gives up raises
 // PA_DEV_WAIT_TIMEOUT and leaves its loop, in-flight copies and MMAs are
 // waited for (bounded) and tensor memory is freed before the CTA exits.
@@ -49,15 +51,13 @@
 
 namespace pa {
 
-// Back-off of the MMA thread's polling loop when nothing is ready (0: spin).
-#ifndef PA_PREFILL_MMA_SLEEP_NS
-#define PA_PREFILL_MMA_SLEEP_NS 0
-#endif
-
 // Softmax warpgroups per Q tile: 2 = each row's S columns split between two
 // threads (which swap row maxima and sums), 1 = one thread per whole row.
+// One is faster at both head_dims (10 warps instead of 18: the MMA warp shares
+// its scheduler with two softmax warps instead of four, no max exchange, and
+// 168 registers a thread instead of 96).
 #ifndef PA_PREFILL_SPLIT_D64
-#define PA_PREFILL_SPLIT_D64 2
+#define PA_PREFILL_SPLIT_D64 1
 #endif
 #ifndef PA_PREFILL_SPLIT_D128
 #define PA_PREFILL_SPLIT_D128 1
@@ -67,12 +67,13 @@ namespace pa {
 #define PA_PREFILL_REGROW 1
 #endif
 
-// Tile plan per head_dim.  A tcgen05.mma with M = 128 and K = 16 costs about
-// 80 cycles whatever N <= 128 is (measured on GB300: N = 64 reaches 38 % of
-// the tensor peak, N = 128 80 %, N = 256 all of it), so the MMAs are kept
-// wide: 128-token K/V tiles, 192 at head_dim 64 (its O is only 64 columns, so
-// two Q tiles of S + O still fit 512 columns, and each MMA group does 1.5x the
-// work for the same issue overhead: 736 -> 825 TFLOP/s).  head_dim 64 / 128 run
+// Tile plan per head_dim.  A tcgen05.mma with M = 128 and K = 16 takes the
+// tensor pipe 65 cycles at N = 128, 129 at N = 256 and 49 at N = 64 (bound by
+// the 6 KB of shared-memory operands it reads: 0.65 of the peak rate), and
+// every MMA costs the issuing warp the same, so the MMAs are kept wide:
+// 128-token K/V tiles, 192 at head_dim 64 (its O is only 64 columns, so two Q
+// tiles of S + O still fit 512 columns, and each MMA group does 1.5x the work
+// for the same issue overhead: 736 -> 825 TFLOP/s when measured).  head_dim 64 / 128 run
 // two Q tiles per CTA, each with one S buffer in tensor memory (the two tiles
 // take turns on the tensor pipe).  head_dim 256 (its O alone takes 256
 // columns) runs on CTA pairs (pa_prefill_pair.cuh); the one-Q-tile layout with
@@ -561,99 +562,80 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
-        // The whole warp runs this loop, its control flow warp-uniform (barrier
-        // tests folded into one vote), and one elected lane issues each MMA and
-        // commit: a lone thread in a divergent branch issued an MMA every ~47
-        // cycles, slower than the pipe once the softmax warps share its scheduler.
+        // The whole warp runs the issue sequence, its control flow warp-uniform,
+        // and one elected lane issues each MMA and commit (a lone thread in a
+        // divergent branch issued an MMA every ~47 cycles, slower than the pipe
+        // once the softmax warps share its scheduler).  The sequence is fixed:
+        // QK of the first SB tiles for every Q tile, then per K/V tile j and Q
+        // tile t the PV of j and the QK of j + SB (the QK that overwrites an S
+        // buffer right behind the PV that reads its P: one thread's MMAs run on
+        // the tensor pipe in issue order, so the QK's writes come after the PV's
+        // operand reads).  Each step waits (suspending, bounded) on exactly the
+        // barrier it needs: a loop polling every tile's barriers saw a completed
+        // phase ~1000 cycles late, the pipe idle meanwhile.  Every barrier waited
+        // on depends only on MMAs issued earlier in the sequence, so the fixed
+        // order cannot deadlock.
         constexpr uint32_t kAll = 0xffffffffu;
         constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
         constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
         bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
-        int qk[NQ], pv[NQ];
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
+            return ok;
+        };
+        // S_j = Q_t K_j^T into S buffer j % SB; the last Q tile's QK frees the K stage
+        auto issue_qk = [&](int t, int j) {
+            const uint32_t tb = tile_bars + t * 56;
+            const uint32_t tcol = tmem + t * C::kTileCols;
+            const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
+            const uint32_t qst = q_smem + t * C::kQTileBytes;
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) qk[t] = pv[t] = 0;
-        bool idle = false;
-        long long idle_since = 0;
-        while (ok) {
-            bool busy = false, progress = false;
+            for (int kk = 0; kk < D / 16; ++kk)
+                tc05::mma_ss_elect(
+                    tcol + (j % SB) * N,
+                    tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
+                    tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16, 1024),
+                    idesc_qk, kk > 0 ? 1u : 0u);
+            tc05::commit_elect(tb + (j % SB) * 8);   // s_full
+            if (t == nq - 1) tc05::commit_elect(k_empty + (j % NS) * 8);
+        };
+        // O_t += P_j V_j; the last Q tile's PV frees the V stage
+        auto issue_pv = [&](int t, int j) {
+            const uint32_t tb = tile_bars + t * 56;
+            const uint32_t tcol = tmem + t * C::kTileCols;
+            const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) {
-                if (t >= nq) break;
-                busy |= pv[t] < ntiles;
-                const uint32_t tb = tile_bars + t * 56;
-                const uint32_t tcol = tmem + t * C::kTileCols;
-                // The tile's three barrier tests go out together, so their
-                // shared-memory latencies overlap, and one vote makes the result
-                // uniform over the warp.  A test of an index past the loop's end
-                // is ignored.
-                const int jp = pv[t], jq = qk[t];
-                const uint32_t ready = __reduce_and_sync(
-                    kAll, (mbar_test(tb + 16 + (jp % SB) * 8, (jp / SB) & 1u) ? 1u : 0u) |
-                              (mbar_test(v_full + (jp % NS) * 8, (jp / NS) & 1u) ? 2u : 0u) |
-                              (mbar_test(k_full + (jq % NS) * 8, (jq / NS) & 1u) ? 4u : 0u));
-                // PV of the oldest tile whose P is ready
-                int j = jp;
-                if (j < jq && (ready & 3u) == 3u) {
+            for (int kt = 0; kt < N / 16; ++kt)
+                // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
+                // whose P occupies the first half of its own S columns
+                tc05::mma_ts_elect(tcol + C::kOCol,
+                                   tcol + (j % SB) * N +
+                                       ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
+                                   tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024), idesc_pv,
+                                   (j > 0 || kt > 0) ? 1u : 0u);
+            // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
+            // tracks this PV as well, so none is needed
+            if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
+            if (t == nq - 1) tc05::commit_elect(v_empty + (j % NS) * 8);
+            if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
+        };
+        for (int j = 0; ok && j < SB && j < ntiles; ++j) {
+            if (!wait(k_full + (j % NS) * 8, (j / NS) & 1u)) break;
+            tc05::fence_after_sync();
+            for (int t = 0; t < nq; ++t) issue_qk(t, j);
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            if (!wait(v_full + (j % NS) * 8, (j / NS) & 1u)) break;
+            const int jn = j + SB;   // the QK issued behind this tile's PV
+            for (int t = 0; t < nq; ++t) {
+                if (!wait(tile_bars + t * 56 + 16 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
+                tc05::fence_after_sync();
+                issue_pv(t, j);
+                if (jn < ntiles) {
+                    if (t == 0 && !wait(k_full + (jn % NS) * 8, (jn / NS) & 1u)) break;
                     tc05::fence_after_sync();
-                    const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
-#pragma unroll
-                    for (int kt = 0; kt < N / 16; ++kt)
-                        // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
-                        // whose P occupies the first half of its own S columns
-                        tc05::mma_ts_elect(tcol + C::kOCol,
-                                           tcol + (j % SB) * N +
-                                               ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) +
-                                               kt * 8,
-                                           tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024),
-                                           idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
-                    // s_free: with one S buffer the commit of the QK issued next
-                    // (S_{j+1}) tracks this PV as well, so none is needed
-                    if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
-                    bool last_user = true;   // the V stage is free once every tile used it
-#pragma unroll
-                    for (int u = 0; u < NQ; ++u)
-                        if (u != t && u < nq && pv[u] <= j) last_user = false;
-                    if (last_user) tc05::commit_elect(v_empty + (j % NS) * 8);
-                    if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
-                    ++pv[t];
-                    progress = true;
+                    issue_qk(t, jn);
                 }
-                // QK of the next tile into S buffer j % SB, whose P the PV of
-                // j - SB reads: that PV only has to be issued, not finished,
-                // since one thread's MMAs run on the tensor pipe in issue order
-                // (the QK's writes come after the PV's operand reads)
-                j = jq;
-                if (j < ntiles && j <= pv[t] + SB - 1 && (ready & 4u)) {
-                    tc05::fence_after_sync();
-                    const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
-                    const uint32_t qst = q_smem + t * C::kQTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        tc05::mma_ss_elect(
-                            tcol + (j % SB) * N,
-                            tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
-                            tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16, 1024),
-                            idesc_qk, kk > 0 ? 1u : 0u);
-                    tc05::commit_elect(tb + (j % SB) * 8);   // s_full
-                    bool last_user = true;
-#pragma unroll
-                    for (int u = 0; u < NQ; ++u)
-                        if (u != t && u < nq && qk[u] <= j) last_user = false;
-                    if (last_user) tc05::commit_elect(k_empty + (j % NS) * 8);
-                    ++qk[t];
-                    progress = true;
-                }
-            }
-            if (!busy) break;
-            if (progress) {
-                idle = false;
-            } else if (!idle) {
-                idle = true;
-                idle_since = clock64();
-            } else if (__any_sync(kAll, clock64() - idle_since > 1000000000ll)) {
-                ok = false;
-            } else if (PA_PREFILL_MMA_SLEEP_NS > 0) {
-                __nanosleep(PA_PREFILL_MMA_SLEEP_NS);
             }
         }
         if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
