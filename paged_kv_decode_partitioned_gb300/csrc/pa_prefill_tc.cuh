@@ -13,15 +13,17 @@
 // One CTA = NQ Q tiles of 128 query rows of one (sequence, KV head): row =
 // chunk token x query head of the GQA group, so every row of the CTA uses
 // every K/V tile it loads, and with two Q tiles each loaded K/V byte feeds
-// 256 rows.  Warp roles (64 + 128 kSplit NQ threads):
-//   warp 0     TMA producer: Q once (a 4-D map whose box is the group's heads
-//              x the CTA's chunk tokens), then K and V tiles of the context
-//              (128 tokens, 192 at head_dim 64) through NS shared-memory
-//              stages; each lane looks up the block of one copy and issues it,
-//              so a tile's copies go out in parallel: K one (16-row box,
-//              64-element piece) per copy, V one 16-row box with all its pieces
-//              per copy (a cache map with the row ahead of the piece).  Each
-//              CTA starts its walk at its own tile and wraps around;
+// 256 rows.  Warp roles (96 + 128 kSplit NQ threads):
+//   warp 0     TMA producer of Q (once: a 4-D map whose box is the group's
+//              heads x the CTA's chunk tokens) and of the K tiles of the
+//              context (128 tokens, 192 at head_dim 64) through NK shared-
+//              memory stages, one (16-row box, 64-element piece) per copy; the
+//              last warp is the V producer, through its own NV stages, one
+//              16-row box with all its pieces per copy (a cache map with the
+//              row ahead of the piece), and zeroes the tail tile's rows past
+//              the context.  Each lane looks up the block of one copy and
+//              issues it, so a tile's copies go out in parallel.  Each CTA
+//              starts its walk at its own tile and wraps around;
 //   warp 1     tensor-memory owner and MMA issuer: for each Q tile, S_j =
 //              Q K_j^T into the tile's S buffer in tensor memory and O += P_j
 //              V_j with P read from tensor memory (the S buffer it was written
@@ -84,7 +86,11 @@ struct PrefillTcCfg {
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
     static constexpr int kN = D <= 64 ? 192 : 128;                // cache tokens per tile
     static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
-    static constexpr int kStages = D <= 64 ? 3 : (D <= 128 ? 2 : 1);
+    // K and V stages: K gets more, since the QK that reads K(j) comes a whole
+    // softmax before the PV that reads V(j), and one tile's K copies (2 KB
+    // each) take ~2300 cycles to land through the SM's TMA unit
+    static constexpr int kKStages = D <= 64 ? 4 : (D <= 128 ? 3 : 1);
+    static constexpr int kVStages = D <= 64 ? 3 : (D <= 128 ? 2 : 1);
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
     static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
@@ -95,13 +101,14 @@ struct PrefillTcCfg {
     // V one 16-token box at a time with all its pieces ([box][piece][16 rows]
     // [128 B], the MN-major operand), one copy per box
     static constexpr int kVBox = kPieces * 2048;
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
-    // barriers: q_full, vtail, mma_done, k_full[NS], v_full[NS], k_empty[NS],
-    // v_empty[NS]; per Q tile s_full[2], p_full[2], s_free[2], o_full (the
+    static constexpr int kKOffset = kQBytes;                          // K stages
+    static constexpr int kVOffset = kKOffset + kKStages * kTileBytes;   // V stages
+    static constexpr int kBarOffset = kVOffset + kVStages * kTileBytes;
+    // barriers: q_full, vtail, mma_done, k_full[NK], k_empty[NK], v_full[NV],
+    // v_empty[NV]; per Q tile s_full[2], p_full[2], s_free[2], o_full (the
     // first kSBufs of each pair in use); then the tensor-memory slot
     static constexpr int kTileBars = 7;
-    static constexpr int kNumBars = 3 + 4 * kStages + kTileBars * kQTiles;
+    static constexpr int kNumBars = 3 + 2 * kKStages + 2 * kVStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
     // each Q tile's softmax runs in kSplit warpgroups, one per 1 / kSplit of
     // the S columns of every row; with two, they swap row maxima (two buffers
@@ -113,9 +120,11 @@ struct PrefillTcCfg {
     static constexpr int kHalfCols = kN / kSplit;
     static constexpr int kXBarOffset = kSlotOffset + 16;
     static constexpr int kXOffset = kXBarOffset + kQTiles * 3 * 8 + 8;
-    static constexpr int kXBytes = kQTiles * 3 * 2 * 128 * 4;   // [tile][max0, max1, sum][half][row]
+    static constexpr int kXBytes = kSplit > 1 ? kQTiles * 3 * 2 * 128 * 4 : 0;   // [tile][max0, max1, sum][half][row]
     static constexpr int kLaunchBytes = kXOffset + kXBytes + 1024;
-    static constexpr int kThreads = 64 + 128 * kSplit * kQTiles;
+    // warp 0 Q and K producer, warp 1 MMA, then the softmax warps, then the V producer
+    static constexpr int kVWarp = 2 + 4 * kSplit * kQTiles;
+    static constexpr int kThreads = 32 * (kVWarp + 1);
     // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
     static constexpr int kOCol = kSBufs * kN;
     static constexpr int kTileCols = kSBufs * kN + D;
@@ -359,18 +368,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     using C = PrefillTcCfg<D>;
-    constexpr int N = C::kN, NS = C::kStages, NQ = C::kQTiles, SB = C::kSBufs;
+    constexpr int N = C::kN, NK = C::kKStages, NV = C::kVStages, NQ = C::kQTiles, SB = C::kSBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t base = smem_u32(smem);
     const uint32_t q_smem = base;
-    const uint32_t stage0 = base + C::kQBytes;
+    const uint32_t kstage0 = base + C::kKOffset, vstage0 = base + C::kVOffset;
     const uint32_t bars = base + C::kBarOffset;
     const uint32_t q_full = bars, vtail = bars + 8, mma_done = bars + 16;
-    const uint32_t k_full = bars + 24, v_full = k_full + NS * 8;
-    const uint32_t k_empty = v_full + NS * 8, v_empty = k_empty + NS * 8;
-    const uint32_t tile_bars = v_empty + NS * 8;   // + t * 56: s_full, p_full, s_free, o_full
+    const uint32_t k_full = bars + 24, k_empty = k_full + NK * 8;
+    const uint32_t v_full = k_empty + NK * 8, v_empty = v_full + NV * 8;
+    const uint32_t tile_bars = v_empty + NV * 8;   // + t * 56: s_full, p_full, s_free, o_full
     const uint32_t slot = base + C::kSlotOffset;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -412,10 +421,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(vtail, 1);
         mbar_init(mma_done, 1);
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NK; ++i) {
             mbar_init(k_full + i * 8, 1);
-            mbar_init(v_full + i * 8, 1);
             mbar_init(k_empty + i * 8, 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(v_full + i * 8, 1);
             mbar_init(v_empty + i * 8, 1);
         }
         for (int t = 0; t < NQ; ++t) {
@@ -437,16 +448,16 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     tc05::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kSlotOffset);
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
+    if (warp == 0 || warp == C::kVWarp) {
+        // ------------------------------ producers ------------------------------
+        // warp 0 loads Q and the K tiles, the last warp the V tiles, each
+        // through its own stages, so a K copy never waits behind a V stage
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kBoxes = N / kTile;   // 16-token boxes per tile
-        constexpr int kOps = kBoxes * C::kPieces;   // copies per K (or V) tile
+        constexpr int kOps = kBoxes * C::kPieces;   // copies per K tile
         static_assert(kOps <= 32, "one copy per lane");
-        const int op_box = (lane % kOps) / C::kPieces, op_piece = (lane % kOps) % C::kPieces;
-        const int v_box = lane % kBoxes;   // V: one copy per box moves all its pieces
-        // block of this lane's K (V) box of tile jt (0 when the lane has no copy).
+        // block of this lane's box of tile jt (0 when the lane has no copy).
         // The read goes out a tile ahead and is checked only when the copy is
         // issued, so its latency overlaps the stage waits in between (with one
         // stage, a read consumed at once put ~3000 cycles on every tile's K load).
@@ -459,107 +470,122 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
                 atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
         };
-        // Q rows the box does not cover (kRows % group) are never loaded: zero
-        // them so those rows stay finite (and never force an O rescale).
-        const int qrows = g * p.tokens_per_cta;
-        if (qrows < C::kRows) {
-            for (int c = 0; c < C::kPieces; ++c)
-                for (int e = lane; e < (C::kRows - qrows) * 8; e += 32)
-                    *reinterpret_cast<uint4 *>(smem + c * C::kQPiece + qrows * 128 + e * 16) =
-                        make_uint4(0, 0, 0, 0);
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-        if (lane == 0) {
-            mbar_expect_tx(q_full, static_cast<uint32_t>(C::kPieces * 128 * qrows));
-#pragma unroll
-            for (int c = 0; c < C::kPieces; ++c)
-                tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
-        }
-        const bool k_has = lane < kOps, v_has = lane < kBoxes;
-        int jt_next = rot, phys_next = box_block(rot, op_box, k_has), vphys_next = box_block(rot, v_box, v_has);
-        int issued = 0;
-        bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
-            const int st = j % NS;
-            const int jt = jt_next, op_phys = phys_next, v_phys = vphys_next;
-            jt_next = jt + 1 == ntiles ? 0 : jt + 1;
-            if (j + 1 < ntiles) {   // next tile's table entries
-                phys_next = box_block(jt_next, op_box, k_has);
-                vphys_next = box_block(jt_next, v_box, v_has);
-            }
-            const uint32_t kdst = stage0 + st * C::kStageBytes, vdst = kdst + C::kTileBytes;
-            const bool last = jt == ntiles - 1;   // the context's tail tile
-            const uint32_t vbar = last ? vtail : v_full + st * 8;
+        // bytes of tile jt's boxes inside the context (K or V: the same)
+        auto tile_bytes = [&](int jt) {
             int boxes = 0;
 #pragma unroll
             for (int k = 0; k < kBoxes; ++k) boxes += jt * kBoxes + k < nbox;
-            const uint32_t bytes = static_cast<uint32_t>(boxes * C::kPieces * 2048);
-            // K of tile j once every QK of tile j - NS is done, V once every PV is
-            if (j >= NS) {
-                const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NS) - 1) & 1u);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    break;
-                }
-            }
-            check_block(op_phys);
-            // one copy per lane: a single thread issuing them back to back is
-            // bound by the issue latency of each copy, not by the TMA engine
-            if (lane == 0) mbar_expect_tx(k_full + st * 8, bytes);
-            __syncwarp();
-            if (k_has && jt * kBoxes + op_box < nbox)
-                tma_load_5d(kdst + op_piece * C::kKvPiece + op_box * 2048, &tmK, k_full + st * 8,
-                            0, op_piece, kvh, ((jt * kBoxes + op_box) * kTile) % p.block_size,
-                            op_phys);
-            if (j >= NS) {
-                const bool w = mbar_wait_cycles(v_empty + st * 8, ((j / NS) - 1) & 1u);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    issued = j;   // K of tile j is in flight: wait for it below
-                    (void)mbar_wait_cycles(k_full + st * 8, (j / NS) & 1u);
-                    break;
-                }
-            }
-            check_block(v_phys);
-            if (lane == 0) mbar_expect_tx(vbar, bytes);
-            __syncwarp();
-            // the V map has the row ahead of the piece: (element, row, piece, head, block)
-            if (v_has && jt * kBoxes + v_box < nbox)
-                tma_load_5d(vdst + v_box * C::kVBox, &tmV, vbar, 0,
-                            ((jt * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, v_phys);
-            issued = j + 1;
-            if (last) {
-                // V rows at or past kv_end hold cache data past the context (or
-                // nothing): zero them before the MMA reads V, since 0 * NaN != 0.
-                const bool w = mbar_wait_cycles(vtail, 0);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    break;
-                }
-                const int first_row = kv_end - jt * N;
-                const int nchunks = (N - first_row) * C::kPieces * 8;   // 16-byte chunks
-                for (int e = lane; e < nchunks; e += 32) {
-                    const int r = first_row + e / (C::kPieces * 8);
-                    const int c = (e / 8) % C::kPieces;
-                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox +
-                                               c * 2048 + (r & 15) * 128 + (e & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
+            return static_cast<uint32_t>(boxes * C::kPieces * 2048);
+        };
+        bool ok = true;
+        if (warp == 0) {
+            // Q rows the box does not cover (kRows % group) are never loaded: zero
+            // them so those rows stay finite (and never force an O rescale).
+            const int qrows = g * p.tokens_per_cta;
+            if (qrows < C::kRows) {
+                for (int c = 0; c < C::kPieces; ++c)
+                    for (int e = lane; e < (C::kRows - qrows) * 8; e += 32)
+                        *reinterpret_cast<uint4 *>(smem + c * C::kQPiece + qrows * 128 + e * 16) =
+                            make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cta(v_full + st * 8);
             }
+            if (lane == 0) {
+                mbar_expect_tx(q_full, static_cast<uint32_t>(C::kPieces * 128 * qrows));
+#pragma unroll
+                for (int c = 0; c < C::kPieces; ++c)
+                    tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
+            }
+            // K: one copy per (16-row box, 64-element piece) and lane
+            const int op_box = (lane % kOps) / C::kPieces, op_piece = (lane % kOps) % C::kPieces;
+            const bool has = lane < kOps;
+            int jt = rot, phys_next = box_block(rot, op_box, has), issued = 0;
+            for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
+                const int st = j % NK, phys = phys_next, jc = jt;
+                jt = jt + 1 == ntiles ? 0 : jt + 1;
+                if (j + 1 < ntiles) phys_next = box_block(jt, op_box, has);   // next tile's entry
+                // K of tile j once every QK of tile j - NK is done
+                if (j >= NK) {
+                    const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NK) - 1) & 1u);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                check_block(phys);
+                // one copy per lane: a single thread issuing them back to back is
+                // bound by the issue latency of each copy, not by the TMA engine
+                if (lane == 0) mbar_expect_tx(k_full + st * 8, tile_bytes(jc));
+                __syncwarp();
+                if (has && jc * kBoxes + op_box < nbox)
+                    tma_load_5d(kstage0 + st * C::kTileBytes + op_piece * C::kKvPiece + op_box * 2048,
+                                &tmK, k_full + st * 8, 0, op_piece, kvh,
+                                ((jc * kBoxes + op_box) * kTile) % p.block_size, phys);
+                issued = j + 1;
+            }
+            if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
+            // copies still landing must land before the CTA exits (at most NK
+            // tiles' K are in flight: each waited for the QK of the one NK before)
+            (void)mbar_wait_cycles(q_full, 0);
+            for (int j = issued > NK ? issued - NK : 0; j < issued; ++j)
+                (void)mbar_wait_cycles(k_full + (j % NK) * 8, (j / NK) & 1u);
+        } else {
+            // V: one copy per 16-row box moves all its pieces
+            const int v_box = lane % kBoxes;
+            const bool has = lane < kBoxes;
+            int jt = rot, phys_next = box_block(rot, v_box, has), issued = 0;
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % NV, phys = phys_next, jc = jt;
+                jt = jt + 1 == ntiles ? 0 : jt + 1;
+                if (j + 1 < ntiles) phys_next = box_block(jt, v_box, has);
+                const uint32_t vdst = vstage0 + st * C::kTileBytes;
+                const bool last = jc == ntiles - 1;   // the context's tail tile
+                const uint32_t vbar = last ? vtail : v_full + st * 8;
+                // V of tile j once every PV of tile j - NV is done
+                if (j >= NV) {
+                    const bool w = mbar_wait_cycles(v_empty + st * 8, ((j / NV) - 1) & 1u);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                check_block(phys);
+                if (lane == 0) mbar_expect_tx(vbar, tile_bytes(jc));
+                __syncwarp();
+                // the V map has the row ahead of the piece: (element, row, piece, head, block)
+                if (has && jc * kBoxes + v_box < nbox)
+                    tma_load_5d(vdst + v_box * C::kVBox, &tmV, vbar, 0,
+                                ((jc * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, phys);
+                issued = j + 1;
+                if (last) {
+                    // V rows at or past kv_end hold cache data past the context (or
+                    // nothing): zero them before the MMA reads V, since 0 * NaN != 0.
+                    const bool w = mbar_wait_cycles(vtail, 0);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    const int first_row = kv_end - jc * N;
+                    const int nchunks = (N - first_row) * C::kPieces * 8;   // 16-byte chunks
+                    for (int e = lane; e < nchunks; e += 32) {
+                        const int r = first_row + e / (C::kPieces * 8);
+                        const int c = (e / 8) % C::kPieces;
+                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox +
+                                                   c * 2048 + (r & 15) * 128 + (e & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(v_full + st * 8);
+                }
+            }
+            if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
+            // copies still landing must land before the CTA exits
+            const int j_tail = ntiles - 1 - rot;   // use order of the tail tile
+            for (int j = issued > NV ? issued - NV : 0; j < issued; ++j)
+                if (j != j_tail) (void)mbar_wait_cycles(v_full + (j % NV) * 8, (j / NV) & 1u);
+            if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
         }
-        if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
-        // copies still landing must land before the CTA exits
-        (void)mbar_wait_cycles(q_full, 0);
-        const int j_tail = ntiles - 1 - rot;   // use order of the tail tile
-        for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
-            (void)mbar_wait_cycles(k_full + (j % NS) * 8, (j / NS) & 1u);
-            if (j != j_tail) (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
-        }
-        if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         // The whole warp runs the issue sequence, its control flow warp-uniform,
@@ -587,7 +613,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         auto issue_qk = [&](int t, int j) {
             const uint32_t tb = tile_bars + t * 56;
             const uint32_t tcol = tmem + t * C::kTileCols;
-            const uint32_t kst = stage0 + (j % NS) * C::kStageBytes;
+            const uint32_t kst = kstage0 + (j % NK) * C::kTileBytes;
             const uint32_t qst = q_smem + t * C::kQTileBytes;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -597,13 +623,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16, 1024),
                     idesc_qk, kk > 0 ? 1u : 0u);
             tc05::commit_elect(tb + (j % SB) * 8);   // s_full
-            if (t == nq - 1) tc05::commit_elect(k_empty + (j % NS) * 8);
+            if (t == nq - 1) tc05::commit_elect(k_empty + (j % NK) * 8);
         };
         // O_t += P_j V_j; the last Q tile's PV frees the V stage
         auto issue_pv = [&](int t, int j) {
             const uint32_t tb = tile_bars + t * 56;
             const uint32_t tcol = tmem + t * C::kTileCols;
-            const uint32_t vst = stage0 + (j % NS) * C::kStageBytes + C::kTileBytes;
+            const uint32_t vst = vstage0 + (j % NV) * C::kTileBytes;
 #pragma unroll
             for (int kt = 0; kt < N / 16; ++kt)
                 // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
@@ -616,23 +642,23 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
             // tracks this PV as well, so none is needed
             if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
-            if (t == nq - 1) tc05::commit_elect(v_empty + (j % NS) * 8);
+            if (t == nq - 1) tc05::commit_elect(v_empty + (j % NV) * 8);
             if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
         };
         for (int j = 0; ok && j < SB && j < ntiles; ++j) {
-            if (!wait(k_full + (j % NS) * 8, (j / NS) & 1u)) break;
+            if (!wait(k_full + (j % NK) * 8, (j / NK) & 1u)) break;
             tc05::fence_after_sync();
             for (int t = 0; t < nq; ++t) issue_qk(t, j);
         }
         for (int j = 0; ok && j < ntiles; ++j) {
-            if (!wait(v_full + (j % NS) * 8, (j / NS) & 1u)) break;
+            if (!wait(v_full + (j % NV) * 8, (j / NV) & 1u)) break;
             const int jn = j + SB;   // the QK issued behind this tile's PV
             for (int t = 0; t < nq; ++t) {
                 if (!wait(tile_bars + t * 56 + 16 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
                 tc05::fence_after_sync();
                 issue_pv(t, j);
                 if (jn < ntiles) {
-                    if (t == 0 && !wait(k_full + (jn % NS) * 8, (jn / NS) & 1u)) break;
+                    if (t == 0 && !wait(k_full + (jn % NK) * 8, (jn / NK) & 1u)) break;
                     tc05::fence_after_sync();
                     issue_qk(t, jn);
                 }
