@@ -21,15 +21,16 @@
 // buffers in tensor memory, so the QK of the next tile runs under the
 // softmax of the current one.
 //
-// Warp roles (320 threads per CTA):
-//   warp 0     TMA producer of this CTA: its Q rows once, then its halves of
-//              the K and V tiles through NS stages (one copy per lane).  The
-//              copies of both CTAs complete on the even CTA's barriers (the
-//              cta_group::2 form of the copy), which the even CTA arms with
-//              both halves' bytes, so the MMA thread sees a whole tile land
-//              without a message from the odd CTA;
-//   warp 1     tensor-memory owner; in the even CTA, lane 0 issues every MMA
-//              of the pair and commits each group to both CTAs' barriers;
+// Warp roles (352 threads per CTA):
+//   warp 0     TMA producer of this CTA's Q rows (once) and K halves, the last
+//              warp of its V halves, each through NS stages (one copy per
+//              lane).  The copies of both CTAs complete on the even CTA's
+//              barriers (the cta_group::2 form of the copy), which the even CTA
+//              arms with both halves' bytes, so the MMA warp sees a whole tile
+//              land without a message from the odd CTA;
+//   warp 1     tensor-memory owner; in the even CTA it runs the pair's fixed
+//              MMA sequence, one elected lane issuing each MMA and committing
+//              it to both CTAs' barriers;
 //   warps 2..  softmax, as in the single-CTA kernel: two warpgroups, each
 //              half of the S columns of every row, P written over S in this
 //              CTA's tensor memory and reported to the even CTA; O rescaled in
@@ -89,7 +90,9 @@ struct PrefillPairCfg {
     static constexpr int kXBytes = kQTiles * 3 * 2 * 128 * 4;   // [tile][max0, max1, sum][half][row]
     static constexpr int kLaunchBytes = kXOffset + kXBytes + 1024;
     static constexpr int kSoftmaxWarp0 = 2;
-    static constexpr int kThreads = 32 * kSoftmaxWarp0 + 256 * kQTiles;
+    // warp 0 Q and K producer, warp 1 MMA, the softmax warps, then the V producer
+    static constexpr int kVWarp = kSoftmaxWarp0 + 8 * kQTiles;
+    static constexpr int kThreads = 32 * (kVWarp + 1);
     // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
     static constexpr int kOCol = kSBufs * kN;
     static constexpr int kTileCols = kSBufs * kN + D;
@@ -231,8 +234,11 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
     tc05::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::kSlotOffset);
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
+    if (warp == 0 || warp == C::kVWarp) {
+        // ------------------------------ producers ------------------------------
+        // warp 0 loads this CTA's Q rows and K halves, the last warp its V halves,
+        // so a K copy never waits behind a V stage (one producer for both cost
+        // ~9 % at head_dim 128 on single CTAs)
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kKOps = 4 * C::kPieces;    // this CTA's 4 boxes of K x pieces
@@ -255,32 +261,34 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
         };
         // the even CTA's barrier at the same offset (this CTA's own in the even CTA)
         auto lead_bar = [&](uint32_t bar) -> uint32_t { return lead ? bar : dsmem_addr(bar, 0); };
-        // Q: the box covers g * tpc rows; rows past it (and every row of a CTA
-        // without chunk tokens) are zeroed so they stay finite
-        const int qrows = ntok > 0 ? g * tpc : 0;
-        if (qrows < C::kRows) {
-            for (int c = 0; c < C::kPieces; ++c)
-                for (int e = lane; e < (C::kRows - qrows) * 8; e += 32)
-                    *reinterpret_cast<uint4 *>(smem + c * C::kQPiece + qrows * 128 + e * 16) =
-                        make_uint4(0, 0, 0, 0);
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-        if (lane == 0) {
-            if (lead) {   // arm q_full with both CTAs' Q bytes
-                const int ntok1 = max(0, min(tpc, n - (2 * qp + 1) * tpc));
-                const int qrows1 = ntok1 > 0 ? g * tpc : 0;
-                mbar_expect_tx(q_full, static_cast<uint32_t>(C::kPieces * 128 * (qrows + qrows1)));
-            }
-            if (qrows > 0) {
-#pragma unroll
-                for (int c = 0; c < C::kPieces; ++c)
-                    tma_load_4d_pair(q_smem + c * C::kQPiece, &tmQ, lead_bar(q_full), 0, c, kvh * g,
-                                     row0 + tok0);
-            }
-            if (!lead) mbar_arrive_cluster(lead_bar(q_full));   // zeroed rows published
-        }
         const bool k_has = lane < kKOps, v_has = lane < kVOps;
+        if (warp == 0) {
+            // Q: the box covers g * tpc rows; rows past it (and every row of a CTA
+            // without chunk tokens) are zeroed so they stay finite
+            const int qrows = ntok > 0 ? g * tpc : 0;
+            if (qrows < C::kRows) {
+                for (int c = 0; c < C::kPieces; ++c)
+                    for (int e = lane; e < (C::kRows - qrows) * 8; e += 32)
+                        *reinterpret_cast<uint4 *>(smem + c * C::kQPiece + qrows * 128 + e * 16) =
+                            make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                if (lead) {   // arm q_full with both CTAs' Q bytes
+                    const int ntok1 = max(0, min(tpc, n - (2 * qp + 1) * tpc));
+                    const int qrows1 = ntok1 > 0 ? g * tpc : 0;
+                    mbar_expect_tx(q_full, static_cast<uint32_t>(C::kPieces * 128 * (qrows + qrows1)));
+                }
+                if (qrows > 0) {
+#pragma unroll
+                    for (int c = 0; c < C::kPieces; ++c)
+                        tma_load_4d_pair(q_smem + c * C::kQPiece, &tmQ, lead_bar(q_full), 0, c, kvh * g,
+                                         row0 + tok0);
+                }
+                if (!lead) mbar_arrive_cluster(lead_bar(q_full));   // zeroed rows published
+            }
+        }
         auto tile_at = [&](int j) -> int { return j + rot < ntiles ? j + rot : j + rot - ntiles; };
         // 16-token boxes of context tile jt inside the context
         auto boxes_of = [&](int jt) -> int {
@@ -361,21 +369,25 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             }
             return true;
         };
-        for (int j = 0; ok && j < ntiles; ++j) {
-            ok = issue_k(j);
-            if (ok) ok = issue_v(j);
+        if (warp == 0) {
+            for (int j = 0; ok && j < ntiles; ++j) ok = issue_k(j);
+        } else {
+            for (int j = 0; ok && j < ntiles; ++j) ok = issue_v(j);
         }
         if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
         // copies still landing must land before the CTA exits: the even CTA's
         // barriers count both CTAs' bytes, so the even CTA waits for the pair
-        if (lead) {
+        if (warp == 0 && lead) {
             (void)mbar_wait_cycles(q_full, 0);
             for (int j = k_issued > NS ? k_issued - NS : 0; j < k_issued; ++j)
                 (void)mbar_wait_cycles(k_full + (j % NS) * 8, (j / NS) & 1u);
-            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
-                if (j != j_tail) (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
         }
-        if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
+        if (warp != 0) {
+            if (lead)
+                for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
+                    if (j != j_tail) (void)mbar_wait_cycles(v_full + (j % NS) * 8, (j / NS) & 1u);
+            if (issued > j_tail) (void)mbar_wait_cycles(vtail, 0);
+        }
     } else if (warp == 1) {
         // ------------------------- MMA issuer (even CTA) -------------------------
         // The whole warp runs a fixed issue sequence (warp-uniform control flow)

@@ -64,6 +64,19 @@ namespace pa {
 #ifndef PA_PREFILL_SPLIT_D128
 #define PA_PREFILL_SPLIT_D128 1
 #endif
+// Shared-memory stages of K and of V tiles per head_dim.
+#ifndef PA_PREFILL_KSTAGES_D64
+#define PA_PREFILL_KSTAGES_D64 3
+#endif
+#ifndef PA_PREFILL_VSTAGES_D64
+#define PA_PREFILL_VSTAGES_D64 3
+#endif
+#ifndef PA_PREFILL_KSTAGES_D128
+#define PA_PREFILL_KSTAGES_D128 2
+#endif
+#ifndef PA_PREFILL_VSTAGES_D128
+#define PA_PREFILL_VSTAGES_D128 2
+#endif
 // Whole rows of head_dim >= 128 hold their S in registers between the passes.
 #ifndef PA_PREFILL_REGROW
 #define PA_PREFILL_REGROW 1
@@ -86,11 +99,10 @@ struct PrefillTcCfg {
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
     static constexpr int kN = D <= 64 ? 192 : 128;                // cache tokens per tile
     static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
-    // K and V stages: K gets more, since the QK that reads K(j) comes a whole
-    // softmax before the PV that reads V(j), and one tile's K copies (2 KB
-    // each) take ~2300 cycles to land through the SM's TMA unit
-    static constexpr int kKStages = D <= 64 ? 4 : (D <= 128 ? 3 : 1);
-    static constexpr int kVStages = D <= 64 ? 3 : (D <= 128 ? 2 : 1);
+    // K and V stages (their own producers and barriers; a third K stage at
+    // head_dim 128 or a fourth at head_dim 64 measured no faster)
+    static constexpr int kKStages = D <= 64 ? PA_PREFILL_KSTAGES_D64 : (D <= 128 ? PA_PREFILL_KSTAGES_D128 : 1);
+    static constexpr int kVStages = D <= 64 ? PA_PREFILL_VSTAGES_D64 : (D <= 128 ? PA_PREFILL_VSTAGES_D128 : 1);
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
     static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
