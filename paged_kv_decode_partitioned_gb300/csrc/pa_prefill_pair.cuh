@@ -542,8 +542,8 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     }
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
-                l += full ? tile_row_p<T, HC, false, true>(sb, lim, sl2, mu)
-                          : tile_row_p<T, HC, true, true>(sb, lim, sl2, mu);
+                l += full ? tile_row_p<T, HC, false, true>(sb, lim, sl2, mu, 0u, false)
+                          : tile_row_p<T, HC, true, true>(sb, lim, sl2, mu, 0u, false);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();

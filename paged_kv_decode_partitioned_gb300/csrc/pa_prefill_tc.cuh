@@ -77,7 +77,18 @@ namespace pa {
 #ifndef PA_PREFILL_VSTAGES_D128
 #define PA_PREFILL_VSTAGES_D128 2
 #endif
-// Whole rows of head_dim >= 128 hold their S in registers between the passes.
+// P handed to the MMA warp in two halves, per head_dim.
+#ifndef PA_PREFILL_HALFP_D64
+#define PA_PREFILL_HALFP_D64 1
+#endif
+#ifndef PA_PREFILL_HALFP_D128
+#define PA_PREFILL_HALFP_D128 0
+#endif
+// K/V tile width at head_dim 64 (128 at head_dim 128).
+#ifndef PA_PREFILL_N_D64
+#define PA_PREFILL_N_D64 192
+#endif
+// Whole rows of at most 128 columns hold their S in registers between the passes.
 #ifndef PA_PREFILL_REGROW
 #define PA_PREFILL_REGROW 1
 #endif
@@ -97,7 +108,7 @@ template <int D>
 struct PrefillTcCfg {
     static constexpr int kQTiles = D <= 128 ? 2 : 1;
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
-    static constexpr int kN = D <= 64 ? 192 : 128;                // cache tokens per tile
+    static constexpr int kN = D <= 64 ? PA_PREFILL_N_D64 : 128;   // cache tokens per tile
     static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
     // K and V stages (their own producers and barriers; a third K stage at
     // head_dim 128 or a fourth at head_dim 64 measured no faster)
@@ -118,8 +129,9 @@ struct PrefillTcCfg {
     static constexpr int kBarOffset = kVOffset + kVStages * kTileBytes;
     // barriers: q_full, vtail, mma_done, k_full[NK], k_empty[NK], v_full[NV],
     // v_empty[NV]; per Q tile s_full[2], p_full[2], s_free[2], o_full (the
-    // first kSBufs of each pair in use); then the tensor-memory slot
-    static constexpr int kTileBars = 7;
+    // first kSBufs of each pair in use), p_half; then the tensor-memory slot
+    static constexpr int kTileBars = 8;
+    static constexpr int kTileBarBytes = kTileBars * 8;
     static constexpr int kNumBars = 3 + 2 * kKStages + 2 * kVStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
     // each Q tile's softmax runs in kSplit warpgroups, one per 1 / kSplit of
@@ -130,6 +142,13 @@ struct PrefillTcCfg {
     static constexpr int kSplit = D <= 64 ? PA_PREFILL_SPLIT_D64 : PA_PREFILL_SPLIT_D128;
     static_assert(kSplit == 1 || kSplit == 2, "one or two softmax warpgroups per Q tile");
     static constexpr int kHalfCols = kN / kSplit;
+    // With one S buffer and one softmax warpgroup, P can be handed over in two
+    // halves (p_half after the P of the tile's first N / 2 tokens), so the
+    // first half of the PV runs under the second half's exponentials: 4 %
+    // faster at head_dim 64 (192-column rows), 1.6 % slower at head_dim 128
+    // (the mid-pass store wait costs more than the overlap gains there).
+    static constexpr bool kHalfP =
+        kSBufs == 1 && kSplit == 1 && (D <= 64 ? PA_PREFILL_HALFP_D64 : PA_PREFILL_HALFP_D128);
     static constexpr int kXBarOffset = kSlotOffset + 16;
     static constexpr int kXOffset = kXBarOffset + kQTiles * 3 * 8 + 8;
     static constexpr int kXBytes = kSplit > 1 ? kQTiles * 3 * 2 * 128 * 4 : 0;   // [tile][max0, max1, sum][half][row]
@@ -217,6 +236,15 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// Hand over the P of a tile's first half: its tensor-memory stores complete,
+// ordered before the warp's arrive (one per warp) on `bar`.
+__device__ __forceinline__ void p_half_arrive(uint32_t bar, bool leader) {
+    tc05::wait_st();
+    tc05::fence_before_sync();
+    __syncwarp();
+    if (leader) mbar_arrive_cta(bar);
+}
+
 // Row max of one S tile in tensor memory (raw logits, columns c <= lim only
 // when MASK), read in 32-column chunks with the next chunk's load in flight
 // while the current one is reduced.  Unmasked and PACKED, each step folds two
@@ -263,7 +291,8 @@ __device__ __forceinline__ float tile_row_max(uint32_t sb, int lim) {
 // head_dim 64 the pairs spill registers of the 576-thread CTA, so it keeps the
 // scalar form).
 template <typename T, int N, bool MASK, bool PACKED>
-__device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, float mu) {
+__device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, float mu,
+                                            uint32_t half_bar, bool leader) {
     uint32_t rr[2][32];
     tc05::ld32_async(sb, rr[0]);
     if constexpr (PACKED && !MASK) {
@@ -285,6 +314,7 @@ __device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, flo
                 pk[i] = Mma<T>::pack(e0, e1);
             }
             tc05::st16(sb + h * 16, pk);
+            if (half_bar != 0 && h == N / 64 - 1) p_half_arrive(half_bar, leader);
         }
         const float2 a = f2_split(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
         return a.x + a.y;
@@ -308,6 +338,7 @@ __device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, flo
                 pk[i] = Mma<T>::pack(e0, e1);
             }
             tc05::st16(sb + h * 16, pk);
+            if (half_bar != 0 && h == N / 64 - 1) p_half_arrive(half_bar, leader);
         }
         return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
     }
@@ -348,7 +379,7 @@ __device__ __forceinline__ float row_load_max(uint32_t (&sr)[N / 32][32], uint32
 
 template <typename T, int N, bool MASK>
 __device__ __forceinline__ float row_p_regs(const uint32_t (&sr)[N / 32][32], uint32_t sb, int lim,
-                                            float sl2, float mu) {
+                                            float sl2, float mu, uint32_t half_bar, bool leader) {
     uint64_t sp[4];   // four pair-sum chains
     const uint64_t scale2 = f2(sl2, sl2), neg_mu2 = f2(-mu, -mu);
 #pragma unroll
@@ -369,6 +400,7 @@ __device__ __forceinline__ float row_p_regs(const uint32_t (&sr)[N / 32][32], ui
             pk[i] = Mma<T>::pack(e0, e1);
         }
         tc05::st16(sb + h * 16, pk);
+        if (half_bar != 0 && h == N / 64 - 1) p_half_arrive(half_bar, leader);
     }
     const float2 a = f2_split(fadd2(fadd2(sp[0], sp[1]), fadd2(sp[2], sp[3])));
     return a.x + a.y;
@@ -391,7 +423,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     const uint32_t q_full = bars, vtail = bars + 8, mma_done = bars + 16;
     const uint32_t k_full = bars + 24, k_empty = k_full + NK * 8;
     const uint32_t v_full = k_empty + NK * 8, v_empty = v_full + NV * 8;
-    const uint32_t tile_bars = v_empty + NV * 8;   // + t * 56: s_full, p_full, s_free, o_full
+    const uint32_t tile_bars = v_empty + NV * 8;   // + t * kTileBarBytes: s_full, p_full, s_free, o_full, p_half
     const uint32_t slot = base + C::kSlotOffset;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
@@ -442,13 +474,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             mbar_init(v_empty + i * 8, 1);
         }
         for (int t = 0; t < NQ; ++t) {
-            const uint32_t tb = tile_bars + t * 56;
+            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
             for (int i = 0; i < 2; ++i) {
                 mbar_init(tb + i * 8, 1);          // s_full
                 mbar_init(tb + 16 + i * 8, 4 * C::kSplit);   // p_full: one arrive per softmax warp
                 mbar_init(tb + 32 + i * 8, 1);     // s_free
             }
             mbar_init(tb + 48, 1);                 // o_full
+            mbar_init(tb + 56, 4 * C::kSplit);     // p_half
             if (C::kSplit > 1)
                 for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
         }
@@ -623,7 +656,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         };
         // S_j = Q_t K_j^T into S buffer j % SB; the last Q tile's QK frees the K stage
         auto issue_qk = [&](int t, int j) {
-            const uint32_t tb = tile_bars + t * 56;
+            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
             const uint32_t tcol = tmem + t * C::kTileCols;
             const uint32_t kst = kstage0 + (j % NK) * C::kTileBytes;
             const uint32_t qst = q_smem + t * C::kQTileBytes;
@@ -637,13 +670,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             tc05::commit_elect(tb + (j % SB) * 8);   // s_full
             if (t == nq - 1) tc05::commit_elect(k_empty + (j % NK) * 8);
         };
-        // O_t += P_j V_j; the last Q tile's PV frees the V stage
-        auto issue_pv = [&](int t, int j) {
-            const uint32_t tb = tile_bars + t * 56;
+        // O_t += P_j V_j over the K-steps [kt0, kt1) (16 tokens each); the end of
+        // the last Q tile's PV frees the V stage
+        auto issue_pv = [&](int t, int j, int kt0, int kt1) {
+            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
             const uint32_t tcol = tmem + t * C::kTileCols;
             const uint32_t vst = vstage0 + (j % NV) * C::kTileBytes;
 #pragma unroll
-            for (int kt = 0; kt < N / 16; ++kt)
+            for (int kt = kt0; kt < kt1; ++kt)
                 // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
                 // whose P occupies the first half of its own S columns
                 tc05::mma_ts_elect(tcol + C::kOCol,
@@ -651,6 +685,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                                        ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
                                    tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024), idesc_pv,
                                    (j > 0 || kt > 0) ? 1u : 0u);
+            if (kt1 < N / 16) return;
             // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
             // tracks this PV as well, so none is needed
             if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
@@ -666,9 +701,17 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             if (!wait(v_full + (j % NV) * 8, (j / NV) & 1u)) break;
             const int jn = j + SB;   // the QK issued behind this tile's PV
             for (int t = 0; t < nq; ++t) {
-                if (!wait(tile_bars + t * 56 + 16 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
+                const uint32_t tb = tile_bars + t * C::kTileBarBytes;
+                int kt0 = 0;
+                if (C::kHalfP) {   // the PV of the first N / 2 tokens once their P is in
+                    if (!wait(tb + 56, j & 1u)) break;   // p_half
+                    tc05::fence_after_sync();
+                    issue_pv(t, j, 0, N / 32);
+                    kt0 = N / 32;
+                }
+                if (!wait(tb + 16 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
                 tc05::fence_after_sync();
-                issue_pv(t, j);
+                issue_pv(t, j, kt0, N / 16);
                 if (jn < ntiles) {
                     if (t == 0 && !wait(k_full + (jn % NK) * 8, (jn / NK) & 1u)) break;
                     tc05::fence_after_sync();
@@ -690,7 +733,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         // 18-warp CTA of head_dim 64 with split rows is capped at 96 per thread
         constexpr bool PK = D >= 128 || SP == 1;
         // whole rows of head_dim >= 128 keep S in registers between the passes
-        constexpr bool RR = PA_PREFILL_REGROW && SP == 1 && D >= 128;
+        constexpr bool RR = PA_PREFILL_REGROW && SP == 1 && N <= 128;
         constexpr int RC = RR ? N / 32 : 1;
         const int t = idx / (4 * SP);     // the Q tile of this warp
         const int hf = (idx >> 2) % SP;   // the part of the S columns it handles
@@ -703,7 +746,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             const int pos = pos_first + tq;   // last cache token this row sees
             const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
             const uint32_t tcol = tmem + lane_base + t * C::kTileCols;
-            const uint32_t tb = tile_bars + t * 56;
+            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
             const uint32_t xbar = base + C::kXBarOffset + t * 3 * 8;   // max exchange x2, sums
             float *xch = reinterpret_cast<float *>(smem + C::kXOffset) + t * 3 * 256;
             const float sl2 = p.scale_log2;
@@ -777,12 +820,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 }
                 // pass 2: P of this part over the first half of its own S columns
                 const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
+                const uint32_t hb = C::kHalfP ? tb + 56 : 0u;   // p_half
                 if constexpr (RR)
-                    l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu)
-                              : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu);
+                    l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu, hb, lane == 0)
+                              : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu, hb, lane == 0);
                 else
-                    l += full ? tile_row_p<T, HC, false, PK>(sb, lim, sl2, mu)
-                              : tile_row_p<T, HC, true, PK>(sb, lim, sl2, mu);
+                    l += full ? tile_row_p<T, HC, false, PK>(sb, lim, sl2, mu, hb, lane == 0)
+                              : tile_row_p<T, HC, true, PK>(sb, lim, sl2, mu, hb, lane == 0);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
