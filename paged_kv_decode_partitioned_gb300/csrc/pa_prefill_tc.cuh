@@ -345,17 +345,19 @@ __device__ __forceinline__ float tile_row_p(uint32_t sb, int lim, float sl2, flo
 }
 
 // Register-resident form of the two passes, for one thread per whole row
-// with registers to spare: the row's S is read from tensor memory once (each
-// 32-column chunk's read in flight while the previous chunk is reduced to the
-// row max) and the P pass works from the registers.
+// with registers to spare: the row's S is read from tensor memory once (all
+// chunks' reads in flight together; reading chunk by chunk with the next one
+// in flight measured the same) and the P pass works from the registers.
 template <int N, bool MASK>
 __device__ __forceinline__ float row_load_max(uint32_t (&sr)[N / 32][32], uint32_t sb, int lim) {
     float mt = -INFINITY;
-    tc05::ld32_async(sb, sr[0]);
+    // every chunk's read in flight at once, then one wait
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) tc05::ld32_async(sb + h * 32, sr[h]);
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) tc05::wait_ld(sr[h]);
 #pragma unroll
     for (int h = 0; h < N / 32; ++h) {
-        tc05::wait_ld(sr[h]);   // the only read in flight is chunk h's
-        if (h + 1 < N / 32) tc05::ld32_async(sb + (h + 1) * 32, sr[h + 1]);
         float mx[8];
         if constexpr (!MASK) {
 #pragma unroll
