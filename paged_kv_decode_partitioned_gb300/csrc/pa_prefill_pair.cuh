@@ -21,7 +21,7 @@
 // buffers in tensor memory, so the QK of the next tile runs under the
 // softmax of the current one.
 //
-// Warp roles (352 threads per CTA):
+// Warp roles (96 + 128 kSplit NQ threads per CTA: 224 at head_dim 256):
 //   warp 0     TMA producer of this CTA's Q rows (once) and K halves, the last
 //              warp of its V halves, each through NS stages (one copy per
 //              lane).  The copies of both CTAs complete on the even CTA's
@@ -31,10 +31,11 @@
 //   warp 1     tensor-memory owner; in the even CTA it runs the pair's fixed
 //              MMA sequence, one elected lane issuing each MMA and committing
 //              it to both CTAs' barriers;
-//   warps 2..  softmax, as in the single-CTA kernel: two warpgroups, each
-//              half of the S columns of every row, P written over S in this
-//              CTA's tensor memory and reported to the even CTA; O rescaled in
-//              place when a row's max grows by more than 2^8; O / l -> out.
+//   warps 2..  softmax, as in the single-CTA kernel: kSplit warpgroups per
+//              Q tile (one by default: a thread per whole row, its S held in
+//              registers), P written over S in this CTA's tensor memory and
+//              reported to the even CTA; O rescaled in place when a row's max
+//              grows by more than 2^8; O / l -> out.
 // Arrivals from the odd CTA on the even CTA's barriers are CTA-scope
 // releases (a cluster-scope release costs ~3x the round trip between the
 // SMs, measured: 945 against 364 cycles) except for the two that publish
@@ -49,6 +50,16 @@
 #include "pa_prefill_tc.cuh"
 
 namespace pa {
+
+// Softmax warpgroups per Q tile on pairs (as PA_PREFILL_SPLIT_* for single
+// CTAs): one thread per whole row, the row's S held in registers, measured
+// 1940 -> 2050 TFLOP/s at head_dim 256 against two warpgroups on column halves.
+#ifndef PA_PREFILL_PAIR_SPLIT_D128
+#define PA_PREFILL_PAIR_SPLIT_D128 1
+#endif
+#ifndef PA_PREFILL_PAIR_SPLIT_D256
+#define PA_PREFILL_PAIR_SPLIT_D256 1
+#endif
 
 template <int D>
 struct PrefillPairCfg {
@@ -82,16 +93,19 @@ struct PrefillPairCfg {
     static constexpr int kTileBars = 7;
     static constexpr int kNumBars = 4 + 4 * kStages + kTileBars * kQTiles;
     static constexpr int kSlotOffset = kBarOffset + kNumBars * 8;
-    static constexpr int kHalfCols = kN / 2;
-    // each Q tile's two softmax warpgroups swap row maxima (two buffers by
-    // tile parity) and, at the end, row sums: xbar[2] and xend per Q tile
+    // kSplit softmax warpgroups per Q tile, each 1 / kSplit of the S columns of
+    // every row; with two, they swap row maxima (two buffers by tile parity)
+    // and, at the end, row sums: xbar[2] and xend per Q tile
+    static constexpr int kSplit = D == 128 ? PA_PREFILL_PAIR_SPLIT_D128 : PA_PREFILL_PAIR_SPLIT_D256;
+    static_assert(kSplit == 1 || kSplit == 2, "one or two softmax warpgroups per Q tile");
+    static constexpr int kHalfCols = kN / kSplit;
     static constexpr int kXBarOffset = kSlotOffset + 16;
     static constexpr int kXOffset = kXBarOffset + kQTiles * 3 * 8 + 8;
-    static constexpr int kXBytes = kQTiles * 3 * 2 * 128 * 4;   // [tile][max0, max1, sum][half][row]
+    static constexpr int kXBytes = kSplit > 1 ? kQTiles * 3 * 2 * 128 * 4 : 0;   // [tile][max0, max1, sum][half][row]
     static constexpr int kLaunchBytes = kXOffset + kXBytes + 1024;
     static constexpr int kSoftmaxWarp0 = 2;
     // warp 0 Q and K producer, warp 1 MMA, the softmax warps, then the V producer
-    static constexpr int kVWarp = kSoftmaxWarp0 + 8 * kQTiles;
+    static constexpr int kVWarp = kSoftmaxWarp0 + 4 * kSplit * kQTiles;
     static constexpr int kThreads = 32 * (kVWarp + 1);
     // tensor memory per Q tile: S buffers [0, kSBufs N), O [kSBufs N, kSBufs N + D)
     static constexpr int kOCol = kSBufs * kN;
@@ -219,10 +233,11 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(tb + i * 8, 1);          // s_full
                 mbar_init(tb + 16 + i * 8, 1);     // s_free
-                mbar_init(tb + 32 + i * 8, 16);    // p_full: one arrive per softmax warp of both CTAs
+                mbar_init(tb + 32 + i * 8, 8 * C::kSplit);   // p_full: one arrive per softmax warp of both CTAs
             }
             mbar_init(tb + 48, 1);                 // o_full
-            for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
+            if (C::kSplit > 1)
+                for (int i = 0; i < 3; ++i) mbar_init(base + C::kXBarOffset + (t * 3 + i) * 8, 8);
         }
         fence_mbar_init();
     }
@@ -470,9 +485,12 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------ softmax ------------------------------
+        constexpr int SP = C::kSplit;
+        // one thread per whole row keeps the row's S in registers between passes
+        constexpr bool RR = SP == 1;
         const int idx = warp - C::kSoftmaxWarp0;
-        const int t = idx >> 3;              // the Q tile of this warp
-        const int hf = (idx >> 2) & 1;       // the half of the S columns it handles
+        const int t = idx / (4 * SP);         // the Q tile of this warp
+        const int hf = (idx >> 2) % SP;       // the part of the S columns it handles
         if (t < nq) {
             const int quarter = warp & 3;         // tensor-memory lanes 32*quarter .. +31
             const int rl = quarter * 32 + lane;   // row within the Q tile
@@ -501,16 +519,25 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
                 const int lim = pos - jt * N - hf * HC;
                 const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
-                const float pm = full ? tile_row_max<HC, false, true>(sb, lim)
-                                      : tile_row_max<HC, true, true>(sb, lim);
-                xch[(j & 1) * 256 + hf * 128 + rl] = pm;
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
-                if (!__all_sync(0xffffffffu, mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
-                    ok = false;
-                    break;
+                uint32_t sr[RR ? N / 32 : 1][32];
+                float pm;
+                if constexpr (RR)
+                    pm = full ? row_load_max<N, false>(sr, sb, lim) : row_load_max<N, true>(sr, sb, lim);
+                else
+                    pm = full ? tile_row_max<HC, false, true>(sb, lim)
+                              : tile_row_max<HC, true, true>(sb, lim);
+                float mt = pm;
+                if constexpr (SP > 1) {
+                    xch[(j & 1) * 256 + hf * 128 + rl] = pm;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                 }
-                float mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                 mt *= sl2;
                 if (j == 0) {
                     m = mt;
@@ -530,20 +557,26 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     const float alpha = m == mn ? 1.f : ex2(m - mn);
                     m = mn;
                     l *= alpha;
+                    // this part's O columns, 16 at a time while the S row is held
+                    constexpr int OC = RR ? 16 : 32;
 #pragma unroll
-                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                        uint32_t rr[32];
-                        const uint32_t oc = tcol + C::kOCol + hf * (D / 2) + c0;
-                        tc05::ld32(oc, rr);
+                    for (int c0 = 0; c0 < D / SP; c0 += OC) {
+                        uint32_t rr[OC];
+                        const uint32_t oc = tcol + C::kOCol + hf * (D / SP) + c0;
+                        if constexpr (RR) tc05::ld16(oc, rr); else tc05::ld32(oc, rr);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
+                        for (int i = 0; i < OC; ++i)
                             rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                        tc05::st32(oc, rr);
+                        if constexpr (RR) tc05::st16(oc, rr); else tc05::st32(oc, rr);
                     }
                 }
                 const float mu = m == -INFINITY ? 0.f : m;
-                l += full ? tile_row_p<T, HC, false, true>(sb, lim, sl2, mu, 0u, false)
-                          : tile_row_p<T, HC, true, true>(sb, lim, sl2, mu, 0u, false);
+                if constexpr (RR)
+                    l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu, 0u, false)
+                              : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu, 0u, false);
+                else
+                    l += full ? tile_row_p<T, HC, false, true>(sb, lim, sl2, mu, 0u, false)
+                              : tile_row_p<T, HC, true, true>(sb, lim, sl2, mu, 0u, false);
                 tc05::wait_st();
                 tc05::fence_before_sync();
                 __syncwarp();
@@ -554,7 +587,7 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                         mbar_arrive_remote(dsmem_addr(tb + 32 + b * 8, 0));
                 }
             }
-            if (ok) {
+            if (SP > 1 && ok) {   // the row sum is the two parts' shares
                 xch[2 * 256 + hf * 128 + rl] = l;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cta(xbar + 16);
@@ -570,11 +603,11 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 T *orow = static_cast<T *>(p.out) +
                           (static_cast<size_t>(row0 + tok0 + tq) * p.num_q_heads + kvh * g + hq) * D +
-                          hf * (D / 2);
+                          hf * (D / SP);
 #pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                for (int c0 = 0; c0 < D / SP; c0 += 32) {
                     uint32_t rr[32];
-                    tc05::ld32(tcol + C::kOCol + hf * (D / 2) + c0, rr);
+                    tc05::ld32(tcol + C::kOCol + hf * (D / SP) + c0, rr);
                     if (valid) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) {
