@@ -277,7 +277,7 @@ def _ramped_keys(pc, rate_log2, seed, spike=None):
 
 @pytest.mark.parametrize("D,rate,spike", [
     (128, 12.0, None), (128, 5.0, None), (64, 12.0, None), (256, 12.0, None),
-    (128, 0.5, (1200, 60.0)), (256, 0.5, (700, 60.0)),
+    (128, 0.5, (1200, 60.0)), (256, 0.5, (700, 60.0)), (64, 0.5, (1000, 60.0)),
 ])
 def test_prefill_running_max_rescales(pa, D, rate, spike):
     """The O rescale path: the row max grows by more than 2^8 from one K/V tile to
