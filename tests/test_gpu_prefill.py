@@ -96,11 +96,13 @@ def test_one_row_chunks_equal_decode(pa):
     assert pa.device_status() == 0
 
 
-def test_nan_past_the_context_is_never_used(pa):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_nan_past_the_context_is_never_used(pa, D):
     """Cache rows past each sequence's last token (and unused blocks) hold NaN:
-    the masked logits and the zeroed V rows of the last stage keep them out."""
-    w = _workload(16, 2, 128, 32, torch.float16)
-    host = make_prefill_case(w, ctx_lens=[7, 100, 33], q_lens=[20, 61, 1], seed=3200)
+    the masked logits and the zeroed V rows of the last stage keep them out
+    (on single CTAs at head_dim 64 and 128, on CTA pairs at 256)."""
+    w = _workload(16, 2, D, 32, torch.float16)
+    host = make_prefill_case(w, ctx_lens=[7, 100, 33], q_lens=[20, 61, 1], seed=3200 + D)
     kc, vc = host.case.key_cache.clone(), host.case.value_cache.clone()
     bs = kc.shape[1]
     used = torch.zeros(kc.shape[0], dtype=torch.bool)
@@ -115,14 +117,15 @@ def test_nan_past_the_context_is_never_used(pa):
     vc[~used] = float("nan")
     host.case.key_cache, host.case.value_cache = kc, vc
     out = _run(pa, host.to("cuda"))
-    assert_out_close(out, _oracle(host), "prefill with NaN past the context")
+    assert_out_close(out, _oracle(host), f"prefill with NaN past the context, head_dim {D}")
     assert pa.device_status() == 0
 
 
-def test_block_permutation_gives_identical_bits(pa):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_block_permutation_gives_identical_bits(pa, D):
     """Which physical block holds a page does not change a single output bit."""
-    w = _workload(24, 4, 128, 16, torch.bfloat16)
-    host = make_prefill_case(w, ctx_lens=[300, 50], q_lens=[80, 40], seed=3300)
+    w = _workload(24 if D == 128 else 16, 4 if D < 256 else 2, D, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[300, 50], q_lens=[80, 40], seed=3300 + D)
     dev = host.to("cuda")
     out1 = _run(pa, dev)
     nb = dev.case.key_cache.shape[0]
