@@ -221,7 +221,7 @@ def test_max_q_len_too_small_raises_flag(pa):
 
 
 @pytest.mark.parametrize("name", ["chunk2048_ctx16384_x16", "full100k_x1",
-                                  "d256_chunk2048_ctx16384_x8"])
+                                  "chunk512_ctx4096_x64", "d256_chunk2048_ctx16384_x8"])
 def test_bench_prefill_workloads_sampled(pa, name):
     """The bench's prefill workloads at full size, in the bench's launch, checked on
     sampled rows (first, last and random rows of a few sequences) against the oracle."""
