@@ -293,3 +293,17 @@ def test_prefill_running_max_rescales(pa, D, rate, spike):
     out = _run(pa, host.to("cuda"))
     assert pa.device_status() == 0
     assert_out_close(out, _oracle(host), f"rescaled prefill D={D} rate={rate} spike={spike}")
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,bs", [(64, 32, 4, 16), (128, 24, 4, 48), (256, 16, 2, 32)])
+def test_repeated_launches_are_bit_identical(pa, D, Hq, Hkv, bs):
+    """The MMA order and the softmax are fixed, so every launch gives the same
+    bits: a race in the producer / MMA / softmax hand-offs would show as an
+    occasional difference (single CTAs at head_dim 64 and 128, pairs at 256)."""
+    w = _workload(Hq, Hkv, D, bs, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[3000, 40, 900], q_lens=[600, 40, 129], seed=3700 + D)
+    dev = host.to("cuda")
+    first = _run(pa, dev)
+    for _ in range(8):
+        assert torch.equal(_run(pa, dev).view(torch.int16), first.view(torch.int16))
+    assert pa.device_status() == 0
