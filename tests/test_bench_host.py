@@ -1,6 +1,7 @@
 """Host-side logic of bench.py (no GPU): the roofline numerators, the clock
 record that decides whether a run is kept, and the guard that drops a
 committed traffic figure once the kernel sources change."""
+import json
 import random
 
 import pytest
@@ -79,16 +80,22 @@ def test_clock_summary_median_of_the_samples():
     assert bench.ClockSampler.summary(rows, 1.0, 1.2)["sm_mhz"] == 2000.0
 
 
-@pytest.mark.parametrize("key,kw", [("workload4_P512", {"wid": 4, "partition_size": 512}),
-                                    ("prefill_chunk2048_ctx16384_x16",
-                                     {"wid": "prefill_chunk2048_ctx16384_x16"})])
-def test_committed_traffic_is_dropped_when_the_sources_change(monkeypatch, key, kw):
+def test_committed_traffic_is_dropped_when_the_sources_change(monkeypatch, tmp_path):
     """A committed ncu figure is reported only while the kernel sources it was
     taken on are unchanged (their hash is stored beside it)."""
-    value = bench.committed_traffic(**kw)
-    assert value is not None and value > 0
-    monkeypatch.setattr(bench, "source_sha", lambda path="decode": "0" * 16)
-    assert bench.committed_traffic(**kw) is None
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({
+        "workload4_P512": {"dram_bytes_per_launch": 123, "source_sha": "a" * 16},
+        "prefill_chunk": {"dram_bytes_per_launch": 456, "source_sha": "b" * 16}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    shas = {"decode": "a" * 16, "prefill": "b" * 16}
+    monkeypatch.setattr(bench, "source_sha", lambda path="decode": shas.get(path, "c" * 16))
+    assert bench.committed_traffic(4, partition_size=512) == 123
+    assert bench.committed_traffic("prefill_chunk") == 456
+    assert bench.committed_traffic(3, partition_size=512) is None   # no figure taken
+    shas["decode"] = "d" * 16                                        # decode sources changed
+    assert bench.committed_traffic(4, partition_size=512) is None
+    assert bench.committed_traffic("prefill_chunk") == 456
 
 
 def test_source_hash_covers_every_listed_source():
