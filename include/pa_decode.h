@@ -351,8 +351,8 @@ PA_API int pa_decode_auto_static(void *out, const void *query, const void *key_c
  * past the coverage not written.  q_start is read on the
  * device only: a sequence whose rows fall outside [0, num_rows], or whose
  * chunk is longer than seq_lens[s], is skipped and raises PA_DEV_BAD_ROWS.
- * Supported: head_dim 64, 128 or 256, block_size a multiple of 16, GQA group
- * 1..128.  One kernel launch on `stream`; no workspace.
+ * Supported: head_dim 64, 128 or 256, block_size 8 or a multiple of 16, GQA
+ * group 1..128.  One kernel launch on `stream`; no workspace.
  */
 PA_API int pa_prefill(void *out, const void *query, const void *key_cache,
                       const void *value_cache, const int32_t *block_tables,

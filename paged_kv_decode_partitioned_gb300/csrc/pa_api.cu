@@ -108,10 +108,10 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
 
 // 5-D view of a cache with the row in the block ahead of the piece: (element
 // within a 64-element piece, row in block, piece, KV head, block); one box =
-// `pieces` consecutive 64-element pieces of 16 rows of one KV head, landing
-// piece after piece ([piece][16 rows][128 B], 128-byte swizzled), so one copy
-// moves several pieces of a block.  Used for the V tiles of the prefill
-// kernels (block_size a multiple of 16).
+// `pieces` consecutive 64-element pieces of 16 rows of one KV head (8 rows for
+// block_size 8), landing piece after piece ([piece][rows][128 B], 128-byte
+// swizzled), so one copy moves several pieces of a block.  Used for the V
+// tiles of the prefill kernels.
 int make_cache_map_pieces(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv,
                           int bs, int num_blocks, int pieces) {
     EncodeTiledFn fn = encode_fn();
@@ -121,7 +121,8 @@ int make_cache_map_pieces(CUtensorMap *m, const void *cache, pa_dtype_t dtype, i
                           static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
     cuuint64_t strides[4] = {static_cast<cuuint64_t>(Hkv) * D * e, 64 * e, D * e,
                              static_cast<cuuint64_t>(bs) * Hkv * D * e};
-    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(pieces), 1, 1};
+    const cuuint32_t rows = static_cast<cuuint32_t>(bs < kTile ? bs : kTile);
+    cuuint32_t box[5] = {64, rows, static_cast<cuuint32_t>(pieces), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -887,7 +888,7 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARGUMENT;
     const int group = num_q_heads / num_kv_heads;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
-    if (block_size % kTile != 0) return PA_ERR_UNSUPPORTED;
+    if (block_size % kTile != 0 && block_size != kTile / 2) return PA_ERR_UNSUPPORTED;
     if (group > kPrefillRows) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;

@@ -258,25 +258,33 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kKOps = 4 * C::kPieces;    // this CTA's 4 boxes of K x pieces
         constexpr int kVOps = 8;                 // all 8 boxes of V, this CTA's pieces in one copy
+        static_assert(2 * kKOps <= 32 && 2 * kVOps <= 32, "one copy per lane");
         const bool lead = rank == 0;
-        const int k_box = 4 * static_cast<int>(rank) + (lane % kKOps) / C::kPieces;
-        const int k_piece = (lane % kKOps) % C::kPieces;
-        const int v_box = lane % kVOps;
+        // block_size 8: a 16-token box is two 8-row blocks, a copy each (lane
+        // pairs take the two halves of one box)
+        const bool b8 = p.block_size < kTile;
+        const int op = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
+        const int k_box = 4 * static_cast<int>(rank) + (op % kKOps) / C::kPieces;
+        const int k_piece = (op % kKOps) % C::kPieces;
+        const int v_box = op % kVOps;
         const int v_piece = static_cast<int>(rank) * C::kVPieces;   // first piece of the box
-        // block of this lane's K (V) box of tile jt, read a tile ahead and
-        // checked only when the copy is issued
+        // block of this lane's K (V) box (half) of tile jt, read a tile ahead and
+        // checked only when the copy is issued; -1 (a box of zeros) for a half
+        // past the context
         auto block_of = [&](int jt, int box, bool has) -> int {
             const int bx = jt * (N / kTile) + box;
             if (!has || bx >= nbox) return 0;
-            return __ldg(bt_row + (bx * kTile) / p.block_size);
+            const int tok = bx * kTile + half * (kTile / 2);
+            if (b8 && tok >= kv_end) return -1;
+            return __ldg(bt_row + tok / p.block_size);
         };
         auto check_block = [&](int b) {
-            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
+            if (b != -1 && static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
                 atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
         };
         // the even CTA's barrier at the same offset (this CTA's own in the even CTA)
         auto lead_bar = [&](uint32_t bar) -> uint32_t { return lead ? bar : dsmem_addr(bar, 0); };
-        const bool k_has = lane < kKOps, v_has = lane < kVOps;
+        const bool k_has = op < kKOps, v_has = op < kVOps;
         if (warp == 0) {
             // Q: the box covers g * tpc rows; rows past it (and every row of a CTA
             // without chunk tokens) are zeroed so they stay finite
@@ -330,9 +338,9 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             __syncwarp();
             if (k_has && jt * (N / kTile) + k_box < nbox)
                 tma_load_5d_pair(stage0 + st * C::kStageBytes + k_piece * C::kKPiece +
-                                     (k_box - 4 * static_cast<int>(rank)) * 2048,
+                                     (k_box - 4 * static_cast<int>(rank)) * 2048 + half * 1024,
                                  &tmK, lead_bar(k_full + st * 8), 0, k_piece, kvh,
-                                 ((jt * (N / kTile) + k_box) * kTile) % p.block_size, kb);
+                                 b8 ? 0 : ((jt * (N / kTile) + k_box) * kTile) % p.block_size, kb);
             k_issued = j + 1;
             return true;
         };
@@ -360,8 +368,10 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             __syncwarp();
             if (v_has && jt * (N / kTile) + v_box < nbox)
                 // the V map has the row ahead of the piece: (element, row, piece, head, block)
-                tma_load_5d_pair(vdst + v_box * C::kVBoxBytes, &tmV, vbar, 0,
-                                 ((jt * (N / kTile) + v_box) * kTile) % p.block_size, v_piece, kvh, vb);
+                // ([piece][16 rows] per box; [half][piece][8 rows] with 8-row blocks)
+                tma_load_5d_pair(vdst + v_box * C::kVBoxBytes + half * (C::kVPieces * 1024), &tmV, vbar, 0,
+                                 b8 ? 0 : ((jt * (N / kTile) + v_box) * kTile) % p.block_size, v_piece,
+                                 kvh, vb);
             issued = j + 1;
             if (last) {
                 const bool w = mbar_wait_cycles(vtail, 0);
@@ -371,9 +381,10 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 for (int e = lane; e < nchunks; e += 32) {
                     const int r = first_row + e / (C::kVPieces * 8);
                     const int c = (e / 8) % C::kVPieces;
-                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBoxBytes +
-                                               c * 2048 + (r & 15) * 128 + (e & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
+                    const int off = b8 ? ((r >> 3) & 1) * (C::kVPieces * 1024) + c * 1024 + (r & 7) * 128
+                                       : c * 2048 + (r & 15) * 128;
+                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBoxBytes + off +
+                                               (e & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -416,6 +427,10 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 256);
             constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 256);
             constexpr uint16_t kBoth = 0x3;
+            // V per 16-token box: pieces 2 KB apart, 8-row groups 1 KB apart; with
+            // 8-row blocks pieces 1 KB apart, the halves kVPieces KB apart
+            const bool b8 = p.block_size < kTile;
+            const uint32_t v_lbo = b8 ? 1024u : 2048u, v_sbo = b8 ? C::kVPieces * 1024u : 1024u;
             bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
             auto wait = [&](uint32_t bar, uint32_t parity) {
                 ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
@@ -448,7 +463,7 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     // occupies the first half of that half's S columns
                     tc05::mma2_ts_elect(tcol + C::kOCol,
                                         tcol + (j % SB) * N + ((16 * kt) / HC) * (HC / 2) + kt * 8,
-                                        tc05::sw128_desc(vst + kt * C::kVBoxBytes, 2048, 1024),
+                                        tc05::sw128_desc(vst + kt * C::kVBoxBytes, v_lbo, v_sbo),
                                         idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
                 // s_free: with one S buffer the commit of the QK issued next
                 // (S_{j+1}) tracks this PV as well, so none is needed

@@ -502,19 +502,24 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kBoxes = N / kTile;   // 16-token boxes per tile
-        constexpr int kOps = kBoxes * C::kPieces;   // copies per K tile
-        static_assert(kOps <= 32, "one copy per lane");
-        // block of this lane's box of tile jt (0 when the lane has no copy).
+        constexpr int kOps = kBoxes * C::kPieces;   // copies per K tile (twice with 8-row blocks)
+        static_assert(2 * kOps <= 32, "one copy per lane");
+        // block_size 8: a 16-token box is two 8-row blocks, one copy each
+        const bool b8 = p.block_size < kTile;
+        // block of this lane's box (half) of tile jt (0 when the lane has no
+        // copy; -1, an out-of-range box of zeros, for a half past the context).
         // The read goes out a tile ahead and is checked only when the copy is
         // issued, so its latency overlaps the stage waits in between (with one
         // stage, a read consumed at once put ~3000 cycles on every tile's K load).
-        auto box_block = [&](int jt, int box, bool has) -> int {
+        auto box_block = [&](int jt, int box, int half, bool has) -> int {
             const int bx = jt * kBoxes + box;
             if (!has || bx >= nbox) return 0;
-            return __ldg(bt_row + (bx * kTile) / p.block_size);
+            const int tok = bx * kTile + half * (kTile / 2);
+            if (b8 && tok >= kv_end) return -1;
+            return __ldg(bt_row + tok / p.block_size);
         };
         auto check_block = [&](int b) {
-            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
+            if (b != -1 && static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
                 atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
         };
         // bytes of tile jt's boxes inside the context (K or V: the same)
@@ -543,14 +548,16 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 for (int c = 0; c < C::kPieces; ++c)
                     tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
             }
-            // K: one copy per (16-row box, 64-element piece) and lane
-            const int op_box = (lane % kOps) / C::kPieces, op_piece = (lane % kOps) % C::kPieces;
-            const bool has = lane < kOps;
-            int jt = rot, phys_next = box_block(rot, op_box, has), issued = 0;
+            // K: one copy per (16-row box, 64-element piece) and lane; with
+            // 8-row blocks one per (box, piece, half)
+            const int q = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
+            const int op_box = (q % kOps) / C::kPieces, op_piece = (q % kOps) % C::kPieces;
+            const bool has = q < kOps;
+            int jt = rot, phys_next = box_block(rot, op_box, half, has), issued = 0;
             for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
                 const int st = j % NK, phys = phys_next, jc = jt;
                 jt = jt + 1 == ntiles ? 0 : jt + 1;
-                if (j + 1 < ntiles) phys_next = box_block(jt, op_box, has);   // next tile's entry
+                if (j + 1 < ntiles) phys_next = box_block(jt, op_box, half, has);   // next tile's entry
                 // K of tile j once every QK of tile j - NK is done
                 if (j >= NK) {
                     const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NK) - 1) & 1u);
@@ -565,9 +572,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 if (lane == 0) mbar_expect_tx(k_full + st * 8, tile_bytes(jc));
                 __syncwarp();
                 if (has && jc * kBoxes + op_box < nbox)
-                    tma_load_5d(kstage0 + st * C::kTileBytes + op_piece * C::kKvPiece + op_box * 2048,
+                    tma_load_5d(kstage0 + st * C::kTileBytes + op_piece * C::kKvPiece + op_box * 2048 +
+                                    half * 1024,
                                 &tmK, k_full + st * 8, 0, op_piece, kvh,
-                                ((jc * kBoxes + op_box) * kTile) % p.block_size, phys);
+                                b8 ? 0 : ((jc * kBoxes + op_box) * kTile) % p.block_size, phys);
                 issued = j + 1;
             }
             if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
@@ -577,14 +585,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             for (int j = issued > NK ? issued - NK : 0; j < issued; ++j)
                 (void)mbar_wait_cycles(k_full + (j % NK) * 8, (j / NK) & 1u);
         } else {
-            // V: one copy per 16-row box moves all its pieces
-            const int v_box = lane % kBoxes;
-            const bool has = lane < kBoxes;
-            int jt = rot, phys_next = box_block(rot, v_box, has), issued = 0;
+            // V: one copy per 16-row box moves all its pieces ([piece][16 rows]);
+            // with 8-row blocks one per half box ([half][piece][8 rows])
+            const int v_box = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
+            const bool has = v_box < kBoxes;
+            int jt = rot, phys_next = box_block(rot, v_box, half, has), issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % NV, phys = phys_next, jc = jt;
                 jt = jt + 1 == ntiles ? 0 : jt + 1;
-                if (j + 1 < ntiles) phys_next = box_block(jt, v_box, has);
+                if (j + 1 < ntiles) phys_next = box_block(jt, v_box, half, has);
                 const uint32_t vdst = vstage0 + st * C::kTileBytes;
                 const bool last = jc == ntiles - 1;   // the context's tail tile
                 const uint32_t vbar = last ? vtail : v_full + st * 8;
@@ -601,8 +610,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 __syncwarp();
                 // the V map has the row ahead of the piece: (element, row, piece, head, block)
                 if (has && jc * kBoxes + v_box < nbox)
-                    tma_load_5d(vdst + v_box * C::kVBox, &tmV, vbar, 0,
-                                ((jc * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, phys);
+                    tma_load_5d(vdst + v_box * C::kVBox + half * (C::kPieces * 1024), &tmV, vbar, 0,
+                                b8 ? 0 : ((jc * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, phys);
                 issued = j + 1;
                 if (last) {
                     // V rows at or past kv_end hold cache data past the context (or
@@ -617,9 +626,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     for (int e = lane; e < nchunks; e += 32) {
                         const int r = first_row + e / (C::kPieces * 8);
                         const int c = (e / 8) % C::kPieces;
-                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox +
-                                                   c * 2048 + (r & 15) * 128 + (e & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        const int off = b8 ? ((r >> 3) & 1) * (C::kPieces * 1024) + c * 1024 + (r & 7) * 128
+                                           : c * 2048 + (r & 15) * 128;
+                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox + off +
+                                                   (e & 7) * 16) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -651,6 +661,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         constexpr uint32_t kAll = 0xffffffffu;
         constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
         constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
+        // V's MN-major layout per 16-token box: pieces 2 KB apart and 8-row groups
+        // 1 KB apart ([piece][16 rows]), or with 8-row blocks pieces 1 KB apart and
+        // the two halves kPieces KB apart ([half][piece][8 rows])
+        const bool b8 = p.block_size < kTile;
+        const uint32_t v_lbo = b8 ? 1024u : 2048u, v_sbo = b8 ? C::kPieces * 1024u : 1024u;
         bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
         auto wait = [&](uint32_t bar, uint32_t parity) {
             ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
@@ -685,7 +700,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 tc05::mma_ts_elect(tcol + C::kOCol,
                                    tcol + (j % SB) * N +
                                        ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
-                                   tc05::sw128_desc(vst + kt * C::kVBox, 2048, 1024), idesc_pv,
+                                   tc05::sw128_desc(vst + kt * C::kVBox, v_lbo, v_sbo), idesc_pv,
                                    (j > 0 || kt > 0) ? 1u : 0u);
             if (kt1 < N / 16) return;
             // s_free: with one S buffer the commit of the QK issued next (S_{j+1})

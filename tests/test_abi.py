@@ -260,7 +260,8 @@ def _prefill(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(D=32), -2),                 # head_dim not supported by the prefill kernel
     (dict(D=96), -2),
-    (dict(bs=8), -2),                 # block_size not a multiple of 16
+    (dict(bs=24), -2),                # block_size neither 8 nor a multiple of 16
+    (dict(bs=4), -2),
     (dict(Hq=256, Hkv=1), -2),        # more than 128 query heads per KV head
     (dict(Hq=10, Hkv=4), -1),         # Hq not a multiple of Hkv
     (dict(R=-1), -1),

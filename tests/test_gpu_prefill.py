@@ -38,6 +38,12 @@ SHAPES = [
     # a long context walked by several pairs of one sequence
     ([50, 3], [5, 2], 128, 1, 256, 16, torch.bfloat16),
     ([5000], [300], 4, 2, 256, 16, torch.float16),
+    # block_size 8: each 16-token box is two blocks; contexts ending inside a
+    # block, on a block edge and on a box edge
+    ([0, 8, 9, 1000], [37, 1, 300, 65], 24, 4, 128, 8, torch.bfloat16),
+    ([100, 7, 23], [77, 30, 1], 32, 4, 64, 8, torch.float16),
+    ([300, 15], [45, 2], 16, 2, 256, 8, torch.bfloat16),
+    ([2000, 24], [129, 8], 8, 1, 256, 8, torch.float16),
 ]
 IDS = [f"d{s[4]}_g{s[2] // s[3]}_bs{s[5]}_{str(s[6])[6:]}" for s in SHAPES]
 
@@ -96,13 +102,14 @@ def test_one_row_chunks_equal_decode(pa):
     assert pa.device_status() == 0
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
-def test_nan_past_the_context_is_never_used(pa, D):
+@pytest.mark.parametrize("D,bs", [(64, 32), (128, 32), (256, 32), (64, 8), (128, 8), (256, 8)])
+def test_nan_past_the_context_is_never_used(pa, D, bs):
     """Cache rows past each sequence's last token (and unused blocks) hold NaN:
     the masked logits and the zeroed V rows of the last stage keep them out
-    (on single CTAs at head_dim 64 and 128, on CTA pairs at 256)."""
-    w = _workload(16, 2, D, 32, torch.float16)
-    host = make_prefill_case(w, ctx_lens=[7, 100, 33], q_lens=[20, 61, 1], seed=3200 + D)
+    (on single CTAs at head_dim 64 and 128, on CTA pairs at 256; with 8-token
+    blocks a box half past the context is read as zeros)."""
+    w = _workload(16, 2, D, bs, torch.float16)
+    host = make_prefill_case(w, ctx_lens=[7, 100, 33], q_lens=[20, 61, 1], seed=3200 + D + bs)
     kc, vc = host.case.key_cache.clone(), host.case.value_cache.clone()
     bs = kc.shape[1]
     used = torch.zeros(kc.shape[0], dtype=torch.bool)
@@ -121,11 +128,11 @@ def test_nan_past_the_context_is_never_used(pa, D):
     assert pa.device_status() == 0
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
-def test_block_permutation_gives_identical_bits(pa, D):
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 16), (256, 16), (128, 8), (256, 8)])
+def test_block_permutation_gives_identical_bits(pa, D, bs):
     """Which physical block holds a page does not change a single output bit."""
-    w = _workload(24 if D == 128 else 16, 4 if D < 256 else 2, D, 16, torch.bfloat16)
-    host = make_prefill_case(w, ctx_lens=[300, 50], q_lens=[80, 40], seed=3300 + D)
+    w = _workload(24 if D == 128 else 16, 4 if D < 256 else 2, D, bs, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[300, 50], q_lens=[80, 40], seed=3300 + D + bs)
     dev = host.to("cuda")
     out1 = _run(pa, dev)
     nb = dev.case.key_cache.shape[0]
@@ -295,7 +302,8 @@ def test_prefill_running_max_rescales(pa, D, rate, spike):
     assert_out_close(out, _oracle(host), f"rescaled prefill D={D} rate={rate} spike={spike}")
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,bs", [(64, 32, 4, 16), (128, 24, 4, 48), (256, 16, 2, 32)])
+@pytest.mark.parametrize("D,Hq,Hkv,bs", [(64, 32, 4, 16), (128, 24, 4, 48), (256, 16, 2, 32),
+                                         (128, 24, 4, 8), (256, 16, 2, 8)])
 def test_repeated_launches_are_bit_identical(pa, D, Hq, Hkv, bs):
     """The MMA order and the softmax are fixed, so every launch gives the same
     bits: a race in the producer / MMA / softmax hand-offs would show as an
