@@ -106,23 +106,25 @@ int make_cache_map(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, i
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-// 5-D view of a cache with the row in the block ahead of the piece: (element
-// within a 64-element piece, row in block, piece, KV head, block); one box =
-// `pieces` consecutive 64-element pieces of 16 rows of one KV head (8 rows for
-// block_size 8), landing piece after piece ([piece][rows][128 B], 128-byte
-// swizzled), so one copy moves several pieces of a block.  Used for the V
-// tiles of the prefill kernels.
-int make_cache_map_pieces(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv,
+// 5-D view of a cache as 8-token groups: (element within a 64-element piece,
+// row in the group, piece, KV head, group), group g holding the cache's rows
+// 8 g .. 8 g + 7 counted across blocks (block b, row r: g = b * bs / 8 + r / 8;
+// bs a multiple of 8).  One box = `pieces` consecutive pieces of `groups`
+// consecutive groups of one KV head, landing as [group][piece][8 rows][128 B]
+// (128-byte swizzled): the operand layout of the prefill kernels, a uniform
+// stride of `pieces` KB between 8-token groups.  Two groups (16 tokens of one
+// block) per copy when bs is a multiple of 16, one with block_size 8.
+// Out-of-range boxes read zeros.
+int make_cache_map_groups(CUtensorMap *m, const void *cache, pa_dtype_t dtype, int D, int Hkv,
                           int bs, int num_blocks, int pieces) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return PA_ERR_NO_DEVICE;
     const cuuint64_t e = 2;
-    cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(D / 64),
-                          static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
-    cuuint64_t strides[4] = {static_cast<cuuint64_t>(Hkv) * D * e, 64 * e, D * e,
-                             static_cast<cuuint64_t>(bs) * Hkv * D * e};
-    const cuuint32_t rows = static_cast<cuuint32_t>(bs < kTile ? bs : kTile);
-    cuuint32_t box[5] = {64, rows, static_cast<cuuint32_t>(pieces), 1, 1};
+    const cuuint64_t row = static_cast<cuuint64_t>(Hkv) * D * e;   // bytes between cache rows
+    cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(Hkv),
+                          static_cast<cuuint64_t>(num_blocks) * (bs / 8)};
+    cuuint64_t strides[4] = {row, 64 * e, D * e, 8 * row};
+    cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(pieces), 1, bs % kTile == 0 ? 2u : 1u};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -892,6 +894,8 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     if (group > kPrefillRows) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;
+    // the 8-token group coordinate of the cache views is a 32-bit int
+    if (static_cast<int64_t>(num_blocks) * (block_size / 8) > INT_MAX) return PA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(num_rows) * num_q_heads * head_dim > (static_cast<int64_t>(1) << 40))
         return PA_ERR_INVALID_ARGUMENT;
     if (num_seqs == 0 || num_rows == 0 || max_q_len == 0) return PA_OK;
@@ -905,12 +909,12 @@ int pa_prefill(void *out, const void *query, const void *key_cache, const void *
     DevInfo *di = nullptr;
     int rc = device_info(&di);
     if (rc != PA_OK) return rc;
+    // K and V move one 16-token box per copy (every piece of it a CTA holds)
     CUtensorMap tk, tv;
-    if ((rc = make_cache_map(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
-                             num_blocks)) != PA_OK)
+    if ((rc = make_cache_map_groups(&tk, key_cache, dtype, head_dim, num_kv_heads, block_size,
+                                    num_blocks, head_dim / 64)) != PA_OK)
         return rc;
-    // V tiles move one 16-token box (all of a CTA's pieces of it) per copy
-    if ((rc = make_cache_map_pieces(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
+    if ((rc = make_cache_map_groups(&tv, value_cache, dtype, head_dim, num_kv_heads, block_size,
                                     num_blocks, prefill_v_box_pieces(head_dim))) != PA_OK)
         return rc;
     PrefillParams p{};

@@ -28,9 +28,8 @@ cudaError_t launch_prefill_tc(int D, const CUtensorMap &tmQ, const CUtensorMap &
 
 // Query rows (chunk token x group head) one prefill CTA covers at head_dim D.
 int prefill_rows_per_cta(int D);
-// 64-column pieces of a 16-token V box one prefill copy moves at head_dim D
-// (the V map has the row ahead of the piece): every piece of the row on single
-// CTAs, the CTA's half on CTA pairs.
+// 64-column pieces of a 16-token V box one prefill copy moves at head_dim D:
+// every piece of the row on single CTAs, the CTA's half on CTA pairs.
 int prefill_v_box_pieces(int D);
 
 cudaError_t launch_plan(const PlanParams &pp, cudaStream_t st);

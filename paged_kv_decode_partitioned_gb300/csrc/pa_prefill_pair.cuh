@@ -77,11 +77,13 @@ struct PrefillPairCfg {
     static constexpr int kQPiece = kRows * 128;
     static constexpr int kQTileBytes = 128 * 128;     // one Q tile's rows in a piece
     static constexpr int kQBytes = kPieces * kQPiece;
-    static constexpr int kKPiece = kHalfN * 128;      // K-major: 64 token rows
-    // V (MN-major) lands one 16-token box at a time, the CTA's kVPieces pieces
-    // of the box after one another: [box][piece][16 rows][128 B]
+    // K and V land one 16-token box per copy as 8-token groups, the CTA's
+    // pieces of each group after one another: [group][piece][8 rows][128 B]
+    // (128-byte swizzled); K holds every piece of the CTA's 64 tokens (read
+    // K-major), V the CTA's kVPieces pieces of all 128 tokens (MN-major)
+    static constexpr int kKBoxBytes = kPieces * 2048;
     static constexpr int kVBoxBytes = kVPieces * 2048;
-    static constexpr int kKBytes = kPieces * kKPiece;
+    static constexpr int kKBytes = (kHalfN / 16) * kKBoxBytes;
     static constexpr int kVBytes = (kN / 16) * kVBoxBytes;
     static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kStages = D == 128 ? 4 : 2;
@@ -256,31 +258,34 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
         // ~9 % at head_dim 128 on single CTAs)
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
-        constexpr int kKOps = 4 * C::kPieces;    // this CTA's 4 boxes of K x pieces
-        constexpr int kVOps = 8;                 // all 8 boxes of V, this CTA's pieces in one copy
-        static_assert(2 * kKOps <= 32 && 2 * kVOps <= 32, "one copy per lane");
+        constexpr int kKOps = 4;   // this CTA's 4 boxes of K, every piece in one copy
+        constexpr int kVOps = 8;   // all 8 boxes of V, this CTA's pieces in one copy
         const bool lead = rank == 0;
-        // block_size 8: a 16-token box is two 8-row blocks, a copy each (lane
+        // block_size 8: a 16-token box spans two blocks, a copy each (lane
         // pairs take the two halves of one box)
         const bool b8 = p.block_size < kTile;
         const int op = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
-        const int k_box = 4 * static_cast<int>(rank) + (op % kKOps) / C::kPieces;
-        const int k_piece = (op % kKOps) % C::kPieces;
+        const int k_box = 4 * static_cast<int>(rank) + op % kKOps;
         const int v_box = op % kVOps;
         const int v_piece = static_cast<int>(rank) * C::kVPieces;   // first piece of the box
-        // block of this lane's K (V) box (half) of tile jt, read a tile ahead and
-        // checked only when the copy is issued; -1 (a box of zeros) for a half
-        // past the context
+        auto first_token = [&](int jt, int box) { return (jt * (N / kTile) + box) * kTile + half * (kTile / 2); };
+        // block of this lane's K (V) box (half) of tile jt (0 when the lane has
+        // no copy or the half lies past the context), read a tile ahead and
+        // checked only when the copy is issued
         auto block_of = [&](int jt, int box, bool has) -> int {
-            const int bx = jt * (N / kTile) + box;
-            if (!has || bx >= nbox) return 0;
-            const int tok = bx * kTile + half * (kTile / 2);
-            if (b8 && tok >= kv_end) return -1;
-            return __ldg(bt_row + tok / p.block_size);
+            const int tok = first_token(jt, box);
+            return has && tok < kv_end ? __ldg(bt_row + tok / p.block_size) : 0;
         };
-        auto check_block = [&](int b) {
-            if (b != -1 && static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
-                atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
+        // the copy's 8-token group coordinate; -1 (a box of zeros) for a half
+        // past the context or a block outside the cache (that one flagged)
+        auto group_of = [&](int jt, int box, int b) -> int {
+            const int tok = first_token(jt, box);
+            if (tok >= kv_end) return -1;
+            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks)) {
+                atomicOr(p.status, kBadBlock);
+                return -1;
+            }
+            return b * (p.block_size >> 3) + ((tok % p.block_size) >> 3);
         };
         // the even CTA's barrier at the same offset (this CTA's own in the even CTA)
         auto lead_bar = [&](uint32_t bar) -> uint32_t { return lead ? bar : dsmem_addr(bar, 0); };
@@ -332,15 +337,15 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NS) - 1) & 1u);
                 if (!__all_sync(0xffffffffu, w)) return false;
             }
-            if (k_has) check_block(kb);
             if (lead && lane == 0)   // both CTAs' K halves
                 mbar_expect_tx(k_full + st * 8, static_cast<uint32_t>(boxes_of(jt) * C::kPieces * 2048));
             __syncwarp();
             if (k_has && jt * (N / kTile) + k_box < nbox)
-                tma_load_5d_pair(stage0 + st * C::kStageBytes + k_piece * C::kKPiece +
-                                     (k_box - 4 * static_cast<int>(rank)) * 2048 + half * 1024,
-                                 &tmK, lead_bar(k_full + st * 8), 0, k_piece, kvh,
-                                 b8 ? 0 : ((jt * (N / kTile) + k_box) * kTile) % p.block_size, kb);
+                // the cache maps: (element, row in group, piece, head, group)
+                tma_load_5d_pair(stage0 + st * C::kStageBytes +
+                                     (k_box - 4 * static_cast<int>(rank)) * C::kKBoxBytes +
+                                     half * (C::kPieces * 1024),
+                                 &tmK, lead_bar(k_full + st * 8), 0, 0, 0, kvh, group_of(jt, k_box, kb));
             k_issued = j + 1;
             return true;
         };
@@ -355,7 +360,6 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 const bool w = mbar_wait_cycles(v_empty + st * 8, ((j / NS) - 1) & 1u);
                 if (!__all_sync(0xffffffffu, w)) return false;
             }
-            if (v_has) check_block(vb);
             // the tail tile's V lands on this CTA's own vtail, to be zeroed past
             // the context before the MMA may read it
             const uint32_t vbar = last ? vtail : lead_bar(v_full + st * 8);
@@ -367,11 +371,8 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             }
             __syncwarp();
             if (v_has && jt * (N / kTile) + v_box < nbox)
-                // the V map has the row ahead of the piece: (element, row, piece, head, block)
-                // ([piece][16 rows] per box; [half][piece][8 rows] with 8-row blocks)
-                tma_load_5d_pair(vdst + v_box * C::kVBoxBytes + half * (C::kVPieces * 1024), &tmV, vbar, 0,
-                                 b8 ? 0 : ((jt * (N / kTile) + v_box) * kTile) % p.block_size, v_piece,
-                                 kvh, vb);
+                tma_load_5d_pair(vdst + v_box * C::kVBoxBytes + half * (C::kVPieces * 1024), &tmV, vbar,
+                                 0, 0, v_piece, kvh, group_of(jt, v_box, vb));
             issued = j + 1;
             if (last) {
                 const bool w = mbar_wait_cycles(vtail, 0);
@@ -381,10 +382,9 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                 for (int e = lane; e < nchunks; e += 32) {
                     const int r = first_row + e / (C::kVPieces * 8);
                     const int c = (e / 8) % C::kVPieces;
-                    const int off = b8 ? ((r >> 3) & 1) * (C::kVPieces * 1024) + c * 1024 + (r & 7) * 128
-                                       : c * 2048 + (r & 15) * 128;
-                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBoxBytes + off +
-                                               (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 3) * (C::kVPieces * 1024) +
+                                               c * 1024 + (r & 7) * 128 + (e & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -427,10 +427,6 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
             constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 256);
             constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 256);
             constexpr uint16_t kBoth = 0x3;
-            // V per 16-token box: pieces 2 KB apart, 8-row groups 1 KB apart; with
-            // 8-row blocks pieces 1 KB apart, the halves kVPieces KB apart
-            const bool b8 = p.block_size < kTile;
-            const uint32_t v_lbo = b8 ? 1024u : 2048u, v_sbo = b8 ? C::kVPieces * 1024u : 1024u;
             bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
             auto wait = [&](uint32_t bar, uint32_t parity) {
                 ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
@@ -447,7 +443,7 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     tc05::mma2_ss_elect(
                         tcol + (j % SB) * N,
                         tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
-                        tc05::sw128_desc(kst + (kk >> 2) * C::kKPiece + (kk & 3) * 32, 16, 1024),
+                        tc05::sw128_desc(kst + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kPieces * 1024),
                         idesc_qk, kk > 0 ? 1u : 0u);
                 tc05::commit2_elect(tb + (j % SB) * 8, kBoth);   // s_full
                 if (t == nq - 1) tc05::commit2_elect(k_empty + (j % NS) * 8, kBoth);
@@ -463,7 +459,7 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
                     // occupies the first half of that half's S columns
                     tc05::mma2_ts_elect(tcol + C::kOCol,
                                         tcol + (j % SB) * N + ((16 * kt) / HC) * (HC / 2) + kt * 8,
-                                        tc05::sw128_desc(vst + kt * C::kVBoxBytes, v_lbo, v_sbo),
+                                        tc05::sw128_desc(vst + kt * C::kVBoxBytes, 1024, C::kVPieces * 1024),
                                         idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
                 // s_free: with one S buffer the commit of the QK issued next
                 // (S_{j+1}) tracks this PV as well, so none is needed

@@ -117,13 +117,12 @@ struct PrefillTcCfg {
     static constexpr int kPieces = D / 64;
     static constexpr int kQPiece = kRows * 128;                  // bytes of one Q piece
     static constexpr int kQTileBytes = 128 * 128;                // one Q tile's rows in a piece
-    static constexpr int kKvPiece = kN * 128;                    // bytes of one K (V) piece
     static constexpr int kQBytes = kPieces * kQPiece;
-    static constexpr int kTileBytes = kPieces * kKvPiece;        // K (or V) of one stage
-    // K lands piece by piece ([piece][N rows][128 B], the K-major operand);
-    // V one 16-token box at a time with all its pieces ([box][piece][16 rows]
-    // [128 B], the MN-major operand), one copy per box
-    static constexpr int kVBox = kPieces * 2048;
+    // K and V land one 16-token box per copy, all its pieces, as 8-token
+    // groups: [group][piece][8 rows][128 B] (128-byte swizzled), a uniform
+    // group stride of kPieces KB for both operands (K read K-major, V MN-major)
+    static constexpr int kBoxBytes = kPieces * 2048;
+    static constexpr int kTileBytes = (kN / 16) * kBoxBytes;     // K (or V) of one stage
     static constexpr int kKOffset = kQBytes;                          // K stages
     static constexpr int kVOffset = kKOffset + kKStages * kTileBytes;   // V stages
     static constexpr int kBarOffset = kVOffset + kVStages * kTileBytes;
@@ -502,25 +501,32 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         const int32_t *bt_row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int nbox = (kv_end + kTile - 1) / kTile;
         constexpr int kBoxes = N / kTile;   // 16-token boxes per tile
-        constexpr int kOps = kBoxes * C::kPieces;   // copies per K tile (twice with 8-row blocks)
-        static_assert(2 * kOps <= 32, "one copy per lane");
-        // block_size 8: a 16-token box is two 8-row blocks, one copy each
+        static_assert(2 * kBoxes <= 32, "one copy per lane");
+        // Each producer lane copies one 16-token box of a tile, all its pieces;
+        // with block_size 8 a box spans two blocks, and lane pairs copy its halves.
         const bool b8 = p.block_size < kTile;
+        const int op_box = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
+        const bool has = op_box < kBoxes;
+        auto first_token = [&](int jt) { return (jt * kBoxes + op_box) * kTile + half * (kTile / 2); };
         // block of this lane's box (half) of tile jt (0 when the lane has no
-        // copy; -1, an out-of-range box of zeros, for a half past the context).
-        // The read goes out a tile ahead and is checked only when the copy is
-        // issued, so its latency overlaps the stage waits in between (with one
-        // stage, a read consumed at once put ~3000 cycles on every tile's K load).
-        auto box_block = [&](int jt, int box, int half, bool has) -> int {
-            const int bx = jt * kBoxes + box;
-            if (!has || bx >= nbox) return 0;
-            const int tok = bx * kTile + half * (kTile / 2);
-            if (b8 && tok >= kv_end) return -1;
-            return __ldg(bt_row + tok / p.block_size);
+        // copy or the half lies past the context).  The read goes out a tile
+        // ahead and is checked only when the copy is issued, so its latency
+        // overlaps the stage waits in between (with one stage, a read consumed
+        // at once put ~3000 cycles on every tile's K load).
+        auto box_block = [&](int jt) -> int {
+            const int tok = first_token(jt);
+            return has && tok < kv_end ? __ldg(bt_row + tok / p.block_size) : 0;
         };
-        auto check_block = [&](int b) {
-            if (b != -1 && static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks))
-                atomicOr(p.status, kBadBlock);   // the TMA reads zeros there
+        // the copy's 8-token group coordinate; -1 (a box of zeros) for a half
+        // past the context or a block outside the cache (that one flagged)
+        auto group_of = [&](int jt, int b) -> int {
+            const int tok = first_token(jt);
+            if (tok >= kv_end) return -1;
+            if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks)) {
+                atomicOr(p.status, kBadBlock);
+                return -1;
+            }
+            return b * (p.block_size >> 3) + ((tok % p.block_size) >> 3);
         };
         // bytes of tile jt's boxes inside the context (K or V: the same)
         auto tile_bytes = [&](int jt) {
@@ -548,16 +554,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 for (int c = 0; c < C::kPieces; ++c)
                     tma_load_4d(q_smem + c * C::kQPiece, &tmQ, q_full, 0, c, kvh * g, row0 + tok0);
             }
-            // K: one copy per (16-row box, 64-element piece) and lane; with
-            // 8-row blocks one per (box, piece, half)
-            const int q = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
-            const int op_box = (q % kOps) / C::kPieces, op_piece = (q % kOps) % C::kPieces;
-            const bool has = q < kOps;
-            int jt = rot, phys_next = box_block(rot, op_box, half, has), issued = 0;
+            int jt = rot, phys_next = box_block(rot), issued = 0;
             for (int j = 0; j < ntiles; ++j) {   // j: order of use, jt: tile of the context
                 const int st = j % NK, phys = phys_next, jc = jt;
                 jt = jt + 1 == ntiles ? 0 : jt + 1;
-                if (j + 1 < ntiles) phys_next = box_block(jt, op_box, half, has);   // next tile's entry
+                if (j + 1 < ntiles) phys_next = box_block(jt);   // next tile's entry
                 // K of tile j once every QK of tile j - NK is done
                 if (j >= NK) {
                     const bool w = mbar_wait_cycles(k_empty + st * 8, ((j / NK) - 1) & 1u);
@@ -566,16 +567,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                         break;
                     }
                 }
-                check_block(phys);
                 // one copy per lane: a single thread issuing them back to back is
                 // bound by the issue latency of each copy, not by the TMA engine
                 if (lane == 0) mbar_expect_tx(k_full + st * 8, tile_bytes(jc));
                 __syncwarp();
+                // the cache maps: (element, row in group, piece, head, group)
                 if (has && jc * kBoxes + op_box < nbox)
-                    tma_load_5d(kstage0 + st * C::kTileBytes + op_piece * C::kKvPiece + op_box * 2048 +
-                                    half * 1024,
-                                &tmK, k_full + st * 8, 0, op_piece, kvh,
-                                b8 ? 0 : ((jc * kBoxes + op_box) * kTile) % p.block_size, phys);
+                    tma_load_5d(kstage0 + st * C::kTileBytes + op_box * C::kBoxBytes +
+                                    half * (C::kPieces * 1024),
+                                &tmK, k_full + st * 8, 0, 0, 0, kvh, group_of(jc, phys));
                 issued = j + 1;
             }
             if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
@@ -585,15 +585,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             for (int j = issued > NK ? issued - NK : 0; j < issued; ++j)
                 (void)mbar_wait_cycles(k_full + (j % NK) * 8, (j / NK) & 1u);
         } else {
-            // V: one copy per 16-row box moves all its pieces ([piece][16 rows]);
-            // with 8-row blocks one per half box ([half][piece][8 rows])
-            const int v_box = b8 ? lane >> 1 : lane, half = b8 ? lane & 1 : 0;
-            const bool has = v_box < kBoxes;
-            int jt = rot, phys_next = box_block(rot, v_box, half, has), issued = 0;
+            int jt = rot, phys_next = box_block(rot), issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % NV, phys = phys_next, jc = jt;
                 jt = jt + 1 == ntiles ? 0 : jt + 1;
-                if (j + 1 < ntiles) phys_next = box_block(jt, v_box, half, has);
+                if (j + 1 < ntiles) phys_next = box_block(jt);
                 const uint32_t vdst = vstage0 + st * C::kTileBytes;
                 const bool last = jc == ntiles - 1;   // the context's tail tile
                 const uint32_t vbar = last ? vtail : v_full + st * 8;
@@ -605,13 +601,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                         break;
                     }
                 }
-                check_block(phys);
                 if (lane == 0) mbar_expect_tx(vbar, tile_bytes(jc));
                 __syncwarp();
-                // the V map has the row ahead of the piece: (element, row, piece, head, block)
-                if (has && jc * kBoxes + v_box < nbox)
-                    tma_load_5d(vdst + v_box * C::kVBox + half * (C::kPieces * 1024), &tmV, vbar, 0,
-                                b8 ? 0 : ((jc * kBoxes + v_box) * kTile) % p.block_size, 0, kvh, phys);
+                if (has && jc * kBoxes + op_box < nbox)
+                    tma_load_5d(vdst + op_box * C::kBoxBytes + half * (C::kPieces * 1024), &tmV, vbar,
+                                0, 0, 0, kvh, group_of(jc, phys));
                 issued = j + 1;
                 if (last) {
                     // V rows at or past kv_end hold cache data past the context (or
@@ -626,10 +620,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                     for (int e = lane; e < nchunks; e += 32) {
                         const int r = first_row + e / (C::kPieces * 8);
                         const int c = (e / 8) % C::kPieces;
-                        const int off = b8 ? ((r >> 3) & 1) * (C::kPieces * 1024) + c * 1024 + (r & 7) * 128
-                                           : c * 2048 + (r & 15) * 128;
-                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 4) * C::kVBox + off +
-                                                   (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(smem + (vdst - base) + (r >> 3) * (C::kPieces * 1024) +
+                                                   c * 1024 + (r & 7) * 128 + (e & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -661,11 +654,6 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         constexpr uint32_t kAll = 0xffffffffu;
         constexpr uint32_t idesc_qk = tc05::f16_idesc(TcType<T>::code, 0, 0, N, 128);
         constexpr uint32_t idesc_pv = tc05::f16_idesc(TcType<T>::code, 0, 1, D, 128);
-        // V's MN-major layout per 16-token box: pieces 2 KB apart and 8-row groups
-        // 1 KB apart ([piece][16 rows]), or with 8-row blocks pieces 1 KB apart and
-        // the two halves kPieces KB apart ([half][piece][8 rows])
-        const bool b8 = p.block_size < kTile;
-        const uint32_t v_lbo = b8 ? 1024u : 2048u, v_sbo = b8 ? C::kPieces * 1024u : 1024u;
         bool ok = __all_sync(kAll, mbar_wait_cycles(q_full, 0));
         auto wait = [&](uint32_t bar, uint32_t parity) {
             ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
@@ -682,7 +670,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 tc05::mma_ss_elect(
                     tcol + (j % SB) * N,
                     tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
-                    tc05::sw128_desc(kst + (kk >> 2) * C::kKvPiece + (kk & 3) * 32, 16, 1024),
+                    tc05::sw128_desc(kst + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kPieces * 1024),
                     idesc_qk, kk > 0 ? 1u : 0u);
             tc05::commit_elect(tb + (j % SB) * 8);   // s_full
             if (t == nq - 1) tc05::commit_elect(k_empty + (j % NK) * 8);
@@ -700,8 +688,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
                 tc05::mma_ts_elect(tcol + C::kOCol,
                                    tcol + (j % SB) * N +
                                        ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
-                                   tc05::sw128_desc(vst + kt * C::kVBox, v_lbo, v_sbo), idesc_pv,
-                                   (j > 0 || kt > 0) ? 1u : 0u);
+                                   tc05::sw128_desc(vst + kt * C::kBoxBytes, 1024, C::kPieces * 1024),
+                                   idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
             if (kt1 < N / 16) return;
             // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
             // tracks this PV as well, so none is needed

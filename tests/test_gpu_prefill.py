@@ -150,6 +150,26 @@ def test_block_permutation_gives_identical_bits(pa, D, bs):
     assert pa.device_status() == 0
 
 
+@pytest.mark.parametrize("bad", ["negative", "past_the_cache"])
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 8), (128, 32), (256, 16), (256, 8)])
+def test_bad_table_entry_raises_flag(pa, D, bs, bad):
+    """A block-table entry inside the context outside [0, num_blocks) raises
+    PA_DEV_BAD_BLOCK; its rows read as zeros and the output stays finite."""
+    w = _workload(16, 2, D, bs, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[200, 60], q_lens=[40, 30], seed=3800 + D + bs)
+    dev = host.to("cuda")
+    c = dev.case
+    out = _run(pa, dev)
+    assert pa.device_status() == 0
+    bt = c.block_tables.clone()
+    bt[0, 3] = -1 if bad == "negative" else c.key_cache.shape[0] + 5
+    out = pa.prefill(dev.query, c.key_cache, c.value_cache, bt, c.seq_lens, dev.q_start, c.scale,
+                     max(dev.q_lens))
+    assert pa.device_status() & pa.DEV_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    assert pa.device_status() == 0
+
+
 def _sampled_rows_check(pa, host, dev, out, rows_per_seq, seed):
     """Compare sampled rows with the oracle's decode over the row's visible prefix."""
     c = host.case
