@@ -84,9 +84,20 @@ namespace pa {
 #ifndef PA_PREFILL_HALFP_D128
 #define PA_PREFILL_HALFP_D128 0
 #endif
-// K/V tile width at head_dim 64 (128 at head_dim 128).
+// K/V tile width per head_dim.
 #ifndef PA_PREFILL_N_D64
 #define PA_PREFILL_N_D64 192
+#endif
+#ifndef PA_PREFILL_N_D128
+#define PA_PREFILL_N_D128 128
+#endif
+// S buffers in tensor memory per Q tile, per head_dim (with two, a Q tile's
+// next QK runs under its softmax; 2 x (2 N + head_dim) columns must fit 512).
+#ifndef PA_PREFILL_SBUFS_D64
+#define PA_PREFILL_SBUFS_D64 1
+#endif
+#ifndef PA_PREFILL_SBUFS_D128
+#define PA_PREFILL_SBUFS_D128 1
 #endif
 // Whole rows of at most 128 columns hold their S in registers between the passes.
 #ifndef PA_PREFILL_REGROW
@@ -108,8 +119,9 @@ template <int D>
 struct PrefillTcCfg {
     static constexpr int kQTiles = D <= 128 ? 2 : 1;
     static constexpr int kRows = 128 * kQTiles;                  // query rows per CTA
-    static constexpr int kN = D <= 64 ? PA_PREFILL_N_D64 : 128;   // cache tokens per tile
-    static constexpr int kSBufs = kQTiles == 2 ? 1 : 2;          // S buffers per Q tile
+    static constexpr int kN = D <= 64 ? PA_PREFILL_N_D64 : (D <= 128 ? PA_PREFILL_N_D128 : 128);   // cache tokens per tile
+    static constexpr int kSBufs =
+        kQTiles == 2 ? (D <= 64 ? PA_PREFILL_SBUFS_D64 : PA_PREFILL_SBUFS_D128) : 2;   // S buffers per Q tile
     // K and V stages (their own producers and barriers; a third K stage at
     // head_dim 128 or a fourth at head_dim 64 measured no faster)
     static constexpr int kKStages = D <= 64 ? PA_PREFILL_KSTAGES_D64 : (D <= 128 ? PA_PREFILL_KSTAGES_D128 : 1);
