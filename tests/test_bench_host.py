@@ -120,3 +120,17 @@ def test_whole_job_rates():
     assert ms == 10.0
     assert gbs == pytest.approx(500.0)
     assert tok == pytest.approx(25600.0)
+
+
+def test_prefill_sweep_flops_and_table():
+    """The sweep tool's FLOP count agrees with the bench's brute-force-checked one,
+    and its table has one row per shape and one column per batch."""
+    from paged_kv_decode_partitioned_gb300 import prefill_sweep as ps
+    for s, n, c in ps.BATCHES:
+        assert ps.flops(s, n, c, 24, 128) == bench.prefill_flops([c] * s, [n] * s, 24, 128)
+    rows = [{"head_dim": d, "num_q_heads": 8, "num_kv_heads": 2, "block_size": 16, "seqs": s,
+             "chunk": n, "ctx": c, "ms": 1.0, "tflops": 1.0}
+            for d in (64, 128) for s, n, c in ps.BATCHES[:2]]
+    lines = ps.table(rows).splitlines()
+    assert len(lines) == 2 + 2
+    assert all(line.count("|") == 3 + 2 + 1 for line in lines)
