@@ -208,7 +208,10 @@ __global__ void __launch_bounds__(PrefillPairCfg<D>::kThreads, 1)
     const int pair_end = min(n, (2 * qp + 2) * tpc);
     const int kv_end = L - n + pair_end;   // cache tokens any row of the pair sees
     const int ntiles = (kv_end + N - 1) / N;
-    const int rot = static_cast<int>((static_cast<unsigned>(qp) * 37u) % static_cast<unsigned>(ntiles));
+    const int rot = static_cast<int>(gridDim.x / 2) >= PA_PREFILL_ROT_MIN_CTAS
+                        ? static_cast<int>((static_cast<unsigned>(qp) * PA_PREFILL_ROT_STEP_PAIR) %
+                                           static_cast<unsigned>(ntiles))
+                        : 0;
     const int pos_first = L - n + tok0;
     const int rows_used = g * ntok;
     const int j_tail = ntiles - 1 - rot;   // use order of the context's tail tile

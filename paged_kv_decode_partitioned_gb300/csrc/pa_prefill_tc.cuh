@@ -99,6 +99,34 @@ namespace pa {
 #ifndef PA_PREFILL_SBUFS_D128
 #define PA_PREFILL_SBUFS_D128 1
 #endif
+// A CTA with one Q tile of rows takes the idle tile's tensor memory as a second
+// S buffer when its (sequence, KV head) has at most DUAL_MAX_CTAS CTAs: one query
+// head per KV head with 128-token chunks over 32K ran 750 -> 850 TFLOP/s; where
+// the CTA shares its (sequence, KV head) with full ones (GQA 6, 128-token chunks)
+// the faster walk cost the others more than it saved (1010 -> 775).
+#ifndef PA_PREFILL_DUAL
+#define PA_PREFILL_DUAL 1
+#endif
+#ifndef PA_PREFILL_DUAL_MAX_CTAS
+#define PA_PREFILL_DUAL_MAX_CTAS 1
+#endif
+// The CTAs of one (sequence, KV head) start their context walk ROT_STEP tiles
+// apart (per head_dim; 0: all at tile 0) when there are at least ROT_MIN_CTAS.
+// At head_dim 128 the walks in step share each K/V tile's fetch through L2
+// (+1-6 % over walks 37 tiles apart); at head_dim 64 the spread walks measured
+// 3 % faster, and on CTA pairs the two are alike.
+#ifndef PA_PREFILL_ROT_STEP_D64
+#define PA_PREFILL_ROT_STEP_D64 37
+#endif
+#ifndef PA_PREFILL_ROT_STEP_D128
+#define PA_PREFILL_ROT_STEP_D128 0
+#endif
+#ifndef PA_PREFILL_ROT_STEP_PAIR
+#define PA_PREFILL_ROT_STEP_PAIR 37
+#endif
+#ifndef PA_PREFILL_ROT_MIN_CTAS
+#define PA_PREFILL_ROT_MIN_CTAS 0
+#endif
 // Whole rows of at most 128 columns hold their S in registers between the passes.
 #ifndef PA_PREFILL_REGROW
 #define PA_PREFILL_REGROW 1
@@ -176,6 +204,7 @@ struct PrefillTcCfg {
 };
 
 template <typename T> struct TcType;
+template <int V> struct IntTag { static constexpr int value = V; };
 template <> struct TcType<__nv_bfloat16> { static constexpr int code = 1; };
 template <> struct TcType<__half> { static constexpr int code = 0; };
 
@@ -464,12 +493,21 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     const int pos_first = L - n + tok0;   // position of the CTA's first chunk token
     const int kv_end = pos_first + ntok;  // cache tokens any row of the CTA sees
     const int ntiles = (kv_end + N - 1) / N;
-    // The CTAs of one (sequence, KV head) start their walk over the context
-    // at different tiles: run in lockstep from tile 0 they would all ask the
-    // same L2 lines at once.  The online softmax does not depend on the order.
-    const int rot = static_cast<int>((static_cast<unsigned>(qt) * 37u) % static_cast<unsigned>(ntiles));
+    // Where the CTAs of one (sequence, KV head) start their walk over the
+    // context (PA_PREFILL_ROT_STEP_*).  The online softmax does not depend on
+    // the order.
+    const int rot = static_cast<int>(gridDim.x) >= PA_PREFILL_ROT_MIN_CTAS
+                        ? static_cast<int>((static_cast<unsigned>(qt) *
+                                            (D <= 64 ? PA_PREFILL_ROT_STEP_D64 : PA_PREFILL_ROT_STEP_D128)) %
+                                           static_cast<unsigned>(ntiles))
+                        : 0;
     const int rows_used = g * ntok;
     const int nq = NQ > 1 && rows_used > 128 ? 2 : 1;   // Q tiles with any row to compute
+    // A CTA whose rows fit one Q tile (at most 128) gives that tile the idle
+    // tile's tensor memory as a second S buffer, at column kTileCols, so the
+    // tile's next QK runs under its softmax instead of after its PV.
+    constexpr bool kCanDual = PA_PREFILL_DUAL && C::kSBufs == 1 && NQ == 2;
+    const bool dual = kCanDual && nq == 1 && static_cast<int>(gridDim.x) <= PA_PREFILL_DUAL_MAX_CTAS;
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmQ);
@@ -671,70 +709,86 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             ok = ok && __all_sync(kAll, mbar_wait_cycles(bar, parity));
             return ok;
         };
-        // S_j = Q_t K_j^T into S buffer j % SB; the last Q tile's QK frees the K stage
-        auto issue_qk = [&](int t, int j) {
-            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
-            const uint32_t tcol = tmem + t * C::kTileCols;
-            const uint32_t kst = kstage0 + (j % NK) * C::kTileBytes;
-            const uint32_t qst = q_smem + t * C::kQTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                tc05::mma_ss_elect(
-                    tcol + (j % SB) * N,
-                    tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
-                    tc05::sw128_desc(kst + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kPieces * 1024),
-                    idesc_qk, kk > 0 ? 1u : 0u);
-            tc05::commit_elect(tb + (j % SB) * 8);   // s_full
-            if (t == nq - 1) tc05::commit_elect(k_empty + (j % NK) * 8);
-        };
-        // O_t += P_j V_j over the K-steps [kt0, kt1) (16 tokens each); the end of
-        // the last Q tile's PV frees the V stage
-        auto issue_pv = [&](int t, int j, int kt0, int kt1) {
-            const uint32_t tb = tile_bars + t * C::kTileBarBytes;
-            const uint32_t tcol = tmem + t * C::kTileCols;
-            const uint32_t vst = vstage0 + (j % NV) * C::kTileBytes;
-#pragma unroll
-            for (int kt = kt0; kt < kt1; ++kt)
-                // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
-                // whose P occupies the first half of its own S columns
-                tc05::mma_ts_elect(tcol + C::kOCol,
-                                   tcol + (j % SB) * N +
-                                       ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
-                                   tc05::sw128_desc(vst + kt * C::kBoxBytes, 1024, C::kPieces * 1024),
-                                   idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
-            if (kt1 < N / 16) return;
-            // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
-            // tracks this PV as well, so none is needed
-            if (SB > 1) tc05::commit_elect(tb + 32 + (j % SB) * 8);
-            if (t == nq - 1) tc05::commit_elect(v_empty + (j % NV) * 8);
-            if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
-        };
-        for (int j = 0; ok && j < SB && j < ntiles; ++j) {
-            if (!wait(k_full + (j % NK) * 8, (j / NK) & 1u)) break;
-            tc05::fence_after_sync();
-            for (int t = 0; t < nq; ++t) issue_qk(t, j);
-        }
-        for (int j = 0; ok && j < ntiles; ++j) {
-            if (!wait(v_full + (j % NV) * 8, (j / NV) & 1u)) break;
-            const int jn = j + SB;   // the QK issued behind this tile's PV
-            for (int t = 0; t < nq; ++t) {
+        // the issue sequence for SBX S buffers per Q tile (S buffer b at column b * SC)
+        auto run = [&](auto sbt) {
+            constexpr int SBX = decltype(sbt)::value;
+            constexpr int SC = SBX == C::kSBufs ? N : C::kTileCols;
+            // S_j = Q_t K_j^T into S buffer j % SBX; the last Q tile's QK frees the K stage
+            auto issue_qk = [&](int t, int j) {
                 const uint32_t tb = tile_bars + t * C::kTileBarBytes;
-                int kt0 = 0;
-                if (C::kHalfP) {   // the PV of the first N / 2 tokens once their P is in
-                    if (!wait(tb + 56, j & 1u)) break;   // p_half
-                    tc05::fence_after_sync();
-                    issue_pv(t, j, 0, N / 32);
-                    kt0 = N / 32;
-                }
-                if (!wait(tb + 16 + (j % SB) * 8, (j / SB) & 1u)) break;   // p_full
+                const uint32_t tcol = tmem + t * C::kTileCols;
+                const uint32_t kst = kstage0 + (j % NK) * C::kTileBytes;
+                const uint32_t qst = q_smem + t * C::kQTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc05::mma_ss_elect(
+                        tcol + (j % SBX) * SC,
+                        tc05::sw128_desc(qst + (kk >> 2) * C::kQPiece + (kk & 3) * 32, 16, 1024),
+                        tc05::sw128_desc(kst + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kPieces * 1024),
+                        idesc_qk, kk > 0 ? 1u : 0u);
+                tc05::commit_elect(tb + (j % SBX) * 8);   // s_full
+                if (t == nq - 1) tc05::commit_elect(k_empty + (j % NK) * 8);
+            };
+            // O_t += P_j V_j over the K-steps [kt0, kt1) (16 tokens each); the end of
+            // the last Q tile's PV frees the V stage
+            auto issue_pv = [&](int t, int j, int kt0, int kt1) {
+                const uint32_t tb = tile_bars + t * C::kTileBarBytes;
+                const uint32_t tcol = tmem + t * C::kTileCols;
+                const uint32_t vst = vstage0 + (j % NV) * C::kTileBytes;
+#pragma unroll
+                for (int kt = kt0; kt < kt1; ++kt)
+                    // tokens [16 kt, 16 kt + 16) lie in part (16 kt) / kHalfCols,
+                    // whose P occupies the first half of its own S columns
+                    tc05::mma_ts_elect(tcol + C::kOCol,
+                                       tcol + (j % SBX) * SC +
+                                           ((16 * kt) / C::kHalfCols) * (C::kHalfCols / 2) + kt * 8,
+                                       tc05::sw128_desc(vst + kt * C::kBoxBytes, 1024, C::kPieces * 1024),
+                                       idesc_pv, (j > 0 || kt > 0) ? 1u : 0u);
+                if (kt1 < N / 16) return;
+                // s_free: with one S buffer the commit of the QK issued next (S_{j+1})
+                // tracks this PV as well, so none is needed
+                if (SBX > 1) tc05::commit_elect(tb + 32 + (j % SBX) * 8);
+                if (t == nq - 1) tc05::commit_elect(v_empty + (j % NV) * 8);
+                if (j == ntiles - 1) tc05::commit_elect(tb + 48);   // o_full
+            };
+            for (int j = 0; ok && j < SBX && j < ntiles; ++j) {
+                if (!wait(k_full + (j % NK) * 8, (j / NK) & 1u)) break;
                 tc05::fence_after_sync();
-                issue_pv(t, j, kt0, N / 16);
-                if (jn < ntiles) {
-                    if (t == 0 && !wait(k_full + (jn % NK) * 8, (jn / NK) & 1u)) break;
+                for (int t = 0; t < nq; ++t) issue_qk(t, j);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                if (!wait(v_full + (j % NV) * 8, (j / NV) & 1u)) break;
+                const int jn = j + SBX;   // the QK issued behind this tile's PV
+                for (int t = 0; t < nq; ++t) {
+                    const uint32_t tb = tile_bars + t * C::kTileBarBytes;
+                    int kt0 = 0;
+                    // the PV of the first N / 2 tokens once their P is in (one S buffer
+                    // only: p_half is one barrier per tile, which a second buffer's
+                    // softmax could complete twice before this wait)
+                    if (C::kHalfP && SBX == 1) {
+                        if (!wait(tb + 56, j & 1u)) break;   // p_half
+                        tc05::fence_after_sync();
+                        issue_pv(t, j, 0, N / 32);
+                        kt0 = N / 32;
+                    }
+                    if (!wait(tb + 16 + (j % SBX) * 8, (j / SBX) & 1u)) break;   // p_full
                     tc05::fence_after_sync();
-                    issue_qk(t, jn);
+                    issue_pv(t, j, kt0, N / 16);
+                    if (jn < ntiles) {
+                        if (t == 0 && !wait(k_full + (jn % NK) * 8, (jn / NK) & 1u)) break;
+                        tc05::fence_after_sync();
+                        issue_qk(t, jn);
+                    }
                 }
             }
+        };
+        if constexpr (kCanDual) {
+            if (dual)
+                run(IntTag<2>{});
+            else
+                run(IntTag<C::kSBufs>{});
+        } else {
+            run(IntTag<C::kSBufs>{});
         }
         if (!ok && lane == 0) atomicOr(p.status, kWaitTimeout);
         // every MMA issued has completed before tensor memory is freed
@@ -769,85 +823,97 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
             const float sl2 = p.scale_log2;
             float m = -INFINITY, l = 0.f;   // l: this part's share of the row sum
             bool ok = true;
-            for (int j = 0; j < ntiles; ++j) {
-                const int b = j % SB;
-                const bool w = mbar_wait_cycles(tb + b * 8, (j / SB) & 1u);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    break;
-                }
-                tc05::fence_after_sync();
-                const uint32_t sb = tcol + b * N + hf * HC;   // this part's S columns
-                const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
-                const int lim = pos - jt * N - hf * HC;   // own columns c <= lim are visible
-                // pass 1: this part's row max (with two parts, swapped with the other's)
-                const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
-                uint32_t sr[RC][32];
-                float pm;
-                if constexpr (RR)
-                    pm = full ? row_load_max<N, false>(sr, sb, lim) : row_load_max<N, true>(sr, sb, lim);
-                else
-                    pm = full ? tile_row_max<HC, false, PK>(sb, lim)
-                              : tile_row_max<HC, true, PK>(sb, lim);
-                float mt = pm;
-                if constexpr (SP > 1) {
-                    xch[(j & 1) * 256 + hf * 128 + rl] = pm;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
+            auto tiles = [&](auto sbt) {
+                constexpr int SBX = decltype(sbt)::value;
+                constexpr int SC = SBX == C::kSBufs ? N : C::kTileCols;
+                for (int j = 0; j < ntiles; ++j) {
+                    const int b = j % SBX;
+                    const bool w = mbar_wait_cycles(tb + b * 8, (j / SBX) & 1u);
+                    if (!__all_sync(0xffffffffu, w)) {
                         ok = false;
                         break;
                     }
-                    mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
-                }
-                mt *= sl2;   // log2 domain (scale > 0)
-                if (j == 0) {
-                    m = mt;   // -inf when every column of the first tile is past the row
-                } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
-                    // O must hold P_{j-1} V_{j-1} before it is rescaled (all parts
-                    // see the same maxima, so all take this branch for a row).  With
-                    // one S buffer, PV_{j-1} went out before QK_j from the same thread,
-                    // so the S_j commit waited for above has already seen it finish.
-                    if (SB > 1) {
-                        const bool w2 =
-                            mbar_wait_cycles(tb + 32 + ((j - 1) % SB) * 8, ((j - 1) / SB) & 1u);
-                        if (!__all_sync(0xffffffffu, w2)) {
+                    tc05::fence_after_sync();
+                    const uint32_t sb = tcol + b * SC + hf * HC;   // this part's S columns
+                    const int jt = j + rot < ntiles ? j + rot : j + rot - ntiles;
+                    const int lim = pos - jt * N - hf * HC;   // own columns c <= lim are visible
+                    // pass 1: this part's row max (with two parts, swapped with the other's)
+                    const bool full = __all_sync(0xffffffffu, lim >= HC - 1);
+                    uint32_t sr[RC][32];
+                    float pm;
+                    if constexpr (RR)
+                        pm = full ? row_load_max<N, false>(sr, sb, lim) : row_load_max<N, true>(sr, sb, lim);
+                    else
+                        pm = full ? tile_row_max<HC, false, PK>(sb, lim)
+                                  : tile_row_max<HC, true, PK>(sb, lim);
+                    float mt = pm;
+                    if constexpr (SP > 1) {
+                        xch[(j & 1) * 256 + hf * 128 + rl] = pm;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cta(xbar + (j & 1) * 8);
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait_cycles(xbar + (j & 1) * 8, (j >> 1) & 1u))) {
                             ok = false;
                             break;
                         }
-                        tc05::fence_after_sync();
+                        mt = fmaxf(pm, xch[(j & 1) * 256 + (1 - hf) * 128 + rl]);
                     }
-                    const float mn = fmaxf(m, mt);
-                    const float alpha = m == mn ? 1.f : ex2(m - mn);   // 0 when m was -inf
-                    m = mn;
-                    l *= alpha;
-                    // this part's O columns, 16 at a time while the S row is held
-                    constexpr int OC = RR ? 16 : 32;
+                    mt *= sl2;   // log2 domain (scale > 0)
+                    if (j == 0) {
+                        m = mt;   // -inf when every column of the first tile is past the row
+                    } else if (__any_sync(0xffffffffu, mt > m + 8.f)) {
+                        // O must hold P_{j-1} V_{j-1} before it is rescaled (all parts
+                        // see the same maxima, so all take this branch for a row).  With
+                        // one S buffer, PV_{j-1} went out before QK_j from the same thread,
+                        // so the S_j commit waited for above has already seen it finish.
+                        if (SBX > 1) {
+                            const bool w2 =
+                                mbar_wait_cycles(tb + 32 + ((j - 1) % SBX) * 8, ((j - 1) / SBX) & 1u);
+                            if (!__all_sync(0xffffffffu, w2)) {
+                                ok = false;
+                                break;
+                            }
+                            tc05::fence_after_sync();
+                        }
+                        const float mn = fmaxf(m, mt);
+                        const float alpha = m == mn ? 1.f : ex2(m - mn);   // 0 when m was -inf
+                        m = mn;
+                        l *= alpha;
+                        // this part's O columns, 16 at a time while the S row is held
+                        constexpr int OC = RR ? 16 : 32;
 #pragma unroll
-                    for (int c0 = 0; c0 < D / SP; c0 += OC) {
-                        uint32_t rr[OC];
-                        const uint32_t oc = tcol + C::kOCol + hf * (D / SP) + c0;
-                        if constexpr (RR) tc05::ld16(oc, rr); else tc05::ld32(oc, rr);
+                        for (int c0 = 0; c0 < D / SP; c0 += OC) {
+                            uint32_t rr[OC];
+                            const uint32_t oc = tcol + C::kOCol + hf * (D / SP) + c0;
+                            if constexpr (RR) tc05::ld16(oc, rr); else tc05::ld32(oc, rr);
 #pragma unroll
-                        for (int i = 0; i < OC; ++i)
-                            rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                        if constexpr (RR) tc05::st16(oc, rr); else tc05::st32(oc, rr);
+                            for (int i = 0; i < OC; ++i)
+                                rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                            if constexpr (RR) tc05::st16(oc, rr); else tc05::st32(oc, rr);
+                        }
                     }
+                    // pass 2: P of this part over the first half of its own S columns
+                    const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
+                    const uint32_t hb = C::kHalfP && SBX == 1 ? tb + 56 : 0u;   // p_half
+                    if constexpr (RR)
+                        l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu, hb, lane == 0)
+                                  : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu, hb, lane == 0);
+                    else
+                        l += full ? tile_row_p<T, HC, false, PK>(sb, lim, sl2, mu, hb, lane == 0)
+                                  : tile_row_p<T, HC, true, PK>(sb, lim, sl2, mu, hb, lane == 0);
+                    tc05::wait_st();
+                    tc05::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(tb + 16 + b * 8);   // p_full
                 }
-                // pass 2: P of this part over the first half of its own S columns
-                const float mu = m == -INFINITY ? 0.f : m;   // no column seen yet: P = 0
-                const uint32_t hb = C::kHalfP ? tb + 56 : 0u;   // p_half
-                if constexpr (RR)
-                    l += full ? row_p_regs<T, N, false>(sr, sb, lim, sl2, mu, hb, lane == 0)
-                              : row_p_regs<T, N, true>(sr, sb, lim, sl2, mu, hb, lane == 0);
+            };
+            if constexpr (kCanDual) {
+                if (dual)
+                    tiles(IntTag<2>{});
                 else
-                    l += full ? tile_row_p<T, HC, false, PK>(sb, lim, sl2, mu, hb, lane == 0)
-                              : tile_row_p<T, HC, true, PK>(sb, lim, sl2, mu, hb, lane == 0);
-                tc05::wait_st();
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cta(tb + 16 + b * 8);   // p_full
+                    tiles(IntTag<C::kSBufs>{});
+            } else {
+                tiles(IntTag<C::kSBufs>{});
             }
             if (SP > 1 && ok) {   // the row sum is the two parts' shares
                 xch[2 * 256 + hf * 128 + rl] = l;

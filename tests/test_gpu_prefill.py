@@ -322,6 +322,25 @@ def test_prefill_running_max_rescales(pa, D, rate, spike):
     assert_out_close(out, _oracle(host), f"rescaled prefill D={D} rate={rate} spike={spike}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("keys", ["random", "ramp", "spike"])
+def test_one_tile_ctas_with_a_second_s_buffer(pa, D, keys):
+    """One query head per KV head and chunks of at most 128 rows: each (sequence,
+    KV head) has one CTA with one Q tile, which takes the other tile's tensor
+    memory as a second S buffer (its next QK runs under its softmax, and an O
+    rescale waits for the PV before it).  Keys that raise the row max every tile
+    (ramp) or once (spike) exercise that wait; every row is checked."""
+    w = _workload(8, 8, D, 16, torch.bfloat16)
+    host = make_prefill_case(w, ctx_lens=[2000, 0, 700], q_lens=[128, 100, 1], seed=3800 + D)
+    if keys == "ramp":
+        _ramped_keys(host, 12.0, seed=3810 + D)
+    elif keys == "spike":
+        _ramped_keys(host, 0.5, seed=3820 + D, spike=(1200, 60.0))
+    out = _run(pa, host.to("cuda"))
+    assert pa.device_status() == 0
+    assert_out_close(out, _oracle(host), f"one-tile CTAs, head_dim {D}, {keys} keys")
+
+
 @pytest.mark.parametrize("D,Hq,Hkv,bs", [(64, 32, 4, 16), (128, 24, 4, 48), (256, 16, 2, 32),
                                          (128, 24, 4, 8), (256, 16, 2, 8)])
 def test_repeated_launches_are_bit_identical(pa, D, Hq, Hkv, bs):
