@@ -134,3 +134,13 @@ def test_prefill_sweep_flops_and_table():
     lines = ps.table(rows).splitlines()
     assert len(lines) == 2 + 2
     assert all(line.count("|") == 3 + 2 + 1 for line in lines)
+
+
+def test_sustained_bf16_peak_is_read_when_present(monkeypatch, tmp_path):
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1900.0,
+                                                             "bf16_tflops_sustained": 1700.0}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_bf16_sustained() == 1700.0
+    assert bench.measured_bf16_peak()[0] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1900.0}))
+    assert bench.measured_bf16_sustained() is None
